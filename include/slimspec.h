@@ -1,0 +1,169 @@
+/*
+ * slimspec.h -- C ABI of the GB300 (sm_103a) drafter-head and verifier library.
+ *
+ * Sources named below (article title, section):
+ *   [SlimSpec]  荷兰Nebius团队：给AI“起草员“瘦身，大模型推理速度提升5倍 (mhpn.cn)
+ *   [SpecVocab] 动态词汇推测加速大语言模型推理 (2kiu.com)
+ *   [Explainer] 大模型批改 5 个词，和自己写 1 个词一样快：投机解码讲人话 (liuchunshan.com)
+ *   [SpecTr-GBV] SpecTr-GBV: Multi-Draft Block Verification (hypresin.com)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  * Every tensor pointer is DEVICE memory owned by the caller; row-major,
+ *    contiguous, 16-byte aligned.  The library never allocates or frees
+ *    memory and never synchronises the stream inside a forward call.
+ *  * Calls are asynchronous on `stream` (NULL = the legacy default stream).
+ *    A call returns SS_OK once its kernels are enqueued.  Argument errors are
+ *    detected on the host before anything is launched and nothing is written.
+ *    A failed launch returns SS_ERR_CUDA.
+ *  * `workspace` is caller-owned device scratch of at least the size the
+ *    matching *_workspace_size() reports (256-byte aligned).  Its contents on
+ *    entry do not matter; two calls in flight at once need two workspaces.
+ *  * Sampling draws use caller-supplied uniforms in [0, 1) (one per draw, see
+ *    each call).  Temperature 0 means greedy and the uniforms are not read.
+ *  * Ties in every argmax, top-k and inverse-CDF go to the lowest vocabulary
+ *    index.  Results are deterministic: the same inputs give the same bits.
+ *  * Device-side anomalies (a draft token outside [0, V), a bounded wait that
+ *    ran out) are recorded in a per-device error word; ss_get_device_error()
+ *    reads and clears it.
+ */
+#ifndef SLIMSPEC_H_
+#define SLIMSPEC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SS_OK = 0,
+  SS_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size or value   */
+  SS_ERR_UNSUPPORTED = 2,   /* valid request this build has no kernel for     */
+  SS_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small     */
+  SS_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed    */
+  SS_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out             */
+  SS_ERR_DEVICE_INDEX = 6   /* a device-side index input was out of range     */
+} ss_status;
+
+typedef enum { SS_F32 = 0, SS_BF16 = 1 } ss_dtype;
+
+/* Human-readable name of a status code; never NULL. */
+const char* ss_status_string(int status);
+
+/* Library ABI version (major * 100 + minor). */
+int ss_version(void);
+
+/* Reads and clears the device error word of the current device after
+ * synchronising `stream`.  Returns SS_OK, SS_ERR_TIMEOUT, SS_ERR_DEVICE_INDEX
+ * or SS_ERR_CUDA. */
+int ss_get_device_error(cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * SlimSpec low-rank drafter head, fused with its per-row reduction.
+ *
+ * [SlimSpec] section 三: W_down maps the d-wide hidden state to an r-wide
+ * summary, W_up maps the summary to scores over all V vocabulary entries;
+ * cost O(r*d + V*r) instead of O(V*d).  Computes, per row m:
+ *   z[m]      = h[m] . W_down^T                 (fp32 accumulate; rounded to
+ *                                                nearest-even bf16 when dtype
+ *                                                is SS_BF16)
+ *   l[m, v]   = z[m] . W_up[v]^T   for v < V    (fp32 accumulate)
+ *   greedy (temperature == 0): token = lowest v attaining max_v l[m, v]
+ *   sampling (temperature > 0): w_v = exp((l[m,v] - max)/T); token = smallest
+ *     v whose ascending-order partial sum of w exceeds uniforms[m] * sum_v w_v
+ * The M x V logits are reduced on chip and never written unless out_logits
+ * is given (debug).
+ *
+ *  hidden      M x d      dtype         w_down  r x d   dtype
+ *  w_up        V x r      dtype
+ *  M >= 0 (0 is a no-op), d % 8 == 0, r % 8 == 0, 8 <= r <= 1024 (bf16) or
+ *  4 <= r <= 512 with r % 4 == 0 (f32), V >= 1
+ *  temperature >= 0 and finite; uniforms: M floats in [0,1) (T > 0), else
+ *  may be NULL.
+ *  out_tokens  M int32 (required)
+ *  out_logprob M float   log softmax(l/T)[token]; 0 when greedy   (nullable)
+ *  out_row_max M float   max_v l[m, v]                           (nullable)
+ *  out_row_lse M float   log sum_v exp(l[m,v]/T); the max when greedy (nullable)
+ *  out_z       M x r dtype, the rounded intermediate              (nullable)
+ *  out_logits  M x V float32 (debug; slows the call)              (nullable)
+ * ------------------------------------------------------------------------ */
+size_t slimspec_head_workspace_size(int M, int d, int r, int V, int dtype);
+
+int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_up,
+                          int M, int d, int r, int V, int dtype, float temperature,
+                          const float* uniforms, int32_t* out_tokens,
+                          float* out_logprob, float* out_row_max, float* out_row_lse,
+                          void* out_z, float* out_logits, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * SpecVocab-style dynamic-vocabulary drafter head (bf16 only).
+ *
+ * [SpecVocab] sections 2.2.1-2.2.3:
+ *   h'[m] = bf16( h[m] . W_down^T )       d' = d/16 in the write-up
+ *   s[m]  = h'[m] . W_vocab^T             approximate scores over all V
+ *   K[m]  = the k largest s[m, v] (ties to the lowest v), ascending id order
+ *   z'[m, j] = U[K[m, j]] . h[m]          exact logits of the candidates
+ *   q[m]  = softmax(z'[m] / T); token = K[m, j*] with j* the greedy argmax
+ *           (T == 0) or the inverse-CDF draw with uniforms[m] over the
+ *           candidates in ascending id order.
+ *  hidden M x d, w_down d' x d, w_vocab V x d', u_full V x d (all bf16)
+ *  d % 8 == 0, d' % 8 == 0, d' <= 1024, d <= 8192, 1 <= k <= min(V, 4096)
+ *  out_tokens    M int32 (required)
+ *  out_topk_idx  M x k int32 candidate ids, ascending            (nullable)
+ *  out_topk_prob M x k float q over the candidates (T > 0)       (nullable)
+ *  out_scores    M x V float approximate scores (debug)          (nullable)
+ * ------------------------------------------------------------------------ */
+size_t specvocab_head_workspace_size(int M, int d, int d_prime, int V, int k);
+
+int specvocab_head_forward(const void* hidden, const void* w_down, const void* w_vocab,
+                           const void* u_full, int M, int d, int d_prime, int V, int k,
+                           float temperature, const float* uniforms,
+                           int32_t* out_tokens, int32_t* out_topk_idx,
+                           float* out_topk_prob, float* out_scores, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/* The top-k stage of the SpecVocab head on its own ([SpecVocab] section
+ * 2.2.2): for each of M rows of V float32 scores, the k largest, ties to the
+ * lowest index, written in ascending index order to out_idx (M x k int32).
+ * -0.0 and +0.0 compare equal; scores must not be NaN. */
+size_t ss_topk_workspace_size(int M, int V, int k);
+
+int ss_topk_rows(const float* scores, int M, int V, int k, int32_t* out_idx,
+                 void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Speculative verification of B sequences with gamma drafted tokens each.
+ *
+ * [Explainer] sections "小模型起草，大模型批改" and "为什么答案不会变";
+ * [SpecTr-GBV] 第三步.  With p_j = softmax(target[b, j] / T) and
+ * q_j = softmax(draft[b, j] / T):
+ *   greedy (T == 0): a_j = lowest-index argmax of target[b, j]; n = first j
+ *     with x_j != a_j (else gamma); emit x_0..x_{n-1}, a_n.
+ *   sampling (T > 0): position j keeps x_j iff u[b,j] * q_j(x_j) < p_j(x_j);
+ *     at the first rejection n the token is the inverse-CDF draw with
+ *     u[b, gamma] from max(0, p_n - q_n) (from p_n if that is all zero); if all
+ *     gamma are kept, the bonus token is drawn from p_gamma with u[b, gamma].
+ *  target_logits B x (gamma+1) x V float32
+ *  draft_logits  B x gamma x V float32 (may be NULL when T == 0)
+ *  draft_tokens  B x gamma int32, each in [0, V) (checked on the device)
+ *  uniforms      B x (gamma+1) floats in [0,1) (T > 0), else may be NULL
+ *  1 <= gamma <= 32, V >= 1, B >= 0
+ *  out_tokens    B x (gamma+1) int32: the n+1 emitted tokens, then -1
+ *  out_num_accepted B int32: n
+ * ------------------------------------------------------------------------ */
+size_t spec_verify_workspace_size(int B, int gamma, int V, float temperature);
+
+int spec_verify(const float* target_logits, const float* draft_logits,
+                const int32_t* draft_tokens, int B, int gamma, int V,
+                float temperature, const float* uniforms, int32_t* out_tokens,
+                int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SLIMSPEC_H_ */

@@ -1,0 +1,249 @@
+"""GB300 (sm_103a) drafter head and speculative verifier.
+
+A thin ctypes binding over ``libslimspec.so`` (C ABI in ``include/slimspec.h``).
+Every step of the computation runs in the library's CUDA kernels; this module
+only checks tensors, allocates outputs and workspace with PyTorch and passes
+raw device pointers plus the current CUDA stream.  There is no CPU path: if
+the library is missing or a tensor is not on a CUDA device, the call raises.
+
+Public calls (same names as the C ABI):
+    slimspec_head_forward   SlimSpec low-rank head + per-row reduction
+    specvocab_head_forward  SpecVocab-style dynamic-vocabulary head
+    ss_topk_rows            the top-k stage on its own
+    spec_verify             greedy / sampling verification
+    ss_get_device_error     device error word (synchronises the stream)
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+__all__ = [
+    "SS_OK", "SS_ERR_INVALID_ARG", "SS_ERR_UNSUPPORTED", "SS_ERR_WORKSPACE",
+    "SS_ERR_CUDA", "SS_ERR_TIMEOUT", "SS_ERR_DEVICE_INDEX", "SlimspecError",
+    "lib", "lib_path", "header_functions", "slimspec_head_forward",
+    "specvocab_head_forward", "ss_topk_rows", "spec_verify", "ss_get_device_error",
+    "slimspec_head_workspace_size", "specvocab_head_workspace_size",
+    "spec_verify_workspace_size", "ss_topk_workspace_size",
+]
+
+SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE = 0, 1, 2, 3
+SS_ERR_CUDA, SS_ERR_TIMEOUT, SS_ERR_DEVICE_INDEX = 4, 5, 6
+SS_F32, SS_BF16 = 0, 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_HEADER = os.path.join(os.path.dirname(_HERE), "include", "slimspec.h")
+_LIB = None
+
+_vp, _i, _f, _sz, _u64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t, ctypes.c_uint64
+_SIGS = {
+    "ss_status_string": (ctypes.c_char_p, [_i]),
+    "ss_version": (_i, []),
+    "ss_get_device_error": (_i, [_vp]),
+    "slimspec_head_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "slimspec_head_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp,
+                                   _vp, _vp, _vp, _vp, _sz, _vp]),
+    "specvocab_head_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "specvocab_head_forward": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp,
+                                    _vp, _vp, _vp, _sz, _vp]),
+    "ss_topk_workspace_size": (_sz, [_i, _i, _i]),
+    "ss_topk_rows": (_i, [_vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
+    "spec_verify_workspace_size": (_sz, [_i, _i, _i, _f]),
+    "spec_verify": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _sz, _vp]),
+}
+
+
+class SlimspecError(RuntimeError):
+    """A non-zero ss_status returned by the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {lib().ss_status_string(status).decode()}")
+
+
+def lib_path() -> str:
+    return os.path.join(_HERE, "libslimspec.so")
+
+
+def header_functions() -> list:
+    """Names of the functions declared in include/slimspec.h."""
+    src = open(_HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(?:int|size_t|const char\*)\s+(\w+)\s*\(", src)))
+
+
+def lib() -> ctypes.CDLL:
+    """Loads libslimspec.so (built by ``_build.build()``); raises if absent."""
+    global _LIB
+    if _LIB is None:
+        path = lib_path()
+        if not os.path.exists(path):
+            raise RuntimeError(
+                "libslimspec.so is not built; run "
+                "`python -c 'import __graft_entry__ as g; g.build()'` first")
+        l = ctypes.CDLL(path)
+        for name, (res, args) in _SIGS.items():
+            fn = getattr(l, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = l
+    return _LIB
+
+
+# ------------------------------------------------------------------ helpers --
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SS_BF16
+    if t.dtype == torch.float32:
+        return SS_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensor must live on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("tensor must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != SS_OK:
+        raise SlimspecError(status, where)
+
+
+def _workspace(nbytes: int, device, workspace):
+    if workspace is not None:
+        if workspace.numel() * workspace.element_size() < nbytes:
+            raise ValueError("workspace too small")
+        return workspace
+    return torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+
+
+def slimspec_head_workspace_size(M, d, r, V, dtype_code) -> int:
+    return int(lib().slimspec_head_workspace_size(M, d, r, V, dtype_code))
+
+
+def specvocab_head_workspace_size(M, d, d_prime, V, k) -> int:
+    return int(lib().specvocab_head_workspace_size(M, d, d_prime, V, k))
+
+
+def spec_verify_workspace_size(B, gamma, V, temperature) -> int:
+    return int(lib().spec_verify_workspace_size(B, gamma, V, float(temperature)))
+
+
+def ss_topk_workspace_size(M, V, k) -> int:
+    return int(lib().ss_topk_workspace_size(M, V, k))
+
+
+# -------------------------------------------------------------- entry points --
+def slimspec_head_forward(hidden, w_down, w_up, temperature=0.0, uniforms=None, *,
+                          want_stats=True, want_z=False, want_logits=False,
+                          workspace=None, out=None, stream=None) -> dict:
+    """Low-rank head h -> h W_down^T -> . W_up^T fused with the row reduction.
+
+    hidden (M, d), w_down (r, d), w_up (V, r): same dtype (bf16 or fp32), CUDA.
+    Returns a dict with 'tokens' (M int32) and, as requested, 'logprob',
+    'row_max', 'lse' (M float32), 'z' (M, r) and 'logits' (M, V float32).
+    ``out`` may supply preallocated output tensors under the same keys.
+    """
+    M, d = hidden.shape
+    r, d2 = w_down.shape
+    V, r2 = w_up.shape
+    if d2 != d or r2 != r or w_down.dtype != hidden.dtype or w_up.dtype != hidden.dtype:
+        raise ValueError("shape or dtype mismatch")
+    code = _dtype_code(hidden)
+    dev = hidden.device
+    o = dict(out or {})
+    o.setdefault("tokens", torch.empty(M, dtype=torch.int32, device=dev))
+    if want_stats:
+        for k in ("logprob", "row_max", "lse"):
+            o.setdefault(k, torch.empty(M, dtype=torch.float32, device=dev))
+    if want_z:
+        o.setdefault("z", torch.empty(M, r, dtype=hidden.dtype, device=dev))
+    if want_logits:
+        o.setdefault("logits", torch.empty(M, V, dtype=torch.float32, device=dev))
+    nbytes = slimspec_head_workspace_size(M, d, r, V, code)
+    ws = _workspace(nbytes, dev, workspace)
+    st = lib().slimspec_head_forward(
+        _ptr(hidden), _ptr(w_down), _ptr(w_up), M, d, r, V, code, float(temperature),
+        _ptr(uniforms), _ptr(o["tokens"]), _ptr(o.get("logprob")), _ptr(o.get("row_max")),
+        _ptr(o.get("lse")), _ptr(o.get("z")), _ptr(o.get("logits")), _ptr(ws), ws.numel(),
+        _stream(stream))
+    _check(st, "slimspec_head_forward")
+    return o
+
+
+def specvocab_head_forward(hidden, w_down, w_vocab, u_full, k, temperature=0.0, uniforms=None,
+                           *, want_topk=True, want_prob=False, want_scores=False,
+                           workspace=None, out=None, stream=None) -> dict:
+    """SpecVocab head: router scores, top-k, exact candidate logits, draw (bf16)."""
+    M, d = hidden.shape
+    dp, d2 = w_down.shape
+    V, dp2 = w_vocab.shape
+    V2, d3 = u_full.shape
+    if d2 != d or dp2 != dp or V2 != V or d3 != d:
+        raise ValueError("shape mismatch")
+    dev = hidden.device
+    o = dict(out or {})
+    o.setdefault("tokens", torch.empty(M, dtype=torch.int32, device=dev))
+    if want_topk:
+        o.setdefault("topk_idx", torch.empty(M, k, dtype=torch.int32, device=dev))
+    if want_prob:
+        o.setdefault("topk_prob", torch.empty(M, k, dtype=torch.float32, device=dev))
+    if want_scores:
+        o.setdefault("scores", torch.empty(M, V, dtype=torch.float32, device=dev))
+    nbytes = specvocab_head_workspace_size(M, d, dp, V, k)
+    ws = _workspace(nbytes, dev, workspace)
+    st = lib().specvocab_head_forward(
+        _ptr(hidden), _ptr(w_down), _ptr(w_vocab), _ptr(u_full), M, d, dp, V, k,
+        float(temperature), _ptr(uniforms), _ptr(o["tokens"]), _ptr(o.get("topk_idx")),
+        _ptr(o.get("topk_prob")), _ptr(o.get("scores")), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "specvocab_head_forward")
+    return o
+
+
+def ss_topk_rows(scores, k, *, out=None, stream=None):
+    """Top-k ids (ascending, ties to the lowest id) of each row of fp32 scores."""
+    M, V = scores.shape
+    o = out if out is not None else torch.empty(M, k, dtype=torch.int32, device=scores.device)
+    nbytes = ss_topk_workspace_size(M, V, k)
+    ws = _workspace(nbytes, scores.device, None)
+    st = lib().ss_topk_rows(_ptr(scores), M, V, k, _ptr(o), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "ss_topk_rows")
+    return o
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, temperature=0.0, uniforms=None, *,
+                workspace=None, out=None, stream=None) -> dict:
+    """Verification of B sequences: target (B, g+1, V), draft (B, g, V) fp32,
+    draft_tokens (B, g) int32, uniforms (B, g+1) fp32 when temperature > 0."""
+    B, g1, V = target_logits.shape
+    gamma = g1 - 1
+    dev = target_logits.device
+    o = dict(out or {})
+    o.setdefault("tokens", torch.empty(B, g1, dtype=torch.int32, device=dev))
+    o.setdefault("num_accepted", torch.empty(B, dtype=torch.int32, device=dev))
+    nbytes = spec_verify_workspace_size(B, gamma, V, temperature)
+    ws = _workspace(nbytes, dev, workspace)
+    st = lib().spec_verify(
+        _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, gamma, V,
+        float(temperature), _ptr(uniforms), _ptr(o["tokens"]), _ptr(o["num_accepted"]),
+        _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "spec_verify")
+    return o
+
+
+def ss_get_device_error(stream=None) -> int:
+    """Synchronises the stream, then reads and clears the device error word."""
+    return int(lib().ss_get_device_error(_stream(stream)))

@@ -1,0 +1,212 @@
+// api.cu -- the extern "C" boundary of libslimspec (declared in include/slimspec.h).
+//
+// Every entry point validates its arguments on the host before anything is
+// launched (nothing is written on an argument error), carves its workspace
+// and enqueues the kernels of head.cu / verify.cu / specvocab.cu on the
+// caller's stream.  No entry point allocates, frees or synchronises.
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/slimspec.h"
+#include "ss_common.cuh"
+#include "ss_internal.h"
+
+namespace ss {
+
+// Per-device error word (one instance per device the library is loaded on).
+__device__ unsigned int g_error_word = 0;
+
+unsigned* error_word() {
+  static unsigned* cached[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  if (cached[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    cached[dev] = static_cast<unsigned*>(p);
+  }
+  return cached[dev];
+}
+
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+static bool temp_ok(float t) { return isfinite(t) && t >= 0.f; }
+static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SS_OK : SS_ERR_CUDA; }
+
+static size_t head_ws_bytes(int M, int r, int V, bool bf16) {
+  const HeadPlan plan = head_plan(bf16, r, M, V);
+  if (!plan.ok) return 0;
+  size_t s = 0;
+  s += align256((size_t)M * r * sizeof(float));
+  s += 3 * align256((size_t)M * plan.n_sub * sizeof(float));
+  return s;
+}
+
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" {
+
+const char* ss_status_string(int status) {
+  switch (status) {
+    case SS_OK: return "SS_OK";
+    case SS_ERR_INVALID_ARG: return "SS_ERR_INVALID_ARG: invalid argument";
+    case SS_ERR_UNSUPPORTED: return "SS_ERR_UNSUPPORTED: no kernel for this shape";
+    case SS_ERR_WORKSPACE: return "SS_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case SS_ERR_CUDA: return "SS_ERR_CUDA: CUDA runtime error";
+    case SS_ERR_TIMEOUT: return "SS_ERR_TIMEOUT: a bounded device wait ran out";
+    case SS_ERR_DEVICE_INDEX: return "SS_ERR_DEVICE_INDEX: device-side index out of range";
+    default: return "unknown status";
+  }
+}
+
+int ss_version(void) { return 100; }
+
+int ss_get_device_error(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SS_ERR_CUDA;
+  unsigned v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) return SS_ERR_CUDA;
+  if (v != 0) {
+    const unsigned zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return SS_ERR_CUDA;
+  }
+  if (v & kErrTimeout) return SS_ERR_TIMEOUT;
+  if (v & kErrIndex) return SS_ERR_DEVICE_INDEX;
+  return SS_OK;
+}
+
+// ------------------------------------------------------------------- head --
+static int head_check(int M, int d, int r, int V, int dtype) {
+  if (M < 0 || d <= 0 || r <= 0 || V <= 0) return SS_ERR_INVALID_ARG;
+  if (dtype != SS_F32 && dtype != SS_BF16) return SS_ERR_INVALID_ARG;
+  const bool bf16 = dtype == SS_BF16;
+  if (d % 8 != 0 || r % (bf16 ? 8 : 4) != 0) return SS_ERR_INVALID_ARG;
+  if ((long long)V * r * (bf16 ? 2 : 4) >= (1LL << 40)) return SS_ERR_UNSUPPORTED;
+  if (!head_plan(bf16, r, M, V).ok) return SS_ERR_UNSUPPORTED;
+  return SS_OK;
+}
+
+size_t slimspec_head_workspace_size(int M, int d, int r, int V, int dtype) {
+  if (head_check(M, d, r, V, dtype) != SS_OK) return 0;
+  return head_ws_bytes(M, r, V, dtype == SS_BF16);
+}
+
+int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_up, int M, int d,
+                          int r, int V, int dtype, float temperature, const float* uniforms,
+                          int32_t* out_tokens, float* out_logprob, float* out_row_max,
+                          float* out_row_lse, void* out_z, float* out_logits, void* workspace,
+                          size_t workspace_bytes, cudaStream_t stream) {
+  int st = head_check(M, d, r, V, dtype);
+  if (st != SS_OK) return st;
+  if (!temp_ok(temperature)) return SS_ERR_INVALID_ARG;
+  if (M == 0) return SS_OK;
+  if (!hidden || !w_down || !w_up || !out_tokens) return SS_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(w_down, 16) || !aligned(w_up, 16)) return SS_ERR_INVALID_ARG;
+  if (!aligned(out_tokens, 4) || (out_logprob && !aligned(out_logprob, 4)) ||
+      (out_row_max && !aligned(out_row_max, 4)) || (out_row_lse && !aligned(out_row_lse, 4)) ||
+      (out_z && !aligned(out_z, 4)) || (out_logits && !aligned(out_logits, 4)))
+    return SS_ERR_INVALID_ARG;
+  if (temperature > 0.f && (!uniforms || !aligned(uniforms, 4))) return SS_ERR_INVALID_ARG;
+  const bool bf16 = dtype == SS_BF16;
+  const size_t need = head_ws_bytes(M, r, V, bf16);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return SS_ERR_WORKSPACE;
+
+  const HeadPlan plan = head_plan(bf16, r, M, V);
+  Carver cv(workspace);
+  float* z_ws = cv.take<float>((size_t)M * r);
+  HeadPartials part;
+  part.pmax = cv.take<float>((size_t)M * plan.n_sub);
+  part.psum = cv.take<float>((size_t)M * plan.n_sub);
+  part.parg = cv.take<int>((size_t)M * plan.n_sub);
+
+  cudaError_t e = launch_down_proj(bf16, hidden, w_down, M, d, r, bf16, z_ws, out_z, stream);
+  if (e == cudaSuccess)
+    e = launch_head_stream(plan, bf16, w_up, z_ws, M, r, V, temperature, part, out_logits, stream);
+  if (e == cudaSuccess)
+    e = launch_head_finish(plan, bf16, w_up, z_ws, M, r, V, temperature, part, uniforms,
+                           out_tokens, out_logprob, out_row_max, out_row_lse, stream);
+  return cuda_status(e);
+}
+
+// -------------------------------------------------------------- specvocab --
+static int sv_check(int M, int d, int d_prime, int V, int k) {
+  if (M < 0 || d <= 0 || d_prime <= 0 || V <= 0) return SS_ERR_INVALID_ARG;
+  if (d % 8 != 0 || d_prime % 8 != 0) return SS_ERR_INVALID_ARG;
+  if (k < 1 || k > V) return SS_ERR_INVALID_ARG;
+  if (d > 4096 || d_prime > 1024 || k > 4096) return SS_ERR_UNSUPPORTED;
+  if ((long long)V * d * 2 >= (1LL << 40)) return SS_ERR_UNSUPPORTED;
+  if (!head_plan(true, d_prime, M, V).ok) return SS_ERR_UNSUPPORTED;
+  return SS_OK;
+}
+
+size_t specvocab_head_workspace_size(int M, int d, int d_prime, int V, int k) {
+  if (sv_check(M, d, d_prime, V, k) != SS_OK) return 0;
+  return specvocab_ws_bytes(M, d, d_prime, V, k);
+}
+
+int specvocab_head_forward(const void* hidden, const void* w_down, const void* w_vocab,
+                           const void* u_full, int M, int d, int d_prime, int V, int k,
+                           float temperature, const float* uniforms, int32_t* out_tokens,
+                           int32_t* out_topk_idx, float* out_topk_prob, float* out_scores,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  int st = sv_check(M, d, d_prime, V, k);
+  if (st != SS_OK) return st;
+  if (!temp_ok(temperature)) return SS_ERR_INVALID_ARG;
+  if (M == 0) return SS_OK;
+  if (!hidden || !w_down || !w_vocab || !u_full || !out_tokens) return SS_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(w_down, 16) || !aligned(w_vocab, 16) || !aligned(u_full, 16))
+    return SS_ERR_INVALID_ARG;
+  if (!aligned(out_tokens, 4) || (out_topk_idx && !aligned(out_topk_idx, 4)) ||
+      (out_topk_prob && !aligned(out_topk_prob, 4)) || (out_scores && !aligned(out_scores, 4)))
+    return SS_ERR_INVALID_ARG;
+  if (temperature > 0.f && (!uniforms || !aligned(uniforms, 4))) return SS_ERR_INVALID_ARG;
+  const size_t need = specvocab_ws_bytes(M, d, d_prime, V, k);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return SS_ERR_WORKSPACE;
+  return cuda_status(launch_specvocab(hidden, w_down, w_vocab, u_full, M, d, d_prime, V, k,
+                                      temperature, uniforms, out_tokens, out_topk_idx,
+                                      out_topk_prob, out_scores, workspace, stream));
+}
+
+size_t ss_topk_workspace_size(int M, int V, int k) {
+  if (M < 0 || V <= 0 || k < 1 || k > V) return 0;
+  return topk_ws_bytes(M, V, k);
+}
+
+int ss_topk_rows(const float* scores, int M, int V, int k, int32_t* out_idx, void* workspace,
+                 size_t workspace_bytes, cudaStream_t stream) {
+  if (M < 0 || V <= 0 || k < 1 || k > V) return SS_ERR_INVALID_ARG;
+  if (M == 0) return SS_OK;
+  if (!scores || !out_idx || !aligned(scores, 4) || !aligned(out_idx, 4)) return SS_ERR_INVALID_ARG;
+  if (workspace_bytes < topk_ws_bytes(M, V, k)) return SS_ERR_WORKSPACE;
+  return cuda_status(launch_topk(scores, M, V, k, out_idx, workspace, stream));
+}
+
+// ----------------------------------------------------------------- verify --
+size_t spec_verify_workspace_size(int B, int gamma, int V, float temperature) {
+  if (B < 0 || gamma < 1 || gamma > 32 || V <= 0 || !temp_ok(temperature)) return 0;
+  return verify_ws_bytes(B, gamma, V, temperature > 0.f);
+}
+
+int spec_verify(const float* target_logits, const float* draft_logits, const int32_t* draft_tokens,
+                int B, int gamma, int V, float temperature, const float* uniforms,
+                int32_t* out_tokens, int32_t* out_num_accepted, void* workspace,
+                size_t workspace_bytes, cudaStream_t stream) {
+  if (B < 0 || gamma < 1 || gamma > 32 || V <= 0 || !temp_ok(temperature))
+    return SS_ERR_INVALID_ARG;
+  if ((long long)B * (gamma + 1) * V >= (1LL << 40)) return SS_ERR_UNSUPPORTED;
+  if (B == 0) return SS_OK;
+  const bool sample = temperature > 0.f;
+  if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SS_ERR_INVALID_ARG;
+  if (sample && (!draft_logits || !uniforms)) return SS_ERR_INVALID_ARG;
+  if (!aligned(target_logits, 16) || (draft_logits && !aligned(draft_logits, 16)) ||
+      !aligned(draft_tokens, 4) || !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4) ||
+      (uniforms && !aligned(uniforms, 4)))
+    return SS_ERR_INVALID_ARG;
+  const size_t need = verify_ws_bytes(B, gamma, V, sample);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return SS_ERR_WORKSPACE;
+  return cuda_status(launch_verify(target_logits, draft_logits, draft_tokens, B, gamma, V,
+                                   temperature, uniforms, out_tokens, out_num_accepted, workspace,
+                                   stream));
+}
+
+}  // extern "C"

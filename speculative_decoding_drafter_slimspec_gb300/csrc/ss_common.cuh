@@ -1,0 +1,201 @@
+// ss_common.cuh -- device helpers shared by the sm_103a kernels of libslimspec.
+//
+// Holds: the per-device error word, bounded mbarrier waits, 1-D bulk copies
+// (cp.async.bulk) into shared memory, bf16 unpacking, lane reductions and the
+// (max, sum, argmax) running state of an online softmax.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/slimspec.h"
+
+namespace ss {
+
+// ------------------------------------------------------------------ errors --
+enum : unsigned { kErrTimeout = 1u, kErrIndex = 2u };
+
+// Kernels receive the device address of the library's per-device error word
+// and record anomalies in it with atomicOr (see ss_get_device_error).
+__device__ __forceinline__ void raise_error(unsigned* err, unsigned bits) {
+  if (err) atomicOr(err, bits);
+}
+
+// ------------------------------------------------------------ time / waits --
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// A bounded wait gives up after this many nanoseconds and reports kErrTimeout.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase with the given parity to complete.  Returns false (and
+// records kErrTimeout) if it has not completed within kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) {
+      raise_error(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+
+// 1-D bulk copy global -> shared, completing `bytes` transactions on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// --------------------------------------------------------------- numerics --
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Round-to-nearest-even of an fp32 value to bf16, returned as fp32 and as bits.
+__device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
+  uint32_t b = __float_as_uint(x);
+  b += 0x7FFFu + ((b >> 16) & 1u);
+  return static_cast<uint16_t>(b >> 16);
+}
+__device__ __forceinline__ float round_bf16(float x) {
+  return __uint_as_float(static_cast<uint32_t>(f32_to_bf16_bits(x)) << 16);
+}
+
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2**x on the SFU (ex2.approx; relative error about 2**-22); 2**-inf = 0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kNegInf = -__builtin_huge_valf();
+
+// Running state of an online softmax over a stream of logits:
+//   mx  = largest logit seen, arg = lowest index attaining it,
+//   sum = sum_v exp2((l_v - mx) * c)  with c = log2(e) / T  (sampling only).
+struct RowState {
+  float mx;
+  float sum;
+  int arg;
+};
+
+__device__ __forceinline__ RowState row_state_empty() { return {kNegInf, 0.f, 0x7FFFFFFF}; }
+
+template <bool kSample>
+__device__ __forceinline__ void row_state_push(RowState& s, float x, int v, float c) {
+  if (x > s.mx) {
+    if (kSample) s.sum = __fmaf_rn(s.sum, fast_exp2((s.mx - x) * c), 1.0f);
+    s.mx = x;
+    s.arg = v;
+  } else if (kSample) {
+    s.sum = __fadd_rn(s.sum, fast_exp2((x - s.mx) * c));
+  }
+}
+
+// Combines two states; the argmax tie goes to the lower index.
+template <bool kSample>
+__device__ __forceinline__ RowState row_state_merge(RowState a, RowState b, float c) {
+  RowState o;
+  const bool take_b = (b.mx > a.mx) || (b.mx == a.mx && b.arg < a.arg);
+  o.mx = take_b ? b.mx : a.mx;
+  o.arg = take_b ? b.arg : a.arg;
+  if (kSample) {
+    const float sa = (a.mx == o.mx) ? a.sum : a.sum * fast_exp2((a.mx - o.mx) * c);
+    const float sb = (b.mx == o.mx) ? b.sum : b.sum * fast_exp2((b.mx - o.mx) * c);
+    o.sum = __fadd_rn(sa, sb);
+  } else {
+    o.sum = 0.f;
+  }
+  return o;
+}
+
+template <bool kSample>
+__device__ __forceinline__ RowState shfl_merge(RowState s, int offset, float c) {
+  RowState o;
+  o.mx = __shfl_xor_sync(0xFFFFFFFFu, s.mx, offset);
+  o.sum = __shfl_xor_sync(0xFFFFFFFFu, s.sum, offset);
+  o.arg = __shfl_xor_sync(0xFFFFFFFFu, s.arg, offset);
+  return row_state_merge<kSample>(s, o, c);
+}
+
+// Reduce-scatter of N per-lane values over aligned groups of G lanes
+// (N, G powers of two).  After the call lane l holds, in v[0 .. max(N/G,1)-1],
+// the group-wide sums of the entries with indices
+//   ((l % G) >> (log2 G - s)) << log2(max(N/G,1)) + i,   s = log2(N / max(N/G,1)),
+// and lanes that differ only in their low (log2 G - s) bits hold equal values.
+template <int N, int O>
+struct ReduceScatter {
+  static __device__ __forceinline__ void run(float* v, int lane) {
+    if constexpr (O == 0) {
+      return;
+    } else if constexpr (N > 1) {
+      const bool hi = (lane & O) != 0;
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i) {
+        const float send = hi ? v[i] : v[i + N / 2];
+        const float keep = hi ? v[i + N / 2] : v[i];
+        v[i] = __fadd_rn(keep, __shfl_xor_sync(0xFFFFFFFFu, send, O));
+      }
+      ReduceScatter<N / 2, O / 2>::run(v, lane);
+    } else {
+      v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], O));
+      ReduceScatter<1, O / 2>::run(v, lane);
+    }
+  }
+};
+
+constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// Orderable 32-bit key of a float: larger float <=> larger key; -0 == +0.
+__device__ __forceinline__ uint32_t float_key(float f) {
+  uint32_t b = __float_as_uint(f);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+}  // namespace ss

@@ -1,0 +1,386 @@
+// verify.cu -- speculative verification on sm_103a.
+//
+// Explainer (大模型批改 5 个词…), sections "小模型起草，大模型批改" and "为什么答案不会变",
+// and SpecTr-GBV article, 第三步.  The verifier reads every target row
+// (B x (gamma+1) x V fp32) and, when sampling, every draft row (B x gamma x V):
+// it is an HBM streaming reduction.
+//
+//   k_verify_rows    one warp per (row, 4096-float chunk): 16-byte streaming
+//                    loads, online (max, sum of exp at T, argmax) -> partials
+//   k_verify_decide  one warp per sequence: merges the partials of its rows,
+//                    greedy prefix match or the min(1, p/q) accept tests
+//   k_verify_resid   one warp per (sequence, chunk) of the final draw's row:
+//                    chunk masses of max(0, p_n - q_n) (bonus: of p_gamma,
+//                    straight from the partials)
+//   k_verify_finish  one CTA per sequence: inverse CDF over the chunk masses,
+//                    then an ordered scan of the one chunk that holds the draw
+#include <algorithm>
+
+#include "ss_common.cuh"
+#include "ss_internal.h"
+
+namespace ss {
+
+constexpr int kVChunk = 4096;  // floats per partial
+
+struct VerifyInfo {
+  int n;        // accepted drafted tokens
+  int mode;     // 0: residual of row n, 1: target row n alone (bonus / fallback)
+  float pmx, pinv, qmx, qinv;  // row maxima and reciprocal normalisers
+  float pad0, pad1;
+};
+
+template <bool kSample>
+__device__ __forceinline__ void push4(RowState& s, const float4 a, int v0, float c) {
+  const float m01 = fmaxf(a.x, a.y), m23 = fmaxf(a.z, a.w), m4 = fmaxf(m01, m23);
+  const int off = (a.x == m4) ? 0 : (a.y == m4) ? 1 : (a.z == m4) ? 2 : 3;
+  if (m4 > s.mx) {
+    if (kSample) s.sum = s.sum * fast_exp2((s.mx - m4) * c);
+    s.mx = m4;
+    s.arg = v0 + off;
+  }
+  if (kSample) {
+    const float mx = s.mx;
+    float t = fast_exp2((a.x - mx) * c);
+    t = __fadd_rn(t, fast_exp2((a.y - mx) * c));
+    t = __fadd_rn(t, fast_exp2((a.z - mx) * c));
+    t = __fadd_rn(t, fast_exp2((a.w - mx) * c));
+    s.sum = __fadd_rn(s.sum, t);
+  }
+}
+
+// ------------------------------------------------------------------- K8 ----
+template <bool kSample>
+__global__ void __launch_bounds__(512)
+    k_verify_rows(const float* __restrict__ target, const float* __restrict__ draft,
+                  int n_target_rows, int n_rows, int V, float c, int n_chunks,
+                  float* __restrict__ vmax, float* __restrict__ vsum, int* __restrict__ varg) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  const bool vec = (V & 3) == 0;
+  const long long units = (long long)n_rows * n_chunks;
+  for (long long u = gw; u < units; u += nw) {
+    const int row = (int)(u / n_chunks), ch = (int)(u % n_chunks);
+    const float* src = row < n_target_rows ? target + (size_t)row * V
+                                           : draft + (size_t)(row - n_target_rows) * V;
+    const int lo = ch * kVChunk, hi = min(V, lo + kVChunk);
+    RowState s = row_state_empty();
+    if (vec) {
+      const float4* p4 = reinterpret_cast<const float4*>(src);
+      const int q0 = lo >> 2, q1 = hi >> 2;
+      for (int base = q0; base < q1; base += 128) {
+        float4 a[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int q = base + lane + 32 * k;
+          if (q < q1) a[k] = __ldcs(p4 + q);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int q = base + lane + 32 * k;
+          if (q < q1) push4<kSample>(s, a[k], q * 4, c);
+        }
+      }
+    } else {
+      for (int i = lo + lane; i < hi; i += 32) row_state_push<kSample>(s, __ldcs(src + i), i, c);
+    }
+#pragma unroll
+    for (int b = 0; b < 5; ++b) s = shfl_merge<kSample>(s, 1 << b, c);
+    if (lane == 0) {
+      const size_t o = (size_t)row * n_chunks + ch;
+      vmax[o] = s.mx;
+      varg[o] = s.arg;
+      if (kSample) vsum[o] = s.sum;
+    }
+  }
+}
+
+// Merged state of one row from its chunk partials (result in every lane).
+template <bool kSample>
+__device__ __forceinline__ RowState warp_row_state(int row, int n_chunks, const float* vmax,
+                                                   const float* vsum, const int* varg, float c,
+                                                   int lane) {
+  RowState s = row_state_empty();
+  for (int ch = lane; ch < n_chunks; ch += 32) {
+    const size_t o = (size_t)row * n_chunks + ch;
+    RowState t{vmax[o], kSample ? vsum[o] : 0.f, varg[o]};
+    s = row_state_merge<kSample>(s, t, c);
+  }
+#pragma unroll
+  for (int b = 0; b < 5; ++b) s = shfl_merge<kSample>(s, 1 << b, c);
+  return s;
+}
+
+// ------------------------------------------------------------------- K9 ----
+template <bool kSample>
+__global__ void __launch_bounds__(128)
+    k_verify_decide(const float* __restrict__ target, const float* __restrict__ draft,
+                    const int32_t* __restrict__ tokens, int B, int gamma, int V, float c,
+                    int n_chunks, const float* __restrict__ vmax, const float* __restrict__ vsum,
+                    const int* __restrict__ varg, const float* __restrict__ uniforms,
+                    int32_t* __restrict__ out_tokens, int32_t* __restrict__ out_nacc,
+                    VerifyInfo* __restrict__ info, unsigned* err) {
+  const int lane = threadIdx.x & 31;
+  const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (b >= B) return;
+  const int g1 = gamma + 1;
+  const int n_target_rows = B * g1;
+  int n = gamma, last = -1;
+  RowState P{}, Q{};
+  // every drafted token must be a vocabulary id, including those past the
+  // first rejection that the decision never reads
+  for (int i = lane; i < gamma; i += 32) {
+    const int x = tokens[(size_t)b * gamma + i];
+    if (x < 0 || x >= V) raise_error(err, kErrIndex);
+  }
+  for (int j = 0; j < gamma; ++j) {
+    const int x = tokens[(size_t)b * gamma + j];
+    const bool bad = (x < 0 || x >= V);
+    P = warp_row_state<kSample>(b * g1 + j, n_chunks, vmax, vsum, varg, c, lane);
+    if (!kSample) {
+      if (bad || x != P.arg) { n = j; last = P.arg; break; }
+    } else {
+      Q = warp_row_state<kSample>(n_target_rows + b * gamma + j, n_chunks, vmax, vsum, varg, c,
+                                  lane);
+      bool accept = false;
+      if (!bad) {
+        const float lp = target[((size_t)b * g1 + j) * V + x];
+        const float lq = draft[((size_t)b * gamma + j) * V + x];
+        const float px = __fdiv_rn(fast_exp2((lp - P.mx) * c), P.sum);
+        const float qx = __fdiv_rn(fast_exp2((lq - Q.mx) * c), Q.sum);
+        const float u = uniforms[(size_t)b * g1 + j];
+        accept = u * qx < px;
+      }
+      if (!accept) { n = j; break; }
+    }
+  }
+  if (n == gamma) {
+    P = warp_row_state<kSample>(b * g1 + gamma, n_chunks, vmax, vsum, varg, c, lane);
+    last = P.arg;
+  }
+  for (int i = lane; i < g1; i += 32) {
+    int32_t t = -1;
+    if (i < n) t = tokens[(size_t)b * gamma + i];
+    else if (i == n) t = kSample ? -1 : last;
+    out_tokens[(size_t)b * g1 + i] = t;
+  }
+  if (lane == 0) {
+    out_nacc[b] = n;
+    if (kSample) {
+      VerifyInfo in{};
+      in.n = n;
+      in.mode = (n == gamma) ? 1 : 0;
+      in.pmx = P.mx;
+      in.pinv = __frcp_rn(P.sum);
+      in.qmx = (n == gamma) ? 0.f : Q.mx;
+      in.qinv = (n == gamma) ? 0.f : __frcp_rn(Q.sum);
+      info[b] = in;
+    }
+  }
+}
+
+// Weight of token v in the final draw of a sequence.
+__device__ __forceinline__ float final_weight(const VerifyInfo& in, int mode, float lt, float lq,
+                                              float c) {
+  const float pv = fast_exp2((lt - in.pmx) * c) * in.pinv;
+  if (mode == 1) return pv;
+  const float qv = fast_exp2((lq - in.qmx) * c) * in.qinv;
+  return fmaxf(pv - qv, 0.f);
+}
+
+// ------------------------------------------------------------------ K10 ----
+__global__ void __launch_bounds__(512)
+    k_verify_resid(const float* __restrict__ target, const float* __restrict__ draft, int B,
+                   int gamma, int V, float c, int n_chunks, const float* __restrict__ vmax,
+                   const float* __restrict__ vsum, const VerifyInfo* __restrict__ info,
+                   float* __restrict__ rmass) {
+  const int lane = threadIdx.x & 31;
+  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  const int g1 = gamma + 1;
+  const long long units = (long long)B * n_chunks;
+  for (long long u = gw; u < units; u += nw) {
+    const int b = (int)(u / n_chunks), ch = (int)(u % n_chunks);
+    const VerifyInfo in = info[b];
+    const int trow = b * g1 + in.n;
+    float s = 0.f;
+    if (in.mode == 1) {
+      if (lane == 0) {
+        const size_t o = (size_t)trow * n_chunks + ch;
+        s = vsum[o] * fast_exp2((vmax[o] - in.pmx) * c) * in.pinv;
+      }
+    } else {
+      const float* t = target + (size_t)trow * V;
+      const float* q = draft + ((size_t)b * gamma + in.n) * V;
+      const int lo = ch * kVChunk, hi = min(V, lo + kVChunk);
+      for (int i = lo + lane; i < hi; i += 32)
+        s = __fadd_rn(s, final_weight(in, 0, __ldg(t + i), __ldg(q + i), c));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, o));
+    }
+    if (lane == 0) rmass[(size_t)b * n_chunks + ch] = s;
+  }
+}
+
+// ------------------------------------------------------------------ K11 ----
+__global__ void __launch_bounds__(256)
+    k_verify_finish(const float* __restrict__ target, const float* __restrict__ draft, int B,
+                    int gamma, int V, float c, int n_chunks, const float* __restrict__ vmax,
+                    const float* __restrict__ vsum, const VerifyInfo* __restrict__ info,
+                    const float* __restrict__ rmass, const float* __restrict__ uniforms,
+                    int32_t* __restrict__ out_tokens) {
+  constexpr int NT = 256, PER = kVChunk / NT;  // 16 elements per thread
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g1 = gamma + 1;
+  const VerifyInfo in = info[b];
+  const int trow = b * g1 + in.n;
+  __shared__ int s_ch, s_mode;
+  __shared__ float s_resid;
+  if (tid == 0) {
+    int mode = in.mode;
+    float R = 0.f;
+    for (int ch = 0; ch < n_chunks; ++ch) R = __fadd_rn(R, rmass[(size_t)b * n_chunks + ch]);
+    auto mass = [&](int ch) -> float {
+      if (mode == 0) return rmass[(size_t)b * n_chunks + ch];
+      const size_t o = (size_t)trow * n_chunks + ch;
+      return vsum[o] * fast_exp2((vmax[o] - in.pmx) * c) * in.pinv;
+    };
+    if (!(R > 0.f) && mode == 0) {  // residual vanished: draw from p_n
+      mode = 1;
+      R = 0.f;
+      for (int ch = 0; ch < n_chunks; ++ch) R = __fadd_rn(R, mass(ch));
+    }
+    const float target_mass = uniforms[(size_t)b * g1 + gamma] * R;
+    float cum = 0.f, before = 0.f;
+    int sel = -1, lastp = -1;
+    for (int ch = 0; ch < n_chunks; ++ch) {
+      const float mc = mass(ch);
+      if (mc > 0.f) { lastp = ch; before = cum; }
+      const float nc = __fadd_rn(cum, mc);
+      if (mc > 0.f && nc > target_mass) { sel = ch; before = cum; break; }
+      cum = nc;
+    }
+    if (sel < 0) sel = lastp < 0 ? 0 : lastp;
+    s_ch = sel;
+    s_mode = mode;
+    s_resid = target_mass - before;
+  }
+  __syncthreads();
+  const int ch = s_ch, mode = s_mode;
+  const float resid = s_resid;
+  const float* t = target + (size_t)trow * V;
+  const float* q = draft + ((size_t)b * gamma + in.n) * V;
+  const int lo = ch * kVChunk + tid * PER, hi = min(V, ch * kVChunk + kVChunk);
+  float wv[PER];
+  float my = 0.f;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int v = lo + i;
+    wv[i] = (v < hi) ? final_weight(in, mode, t[v], mode == 0 ? q[v] : 0.f, c) : 0.f;
+    my = __fadd_rn(my, wv[i]);
+  }
+  // exclusive scan of the per-thread sums (fixed order)
+  float incl = my;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl = __fadd_rn(y, incl);
+  }
+  float ex_w = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+  if (lane == 0) ex_w = 0.f;
+  __shared__ float s_w[8];
+  __shared__ int s_first, s_last;
+  if (lane == 31) s_w[warp] = incl;
+  if (tid == 0) { s_first = NT; s_last = -1; }
+  __syncthreads();
+  if (tid == 0) {
+    float run = 0.f;
+    for (int k = 0; k < 8; ++k) { const float x = s_w[k]; s_w[k] = run; run = __fadd_rn(run, x); }
+  }
+  __syncthreads();
+  const float excl = __fadd_rn(s_w[warp], ex_w);
+  const float incl_blk = __fadd_rn(s_w[warp], incl);
+  if (my > 0.f) {
+    atomicMax(&s_last, tid);
+    if (incl_blk > resid) atomicMin(&s_first, tid);
+  }
+  __syncthreads();
+  const int owner = s_first < NT ? s_first : s_last;
+  if (tid == owner) {
+    float cum = excl;
+    int tok = -1, lastp = -1;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      if (wv[i] > 0.f) {
+        lastp = i;
+        cum = __fadd_rn(cum, wv[i]);
+        if (tok < 0 && cum > resid) tok = i;
+      }
+    }
+    if (tok < 0) tok = lastp;
+    out_tokens[(size_t)b * g1 + in.n] = lo + tok;
+  } else if (owner < 0 && tid == 0) {
+    out_tokens[(size_t)b * g1 + in.n] = ch * kVChunk;  // unreachable for finite inputs
+  }
+}
+
+// -------------------------------------------------------------- host side --
+size_t verify_ws_bytes(int B, int gamma, int V, bool sample) {
+  const int n_chunks = (V + kVChunk - 1) / kVChunk;
+  const size_t rows = (size_t)B * (gamma + 1) + (sample ? (size_t)B * gamma : 0);
+  size_t s = 0;
+  s += align256(rows * n_chunks * sizeof(float));       // vmax
+  s += align256(rows * n_chunks * sizeof(float));       // vsum
+  s += align256(rows * n_chunks * sizeof(int));         // varg
+  s += align256((size_t)B * sizeof(VerifyInfo));        // info
+  s += align256((size_t)B * n_chunks * sizeof(float));  // rmass
+  return s;
+}
+
+cudaError_t launch_verify(const float* target, const float* draft, const int32_t* tokens, int B,
+                          int gamma, int V, float temperature, const float* uniforms,
+                          int32_t* out_tokens, int32_t* out_nacc, void* ws, cudaStream_t st) {
+  if (B <= 0) return cudaSuccess;
+  const bool sample = temperature > 0.f;
+  const float c = sample ? (float)(1.4426950408889634 / (double)temperature) : 0.f;
+  const int n_chunks = (V + kVChunk - 1) / kVChunk;
+  const int g1 = gamma + 1;
+  const int n_target_rows = B * g1;
+  const int n_rows = n_target_rows + (sample ? B * gamma : 0);
+  Carver cv(ws);
+  float* vmax = cv.take<float>((size_t)n_rows * n_chunks);
+  float* vsum = cv.take<float>((size_t)n_rows * n_chunks);
+  int* varg = cv.take<int>((size_t)n_rows * n_chunks);
+  VerifyInfo* info = cv.take<VerifyInfo>(B);
+  float* rmass = cv.take<float>((size_t)B * n_chunks);
+
+  const long long units = (long long)n_rows * n_chunks;
+  const int grid = (int)std::max<long long>(1, std::min<long long>((units + 15) / 16, 4LL * sm_count()));
+  if (sample)
+    k_verify_rows<true><<<grid, 512, 0, st>>>(target, draft, n_target_rows, n_rows, V, c,
+                                              n_chunks, vmax, vsum, varg);
+  else
+    k_verify_rows<false><<<grid, 512, 0, st>>>(target, draft, n_target_rows, n_rows, V, c,
+                                               n_chunks, vmax, vsum, varg);
+  const int dgrid = (B + 3) / 4;
+  if (sample)
+    k_verify_decide<true><<<dgrid, 128, 0, st>>>(target, draft, tokens, B, gamma, V, c, n_chunks,
+                                                 vmax, vsum, varg, uniforms, out_tokens, out_nacc,
+                                                 info, error_word());
+  else
+    k_verify_decide<false><<<dgrid, 128, 0, st>>>(target, draft, tokens, B, gamma, V, c,
+                                                  n_chunks, vmax, vsum, varg, uniforms,
+                                                  out_tokens, out_nacc, info, error_word());
+  if (sample) {
+    const long long ru = (long long)B * n_chunks;
+    const int rgrid = (int)std::max<long long>(1, std::min<long long>((ru + 15) / 16, 4LL * sm_count()));
+    k_verify_resid<<<rgrid, 512, 0, st>>>(target, draft, B, gamma, V, c, n_chunks, vmax, vsum,
+                                          info, rmass);
+    k_verify_finish<<<B, 256, 0, st>>>(target, draft, B, gamma, V, c, n_chunks, vmax, vsum, info,
+                                       rmass, uniforms, out_tokens);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace ss

@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: the library builds and loads, exports every symbol
+the header declares, sizes workspaces, and rejects bad arguments on the host
+before launching anything (fake device pointers are never dereferenced here:
+each call below fails validation first)."""
+import ctypes
+import math
+
+import pytest
+
+import __graft_entry__
+import speculative_decoding_drafter_slimspec_gb300 as ss
+
+
+@pytest.fixture(scope="module")
+def lib():
+    __graft_entry__.build()
+    return ss.lib()
+
+
+FAKE = ctypes.c_void_p(1 << 20)      # 16-byte aligned, never dereferenced
+MISAL = ctypes.c_void_p((1 << 20) + 8)
+NULL = None
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = ss.header_functions()
+    assert set(names) == set(ss._SIGS)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert lib.ss_version() == 100
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.ss_status_string(s).decode().startswith("SS_")
+    assert lib.ss_status_string(99) == b"unknown status"
+
+
+def test_workspace_sizes(lib):
+    w = lib.slimspec_head_workspace_size(8, 4096, 512, 128256, ss.SS_BF16)
+    # z (8 x 512 fp32) + three partial arrays of 8 x ceil(128256/32)
+    assert w >= 8 * 512 * 4 + 3 * 8 * 4008 * 4
+    assert lib.slimspec_head_workspace_size(-1, 4096, 512, 128256, ss.SS_BF16) == 0
+    assert lib.slimspec_head_workspace_size(8, 4096, 2048, 128256, ss.SS_BF16) == 0  # r too wide
+    assert lib.spec_verify_workspace_size(16, 6, 201088, ctypes.c_float(0.7)) > 0
+    assert lib.spec_verify_workspace_size(16, 0, 201088, ctypes.c_float(0.7)) == 0
+    assert lib.specvocab_head_workspace_size(32, 4096, 256, 151936, 2048) >= 32 * 151936 * 4
+    assert lib.specvocab_head_workspace_size(32, 4096, 256, 151936, 0) == 0
+
+
+def _head(lib, **kw):
+    a = dict(hidden=FAKE, w_down=FAKE, w_up=FAKE, M=2, d=64, r=32, V=100, dtype=ss.SS_BF16,
+             T=0.0, u=NULL, tok=FAKE, lp=NULL, mx=NULL, lse=NULL, z=NULL, logits=NULL,
+             ws=FAKE, wsb=1 << 20, stream=NULL)
+    a.update(kw)
+    return lib.slimspec_head_forward(a["hidden"], a["w_down"], a["w_up"], a["M"], a["d"], a["r"],
+                                     a["V"], a["dtype"], a["T"], a["u"], a["tok"], a["lp"],
+                                     a["mx"], a["lse"], a["z"], a["logits"], a["ws"], a["wsb"],
+                                     a["stream"])
+
+
+def test_head_argument_errors(lib):
+    E = ss.SS_ERR_INVALID_ARG
+    assert _head(lib, M=-1) == E
+    assert _head(lib, d=60) == E                     # d % 8
+    assert _head(lib, r=20) == E                     # r % 8 for bf16
+    assert _head(lib, dtype=7) == E
+    assert _head(lib, T=float("nan")) == E
+    assert _head(lib, T=-0.5) == E
+    assert _head(lib, T=math.inf) == E
+    assert _head(lib, hidden=NULL) == E
+    assert _head(lib, tok=NULL) == E
+    assert _head(lib, w_up=MISAL) == E
+    assert _head(lib, T=1.0, u=NULL) == E           # sampling needs uniforms
+    assert _head(lib, r=4096) == ss.SS_ERR_UNSUPPORTED
+    assert _head(lib, ws=NULL) == ss.SS_ERR_WORKSPACE
+    assert _head(lib, wsb=16) == ss.SS_ERR_WORKSPACE
+    assert _head(lib, ws=MISAL) == ss.SS_ERR_WORKSPACE
+    assert _head(lib, M=0) == ss.SS_OK               # empty batch: nothing to do
+
+
+def test_verify_argument_errors(lib):
+    def call(B=2, g=3, V=100, T=0.0, tgt=FAKE, dr=NULL, tok=FAKE, u=NULL, ot=FAKE, on=FAKE,
+             ws=FAKE, wsb=1 << 20):
+        return lib.spec_verify(tgt, dr, tok, B, g, V, T, u, ot, on, ws, wsb, NULL)
+    E = ss.SS_ERR_INVALID_ARG
+    assert call(B=-1) == E
+    assert call(g=0) == E
+    assert call(g=33) == E
+    assert call(V=0) == E
+    assert call(T=float("nan")) == E
+    assert call(tgt=NULL) == E
+    assert call(T=0.7) == E                          # sampling needs draft logits
+    assert call(T=0.7, dr=FAKE) == E                 # ... and uniforms
+    assert call(tgt=MISAL) == E
+    assert call(wsb=8) == ss.SS_ERR_WORKSPACE
+    assert call(B=0) == ss.SS_OK
+
+
+def test_specvocab_and_topk_argument_errors(lib):
+    def sv(M=2, d=64, dp=16, V=100, k=10, T=0.0, ws=FAKE, wsb=1 << 24):
+        return lib.specvocab_head_forward(FAKE, FAKE, FAKE, FAKE, M, d, dp, V, k, T, NULL, FAKE,
+                                          NULL, NULL, NULL, ws, wsb, NULL)
+    assert sv(k=0) == ss.SS_ERR_INVALID_ARG
+    assert sv(k=101) == ss.SS_ERR_INVALID_ARG
+    assert sv(dp=12) == ss.SS_ERR_INVALID_ARG
+    assert sv(d=8192) == ss.SS_ERR_UNSUPPORTED
+    assert sv(T=1.0) == ss.SS_ERR_INVALID_ARG         # no uniforms
+    assert sv(wsb=1) == ss.SS_ERR_WORKSPACE
+    assert sv(M=0) == ss.SS_OK
+    assert lib.ss_topk_rows(FAKE, 2, 100, 0, FAKE, NULL, 0, NULL) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_topk_rows(FAKE, 2, 100, 101, FAKE, NULL, 0, NULL) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_topk_rows(NULL, 2, 100, 5, FAKE, NULL, 0, NULL) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_topk_rows(FAKE, 0, 100, 5, FAKE, NULL, 0, NULL) == ss.SS_OK
+
+
+def test_python_binding_refuses_cpu_tensors(lib):
+    import torch
+    h = torch.zeros(2, 64, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        ss.slimspec_head_forward(h, torch.zeros(32, 64, dtype=torch.bfloat16),
+                                 torch.zeros(100, 32, dtype=torch.bfloat16))

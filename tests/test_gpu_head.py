@@ -1,0 +1,161 @@
+"""GPU parity of the SlimSpec low-rank head against the CPU oracle.
+
+Sizes span several vocabulary tiles with a ragged last tile, several m-tiles,
+the fp32 and bf16 paths and every row-width geometry; the full workload
+shapes run in the same launch configuration the benchmark times.
+Tolerances: logits / statistics 2e-2 absolute for bf16 weights, 1e-5 for the
+fp32 workload; tokens by the rules in tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import speculative_decoding_drafter_slimspec_gb300 as ss
+from parity import check_head_tokens
+from gpu_util import device, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+EPS_GREEDY = {"f32": 1e-5, "bf16": 2e-3}
+
+
+def _z_check(z_gpu, hidden, w_down, dtype):
+    ref = oracle.down_projection(hidden, w_down, dtype)
+    if dtype == "f32":
+        scale = np.maximum(1.0, np.abs(ref))
+        assert np.max(np.abs(z_gpu - ref) / scale) < 1e-5
+        return 0
+    # bf16: equal to the oracle's rounding unless the unrounded value sits
+    # within fp32 accumulation error of a rounding midpoint (then one ulp off)
+    raw = oracle.down_projection(hidden, w_down, "f32")
+    diff = z_gpu != ref
+    if np.any(diff):
+        ulp = np.abs(ref[diff]) * 2.0 ** -7
+        assert np.all(np.abs(z_gpu[diff] - ref[diff]) <= ulp * 1.01)
+        mid_dist = np.abs(np.abs(raw[diff] - (z_gpu[diff] + ref[diff]) / 2))
+        assert np.all(mid_dist <= 2.0 ** -16 * np.abs(raw[diff]) + 1e-30)
+    return int(diff.sum())
+
+
+def run_case(seed, M, d, r, V, dtype, T, logits=True):
+    inp = synth.head_inputs(seed, M=M, d=d, r=r, V=V, dtype=dtype)
+    u = synth.uniforms(np.random.default_rng(seed + 1), (M,))
+    dev = device()
+    t = {k: to_dev(v, dtype) for k, v in inp.items()}
+    out = ss.slimspec_head_forward(t["hidden"], t["w_down"], t["w_up"], T,
+                                   to_dev(u, "f32") if T > 0 else None,
+                                   want_z=True, want_logits=logits)
+    torch.cuda.synchronize()
+    assert ss.ss_get_device_error() == ss.SS_OK
+    ref = oracle.slimspec_head(inp["hidden"], inp["w_down"], inp["w_up"], dtype, T,
+                               u if T > 0 else None)
+    g = {k: v.float().cpu().numpy() if v.dtype != torch.int32 else v.cpu().numpy()
+         for k, v in out.items()}
+    flips = _z_check(g["z"].astype(np.float64), inp["hidden"], inp["w_down"], dtype)
+    tol = TOL[dtype]
+    if logits:
+        assert np.max(np.abs(g["logits"] - ref["logits"])) <= tol
+    counts = check_head_tokens(g["tokens"], ref["logits"], T, u, EPS_GREEDY[dtype])
+    np.testing.assert_allclose(g["row_max"], ref["max"], atol=tol, rtol=0)
+    np.testing.assert_allclose(g["lse"], ref["lse"], atol=tol, rtol=0)
+    # logprob of the token the GPU chose, from the oracle's logits
+    lt = ref["logits"][np.arange(M), g["tokens"]]
+    if T > 0:
+        ref_lp = (lt - ref["max"]) / T - (ref["lse"] - ref["max"] / T)
+    else:
+        ref_lp = np.zeros(M)
+    np.testing.assert_allclose(g["logprob"], ref_lp, atol=tol, rtol=0)
+    return counts, flips
+
+
+SMALL = [
+    # seed, M, d, r, V, dtype          geometry exercised
+    (11, 1, 256, 32, 4096, "f32"),    # the oracle-scale workload (LPR=8)
+    (12, 3, 64, 64, 999, "f32"),      # LPR=32, CPL=1, ragged tail
+    (13, 9, 128, 128, 3001, "f32"),   # CPL=2, two m-tiles of 8
+    (14, 1, 256, 64, 1000, "bf16"),   # CPL=1 with idle lanes
+    (15, 5, 720, 360, 2000, "bf16"),  # r=360: 45 chunks, CPL=2 tail
+    (16, 8, 1024, 512, 4133, "bf16"), # CPL=2, MT=8
+    (17, 16, 512, 512, 2050, "bf16"), # two m-tiles
+    (18, 4, 1024, 1024, 1500, "bf16"),# CPL=4, MT=4
+    (19, 2, 64, 32, 1, "bf16"),       # V = 1
+    (20, 3, 64, 32, 31, "bf16"),      # V smaller than one tile
+]
+
+
+@pytest.mark.parametrize("T", [0.0, 0.7, 1.0])
+@pytest.mark.parametrize("case", SMALL, ids=lambda c: f"M{c[1]}-r{c[3]}-V{c[4]}-{c[5]}")
+def test_head_small(case, T):
+    seed, M, d, r, V, dtype = case
+    run_case(seed, M, d, r, V, dtype, T)
+
+
+def test_head_empty_batch():
+    dev = device()
+    h = torch.zeros(0, 64, dtype=torch.bfloat16, device=dev)
+    out = ss.slimspec_head_forward(h, torch.zeros(32, 64, dtype=torch.bfloat16, device=dev),
+                                   torch.zeros(100, 32, dtype=torch.bfloat16, device=dev))
+    torch.cuda.synchronize()
+    assert out["tokens"].numel() == 0
+
+
+def test_head_deterministic():
+    inp = synth.head_inputs(5, M=8, d=512, r=512, V=20000, dtype="bf16")
+    t = {k: to_dev(v, "bf16") for k, v in inp.items()}
+    u = to_dev(synth.uniforms(np.random.default_rng(2), (8,)), "f32")
+    a = ss.slimspec_head_forward(t["hidden"], t["w_down"], t["w_up"], 1.0, u)
+    b = ss.slimspec_head_forward(t["hidden"], t["w_down"], t["w_up"], 1.0, u)
+    torch.cuda.synchronize()
+    for k in a:
+        assert torch.equal(a[k], b[k]), k
+
+
+def test_head_sampling_tie_of_equal_logits():
+    """All logits equal: inverse CDF over a flat distribution picks
+    floor(u * V) (up to boundary rounding); greedy picks index 0."""
+    M, d, r, V = 4, 64, 32, 3000
+    dev = device()
+    h = torch.zeros(M, d, dtype=torch.bfloat16, device=dev)
+    wd = torch.zeros(r, d, dtype=torch.bfloat16, device=dev)
+    wu = torch.zeros(V, r, dtype=torch.bfloat16, device=dev)
+    u = np.array([0.0, 0.25, 0.5, 0.999], np.float32)
+    g = ss.slimspec_head_forward(h, wd, wu, 0.0)
+    s = ss.slimspec_head_forward(h, wd, wu, 1.0, to_dev(u, "f32"))
+    torch.cuda.synchronize()
+    assert g["tokens"].tolist() == [0] * M
+    got = s["tokens"].cpu().numpy()
+    assert np.all(np.abs(got - np.floor(u * V)) <= 1)
+
+
+# ------------------------------------------------ full workload shapes -----
+@pytest.mark.parametrize("M", [1, 4, 8])
+def test_head_llama8b_shape_greedy(M):
+    p = synth.PRESETS["llama8b"]
+    counts, _ = run_case(p.seed + M, M, p.d, p.r, p.V, p.dtype, 0.0, logits=False)
+    assert counts["exact"] + counts["tie"] == M
+
+
+def test_head_gptoss20b_shape_sampling():
+    p = synth.PRESETS["gptoss20b"]
+    run_case(p.seed, p.M, p.d, p.r, p.V, p.dtype, p.temperature, logits=False)
+
+
+def test_head_qwen30b_shape_sampled_rows():
+    """M = 256 rows (64 sequences x gamma 4); the oracle checks 24 sampled rows."""
+    p = synth.PRESETS["qwen30b"]
+    inp = synth.head_inputs(p.seed, M=p.M, d=p.d, r=p.r, V=p.V, dtype=p.dtype)
+    u = synth.uniforms(np.random.default_rng(p.seed + 1), (p.M,))
+    t = {k: to_dev(v, "bf16") for k, v in inp.items()}
+    out = ss.slimspec_head_forward(t["hidden"], t["w_down"], t["w_up"], p.temperature,
+                                   to_dev(u, "f32"))
+    torch.cuda.synchronize()
+    rows = np.unique(np.concatenate([[0, 1, 7, 8, 127, 128, 255],
+                                     np.random.default_rng(3).integers(0, p.M, 17)]))
+    ref = oracle.slimspec_head(inp["hidden"][rows], inp["w_down"], inp["w_up"], "bf16",
+                               p.temperature, u[rows])
+    toks = out["tokens"].cpu().numpy()[rows]
+    check_head_tokens(toks, ref["logits"], p.temperature, u[rows], EPS_GREEDY["bf16"])
+    np.testing.assert_allclose(out["lse"].cpu().numpy()[rows], ref["lse"], atol=2e-2, rtol=0)

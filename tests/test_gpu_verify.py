@@ -1,0 +1,136 @@
+"""GPU parity of spec_verify against the CPU oracle (greedy and sampling).
+
+Logit rows are fp32 inputs shared bit-for-bit by both sides, so argmax
+decisions are exact; sampling decisions follow tests/parity.py.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import speculative_decoding_drafter_slimspec_gb300 as ss
+from parity import check_verify_sampling
+from gpu_util import device, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _drafts(v, T):
+    """Drafted tokens from the draft rows: argmax (T = 0) or an inverse-CDF
+    draw with the drafter's own uniforms (the oracle's row_reduce)."""
+    B, g, V = v["draft"].shape
+    x = np.zeros((B, g), np.int32)
+    for b in range(B):
+        for j in range(g):
+            r = oracle.row_reduce(v["draft"][b, j], T, v["u_draft"][b, j] if T > 0 else None)
+            x[b, j] = r["token"]
+    return x
+
+
+def run_verify(v, x, T):
+    tgt = to_dev(v["target"], "f32")
+    dr = to_dev(v["draft"], "f32") if T > 0 else None
+    u = to_dev(v["u_verify"], "f32") if T > 0 else None
+    o = ss.spec_verify(tgt, dr, to_dev(x, "i32"), T, u)
+    torch.cuda.synchronize()
+    assert ss.ss_get_device_error() == ss.SS_OK
+    return o["tokens"].cpu().numpy(), o["num_accepted"].cpu().numpy()
+
+
+def check(v, x, T, toks, nacc):
+    B = x.shape[0]
+    if T == 0:
+        ref_t, ref_n = oracle.verify_batch(v["target"], None, x, None, 0.0)
+        np.testing.assert_array_equal(nacc, ref_n)
+        np.testing.assert_array_equal(toks, ref_t)
+        return {"exact": B, "boundary": 0}
+    counts = {"exact": 0, "boundary": 0}
+    for b in range(B):
+        n = int(nacc[b])
+        assert 0 <= n <= x.shape[1]
+        assert np.all(toks[b, n + 1:] == -1)
+        verdict = check_verify_sampling(toks[b], n, v["target"][b], v["draft"][b], x[b],
+                                        v["u_verify"][b], T)
+        counts[verdict] += 1
+    return counts
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_verify_tiny(T):
+    p = synth.PRESETS["tiny"]
+    v = synth.verify_logits(p.seed, B=64, gamma=p.gamma, V=p.V, kind="normal", draft_sigma=1.0)
+    x = _drafts(v, T)
+    toks, n = run_verify(v, x, T)
+    c = check(v, x, T, toks, n)
+    assert c["exact"] >= 62
+
+
+@pytest.mark.parametrize("V", [1, 3, 1001, 4097])
+@pytest.mark.parametrize("T", [0.0, 0.5])
+def test_verify_ragged_vocab(V, T):
+    """V not a multiple of 4 (scalar path), V = 1, one element past a chunk."""
+    v = synth.verify_logits(40 + V, B=7, gamma=3, V=V, kind="normal")
+    x = _drafts(v, T)
+    toks, n = run_verify(v, x, T)
+    check(v, x, T, toks, n)
+
+
+def test_verify_tiny_vocab_many_sequences():
+    """V = 4, gamma = 2 with 4096 random (draft, uniform) combinations: every
+    outcome matches the oracle's decision procedure."""
+    rng = np.random.default_rng(9)
+    B, g, V, T = 4096, 2, 4, 1.0
+    base_t = rng.standard_normal((g + 1, V)).astype(np.float32)
+    base_d = rng.standard_normal((g, V)).astype(np.float32)
+    v = {"target": np.ascontiguousarray(np.broadcast_to(base_t, (B, g + 1, V))),
+         "draft": np.ascontiguousarray(np.broadcast_to(base_d, (B, g, V))),
+         "u_verify": synth.uniforms(rng, (B, g + 1))}
+    x = rng.integers(0, V, (B, g)).astype(np.int32)
+    toks, n = run_verify(v, x, T)
+    c = check(v, x, T, toks, n)
+    assert c["exact"] >= B - 5
+    # empirical acceptance at position 0 against sum_x min(p, q) under x ~ uniform
+    p0 = oracle.softmax_t(base_t[0], T)
+    q0 = oracle.softmax_t(base_d[0], T)
+    acc = np.mean([min(1.0, p0[xx] / q0[xx]) for xx in x[:, 0]])
+    assert abs(np.mean(n > 0) - acc) < 4 * np.sqrt(acc * (1 - acc) / B) + 1e-3
+
+
+def test_verify_bad_token_reports_device_error():
+    v = synth.verify_logits(5, B=2, gamma=3, V=500, kind="normal")
+    x = np.array([[1, 2, 3], [4, 600, 5]], np.int32)   # 600 >= V
+    o = ss.spec_verify(to_dev(v["target"], "f32"), None, to_dev(x, "i32"), 0.0)
+    assert ss.ss_get_device_error() == ss.SS_ERR_DEVICE_INDEX
+    assert int(o["num_accepted"][1]) <= 1
+    assert ss.ss_get_device_error() == ss.SS_OK      # cleared by the read
+
+
+# ------------------------------------------------ full workload shapes -----
+def test_verify_llama8b_shape_greedy():
+    p = synth.PRESETS["llama8b"]
+    v = synth.verify_logits(p.seed, B=p.B, gamma=p.gamma, V=p.V, kind="zipf")
+    x = _drafts(v, 0.0)
+    toks, n = run_verify(v, x, 0.0)
+    check(v, x, 0.0, toks, n)
+
+
+def test_verify_gptoss20b_shape_sampling():
+    p = synth.PRESETS["gptoss20b"]
+    v = synth.verify_logits(p.seed, B=p.B, gamma=p.gamma, V=p.V, kind="zipf",
+                            draft_sigma=p.draft_sigma)
+    x = _drafts(v, p.temperature)
+    toks, n = run_verify(v, x, p.temperature)
+    c = check(v, x, p.temperature, toks, n)
+    assert c["exact"] >= p.B - 1
+
+
+@pytest.mark.parametrize("sigma", [0.5, 1.0, 2.0])
+def test_verify_qwen30b_shape_sampling(sigma):
+    p = synth.PRESETS["qwen30b"]
+    v = synth.verify_logits(p.seed + int(sigma * 10), B=p.B, gamma=p.gamma, V=p.V, kind="zipf",
+                            draft_sigma=sigma)
+    x = _drafts(v, p.temperature)
+    toks, n = run_verify(v, x, p.temperature)
+    c = check(v, x, p.temperature, toks, n)
+    assert c["exact"] >= p.B - 2
