@@ -1,0 +1,556 @@
+#!/usr/bin/env python3
+"""Benchmark of the drafter-head + verifier hot path on GB300.
+
+One step is one speculative round of the Llama-3.1-8B-shaped workload
+(d=4096, r=512, V=128256, M=8 sequences, gamma=6, greedy): gamma low-rank head
+calls (each M rows -> M drafted tokens; the drafter backbone between them is
+out of scope, so each call gets its own synthetic hidden states) followed by
+one greedy verification of the M sequences.  value = drafted tokens/s
+(gamma * M per step), whole job over all ranks.
+
+Inputs are resident in HBM; W_up is rotated over gamma copies (one per head
+call) so every weight read of the timed region comes from HBM, not L2.
+The step is captured in a CUDA graph and replayed.  The dominant kernel's
+roofline comes from CUDA events recorded around each library launch on its
+own stream (an eager profiled pass right after the timed region).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the only reference this build has) on
+the host cores, a bounded sample of the same workload per step.
+Multi-GPU: replicas only (the round has no exchange step); one process per
+GPU under torchrun, barrier + max-over-ranks timing.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "drafter head+sample tokens/s at V=128K-201K; verify steps/s; % of HBM roofline"
+UNIT = "drafted tokens/s"
+WORKLOADS = {
+    # name: (d, r, V, M, gamma, temperature)
+    "llama8b": (4096, 512, 128256, 8, 6, 0.0),
+    "gptoss20b": (2880, 360, 201088, 16, 6, 0.7),
+    "qwen30b": (2048, 256, 151936, 256, 4, 1.0),
+}
+WORKLOAD_DESC = {
+    "llama8b": "Llama-3.1-8B-shaped speculative round: 6 low-rank head calls (M=8) + greedy verify (B=8)",
+    "gptoss20b": "GPT-OSS-20B-shaped speculative round: 6 low-rank head calls (M=16, T=0.7) + sampling verify (B=16)",
+    "qwen30b": "Qwen3-30B-A3B-shaped speculative round: 1 low-rank head call (M=256, T=1) + sampling verify (B=64)",
+}
+
+
+# ----------------------------------------------------------------- ranks ---
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def aggregate(units_local: float, seconds_local: float, world: int):
+    """Whole-job (units, seconds): units summed over ranks, time = max over ranks."""
+    if world <= 1:
+        return units_local, seconds_local
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" \
+        else torch.device("cpu")
+    t = torch.tensor([seconds_local], dtype=torch.float64, device=dev)
+    u = torch.tensor([units_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(u.item()), float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks ---
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons every 200 ms."""
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-i", str(gpu_index), "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.th = threading.Thread(target=self._read, daemon=True)
+            self.th.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        rows = []
+        for ts, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        inside = [p for ts, p in rows if t0 <= ts <= t1 + 0.25] or [p for _, p in rows]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"],
+                    "samples": 0}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ------------------------------------------------------------ workload -----
+def make_inputs(name: str, seed: int, dev):
+    """Seeded synthetic tensors on the device: bf16 weights N(0, 1/fan_in),
+    hidden states N(0, 1), Zipf-like target logits (-1.1 ln rank over a random
+    permutation + N(0, 0.25)), draft logits = target + N(0, 1)."""
+    import torch
+    d, r, V, M, gamma, T = WORKLOADS[name]
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    n_calls = gamma if name != "qwen30b" else 1
+    n_copies = max(n_calls, 2)
+    w_down = (torch.randn(r, d, generator=g, device=dev) / d ** 0.5).to(torch.bfloat16)
+    w_ups = [(torch.randn(V, r, generator=g, device=dev) / r ** 0.5).to(torch.bfloat16)
+             for _ in range(n_copies)]
+    hidden = [torch.randn(M, d, generator=g, device=dev).to(torch.bfloat16)
+              for _ in range(n_calls)]
+    u_head = [torch.rand(M, generator=g, device=dev) for _ in range(n_calls)]
+    B = M if name != "qwen30b" else 64
+    ranks = torch.argsort(torch.rand(B * (gamma + 1), V, generator=g, device=dev), dim=1)
+    target = (-1.1 * torch.log(ranks.float() + 1.0)
+              + 0.5 * torch.randn(B * (gamma + 1), V, generator=g, device=dev))
+    target = target.reshape(B, gamma + 1, V).contiguous()
+    del ranks
+    draft = (target[:, :gamma] + torch.randn(B, gamma, V, generator=g, device=dev)).contiguous()
+    if T > 0:
+        probs = torch.softmax(draft / T, dim=2).reshape(B * gamma, V)
+        tokens = torch.multinomial(probs, 1, generator=g).reshape(B, gamma).to(torch.int32)
+        del probs
+    else:
+        tokens = torch.argmax(draft, dim=2).to(torch.int32)
+    u_verify = torch.rand(B, gamma + 1, generator=g, device=dev)
+    return dict(d=d, r=r, V=V, M=M, B=B, gamma=gamma, T=T, n_calls=n_calls, w_down=w_down,
+                w_ups=w_ups, hidden=hidden, u_head=u_head, target=target,
+                draft=draft if T > 0 else None, tokens=tokens, u_verify=u_verify)
+
+
+class Round:
+    """Preallocated outputs / workspaces and the step as a sequence of library
+    calls on the current stream."""
+
+    def __init__(self, x, ss):
+        import torch
+        self.x, self.ss = x, ss
+        dev = x["w_down"].device
+        M, d, r, V, B, gamma = x["M"], x["d"], x["r"], x["V"], x["B"], x["gamma"]
+        self.head_ws = torch.empty(ss.slimspec_head_workspace_size(M, d, r, V, ss.SS_BF16),
+                                   dtype=torch.uint8, device=dev)
+        self.ver_ws = torch.empty(max(256, ss.spec_verify_workspace_size(B, gamma, V, x["T"])),
+                                  dtype=torch.uint8, device=dev)
+        self.head_out = [{"tokens": torch.empty(M, dtype=torch.int32, device=dev)}
+                         for _ in range(x["n_calls"])]
+        self.ver_out = {"tokens": torch.empty(B, gamma + 1, dtype=torch.int32, device=dev),
+                        "num_accepted": torch.empty(B, dtype=torch.int32, device=dev)}
+
+    def step(self):
+        x, ss = self.x, self.ss
+        T = x["T"]
+        for j in range(x["n_calls"]):
+            ss.slimspec_head_forward(x["hidden"][j], x["w_down"], x["w_ups"][j % len(x["w_ups"])],
+                                     T, x["u_head"][j] if T > 0 else None, want_stats=False,
+                                     workspace=self.head_ws, out=self.head_out[j])
+        ss.spec_verify(x["target"], x["draft"], x["tokens"], T,
+                       x["u_verify"] if T > 0 else None, workspace=self.ver_ws,
+                       out=self.ver_out)
+
+
+def head_stream_bytes(x) -> float:
+    """Algorithmic bytes of one k_head_stream launch: the W_up stream (V*r*2),
+    the z rows it multiplies (M*r*2) and its partials (M * ceil(V/32) * 12)."""
+    M, r, V = x["M"], x["r"], x["V"]
+    n_sub = -(-V // 32)
+    return V * r * 2 + M * r * 2 + M * n_sub * 12
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """Per-launch DRAM bytes from the committed ncu summary of this kernel, or
+    None when there is none or the kernel source changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "speculative_decoding_drafter_slimspec_gb300", "csrc", "head.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if fields.get("source_sha256") != sha:
+        return None
+    try:
+        return float(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        p = json.load(open(path))
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+# ------------------------------------------------------------ CPU oracle ---
+def oracle_round_rate(x_np: dict, budget_s: float, max_steps: int | None = None,
+                      steps_exact: int | None = None):
+    """Drafted tokens/s of the CPU oracle on bounded samples of the round.
+
+    A sample is one head row (all of W_up's first S rows) plus one verified
+    sequence over the same S vocabulary entries; its time is scaled by V/S and
+    by the round's gamma*M head rows and B sequences.  S is the largest slice
+    whose sample fits the per-step budget.  Returns (rate, steps, S, seconds)."""
+    import oracle
+    V, M, B, gamma, T = x_np["V"], x_np["M"], x_np["B"], x_np["gamma"], x_np["T"]
+    n_rows = x_np["n_calls"] * M
+
+    def sample(S):
+        t0 = time.perf_counter()
+        oracle.slimspec_head(x_np["hidden"][:1], x_np["w_down"], x_np["w_up"][:S], "bf16", T,
+                             x_np["u_head"][:1] if T > 0 else None)
+        t1 = time.perf_counter()
+        tg = x_np["target"][:1, :, :S]
+        dr = x_np["draft"][:1, :, :S] if T > 0 else None
+        tok = np.minimum(x_np["tokens"][:1], S - 1)
+        oracle.verify_batch(tg, dr, tok, x_np["u_verify"][:1] if T > 0 else None, T)
+        t2 = time.perf_counter()
+        return t1 - t0, t2 - t1
+
+    th, tv = sample(V)          # calibration on the full row (untimed)
+    full = th + tv
+    per_step = budget_s if steps_exact is None else budget_s / max(1, steps_exact)
+    S = V if full <= per_step else max(1024, int(V * per_step / full))
+    steps = steps_exact if steps_exact is not None else max(1, min(max_steps or 10 ** 9,
+                                                                  int(budget_s / max(1e-9, full * S / V))))
+    tot_h = tot_v = 0.0
+    for _ in range(steps):
+        a, b = sample(S)
+        tot_h += a
+        tot_v += b
+    round_s = (tot_h / steps * n_rows + tot_v / steps * B) * (V / S)
+    return n_rows / round_s, steps, S, tot_h + tot_v
+
+
+def numpy_inputs(x):
+    import torch
+    return dict(V=x["V"], M=x["M"], B=x["B"], gamma=x["gamma"], T=x["T"], n_calls=x["n_calls"],
+                hidden=x["hidden"][0].float().cpu().numpy(),
+                w_down=x["w_down"].float().cpu().numpy(),
+                w_up=x["w_ups"][0].float().cpu().numpy(),
+                u_head=x["u_head"][0].cpu().numpy(),
+                target=x["target"].cpu().numpy(),
+                draft=x["draft"].cpu().numpy() if x["draft"] is not None else None,
+                tokens=x["tokens"].cpu().numpy(), u_verify=x["u_verify"].cpu().numpy())
+
+
+def cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------- arms ---
+def run_reference(args, world, rank):
+    """CPU oracle arm: rank 0 alone times K steps (after W) of bounded samples."""
+    if rank != 0:
+        return
+    import torch
+    # inputs built on the CPU with the same recipe (no GPU needed for this arm)
+    dev = torch.device("cpu")
+    x = make_inputs(args.workload, 1234, dev)
+    x_np = numpy_inputs(x)
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    oracle_round_rate(x_np, budget * max(1, args.warmup), steps_exact=max(1, args.warmup))
+    rate, steps, S, secs = oracle_round_rate(x_np, budget * args.steps, steps_exact=args.steps)
+    d, r, V, M, gamma, T = WORKLOADS[args.workload]
+    sample = (f"per step: 1 head row + 1 verified sequence over {S} of {V} vocabulary rows, "
+              f"scaled to the round ({x['n_calls'] * M} head rows + {x['B']} sequences)")
+    line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": 1,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * x["n_calls"] * M / rate, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(args.workload),
+            "cpu_baseline": {"value": rate, "unit": UNIT, "cores": cores(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": rate, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def config_dict(workload):
+    d, r, V, M, gamma, T = WORKLOADS[workload]
+    return {"workload": WORKLOAD_DESC[workload], "d": d, "r": r, "V": V, "M": M,
+            "gamma": gamma, "temperature": T, "parallelism": "replicas",
+            "l2": "W_up rotated over one copy per head call and the round reads "
+                  ">750 MB between re-reads; inputs larger than L2"}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    import speculative_decoding_drafter_slimspec_gb300 as ss
+    import __graft_entry__
+    __graft_entry__.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    x = make_inputs(args.workload, 1234 + rank, dev)
+    rnd = Round(x, ss)
+    stream = torch.cuda.Stream(device=dev)
+    units_per_step = x["n_calls"] * x["M"]
+
+    # warm-up eagerly (also sets kernel attributes before capture)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            rnd.step()
+    stream.synchronize()
+    assert ss.ss_get_device_error() == ss.SS_OK
+
+    graph = torch.cuda.CUDAGraph()
+    n0 = ss.launch_count()
+    with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+        rnd.step()
+    launches_per_step = ss.launch_count() - n0
+
+    sampler = ClockSampler(local) if not args.no_clocks else None
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            graph.replay()
+    stream.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(args.steps):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    wall1 = time.time()
+    torch.cuda.synchronize()
+    barrier(world)
+    if sampler:
+        sampler.stop()
+    sec_local = e0.elapsed_time(e1) / 1000.0
+    units, secs = aggregate(units_per_step * args.steps, sec_local, world)
+    value = units / secs
+    assert ss.ss_get_device_error() == ss.SS_OK
+
+    # eager profiled pass: per-kernel device time from events on the stream
+    ss.profile_start()
+    n_prof = min(50, max(5, args.steps))
+    with torch.cuda.stream(stream):
+        for _ in range(n_prof):
+            rnd.step()
+    stream.synchronize()
+    ss.profile_stop()
+    prof = ss.profile_read()
+
+    # end to end through the public API with host buffers
+    e2e = run_e2e(args, x, ss, stream, world) if not args.no_e2e else None
+
+    if rank != 0:
+        return
+    kern = {}
+    total_ms = sum(ms for _, ms in prof.values())
+    for name, (n, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
+        kern[name] = {"launches_per_step": n / n_prof, "us_per_launch": 1000.0 * ms / n,
+                      "share": ms / total_ms}
+    hs = prof.get("k_head_stream")
+    peak, peak_kind = measured_peaks()
+    roof = None
+    if hs:
+        dur = hs[1] / hs[0] / 1000.0
+        nbytes = head_stream_bytes(x)
+        ach = nbytes / dur / 1e9
+        roof = {"kernel": "k_head_stream", "bound": "hbm", "achieved": ach, "peak": peak,
+                "unit": "GB/s", "frac": ach / peak,
+                "traffic": profiled_traffic("k_head_stream", args.workload),
+                "algorithmic_bytes_per_launch": nbytes, "peak_source": peak_kind,
+                "us_per_launch": dur * 1e6}
+    ver_ms = sum(ms for name, (n, ms) in prof.items() if name.startswith("k_verify")) / n_prof
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1000.0 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded N(0,1/fan_in) bf16 weights, N(0,1) hidden states, "
+                    "Zipf-like target logits",
+            "config": config_dict(args.workload), "roofline": roof,
+            "gpu_launches": int(launches_per_step * args.steps),
+            "verify_steps_per_s": (1000.0 / ver_ms) if ver_ms > 0 else None,
+            "kernels": kern}
+    if sampler:
+        line["clocks"] = sampler.summary(wall0, wall1)
+    if e2e:
+        line["e2e"] = e2e
+    if world == 1 and not args.no_cpu_baseline:
+        x_np = numpy_inputs(x)
+        rate, steps, S, secs_cpu = oracle_round_rate(x_np, args.cpu_budget)
+        line["cpu_baseline"] = {
+            "value": rate, "unit": UNIT, "cores": cores(), "kind": "oracle",
+            "sample": f"{steps} samples of 1 head row + 1 verified sequence over {S} of "
+                      f"{x['V']} vocabulary rows ({secs_cpu:.1f} s of CPU work), scaled to the "
+                      f"round ({units_per_step} head rows + {x['B']} sequences)"}
+    print(json.dumps(line), flush=True)
+
+
+def run_e2e(args, x, ss, stream, world):
+    """Same round through the Python API with pinned host inputs copied in and
+    the tokens copied out inside the timed region, every step."""
+    import torch
+    dev = x["w_down"].device
+    h_host = [h.cpu().pin_memory() for h in x["hidden"]]
+    u_host = [u.cpu().pin_memory() for u in x["u_head"]]
+    t_host = x["target"].cpu().pin_memory()
+    k_host = x["tokens"].cpu().pin_memory()
+    uv_host = x["u_verify"].cpu().pin_memory()
+    d_host = x["draft"].cpu().pin_memory() if x["draft"] is not None else None
+    out_host = torch.empty(x["n_calls"] * x["M"] + x["B"] * (x["gamma"] + 1) + x["B"],
+                           dtype=torch.int32).pin_memory()
+    T = x["T"]
+    h_dev = [torch.empty_like(h) for h in x["hidden"]]
+    u_dev = [torch.empty_like(u) for u in x["u_head"]]
+    t_dev = torch.empty_like(x["target"])
+    k_dev = torch.empty_like(x["tokens"])
+    uv_dev = torch.empty_like(x["u_verify"])
+    d_dev = torch.empty_like(x["draft"]) if x["draft"] is not None else None
+    rnd = Round(x, ss)
+    res = torch.empty_like(out_host, device=dev)
+
+    def step():
+        for j in range(x["n_calls"]):
+            h_dev[j].copy_(h_host[j], non_blocking=True)
+            if T > 0:
+                u_dev[j].copy_(u_host[j], non_blocking=True)
+        t_dev.copy_(t_host, non_blocking=True)
+        k_dev.copy_(k_host, non_blocking=True)
+        if T > 0:
+            uv_dev.copy_(uv_host, non_blocking=True)
+            d_dev.copy_(d_host, non_blocking=True)
+        off = 0
+        for j in range(x["n_calls"]):
+            o = ss.slimspec_head_forward(h_dev[j], x["w_down"], x["w_ups"][j % len(x["w_ups"])],
+                                         T, u_dev[j] if T > 0 else None, want_stats=False,
+                                         workspace=rnd.head_ws, out=rnd.head_out[j])
+            res[off:off + x["M"]].copy_(o["tokens"])
+            off += x["M"]
+        v = ss.spec_verify(t_dev, d_dev, k_dev, T, uv_dev if T > 0 else None,
+                           workspace=rnd.ver_ws, out=rnd.ver_out)
+        n = x["B"] * (x["gamma"] + 1)
+        res[off:off + n].copy_(v["tokens"].reshape(-1))
+        res[off + n:].copy_(v["num_accepted"])
+        out_host.copy_(res, non_blocking=True)
+
+    n_steps = min(args.steps, args.e2e_steps)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            step()
+    stream.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(n_steps):
+            step()
+        e1.record(stream)
+    stream.synchronize()
+    barrier(world)
+    units, secs = aggregate(x["n_calls"] * x["M"] * n_steps, e0.elapsed_time(e1) / 1000.0, world)
+    h2d = sum(h.numel() * h.element_size() for h in x["hidden"]) + \
+        x["target"].numel() * 4 + x["tokens"].numel() * 4
+    if T > 0:
+        h2d += sum(u.numel() * 4 for u in x["u_head"]) + x["u_verify"].numel() * 4 + \
+            x["draft"].numel() * 4
+    return {"value": units / secs, "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(out_host.numel() * 4), "steps": n_steps}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama8b")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-clocks", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup()
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -111,7 +111,7 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
  *           (T == 0) or the inverse-CDF draw with uniforms[m] over the
  *           candidates in ascending id order.
  *  hidden M x d, w_down d' x d, w_vocab V x d', u_full V x d (all bf16)
- *  d % 8 == 0, d' % 8 == 0, d' <= 1024, d <= 8192, 1 <= k <= min(V, 4096)
+ *  d % 8 == 0, d' % 8 == 0, d' <= 1024, d <= 4096, 1 <= k <= min(V, 4096)
  *  out_tokens    M int32 (required)
  *  out_topk_idx  M x k int32 candidate ids, ascending            (nullable)
  *  out_topk_prob M x k float q over the candidates (T > 0)       (nullable)
@@ -162,6 +162,22 @@ int spec_verify(const float* target_logits, const float* draft_logits,
                 float temperature, const float* uniforms, int32_t* out_tokens,
                 int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
                 cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Instrumentation (no counterpart in the articles; used by the benchmark).
+ *
+ * ss_launch_count: kernels this library has launched in this process.
+ * ss_profile_start / ss_profile_stop: while on, each launch is bracketed by
+ *   two CUDA events recorded on its stream (host cost: two event records).
+ * ss_profile_read: synchronises on the recorded events and writes, for kernel
+ *   kind 0 .. n_kinds-1, the number of timed launches and their summed device
+ *   time in ms; then forgets the records.  ss_profile_kind_name names a kind.
+ * ------------------------------------------------------------------------ */
+long long ss_launch_count(void);
+int ss_profile_start(void);
+int ss_profile_stop(void);
+int ss_profile_read(int* launches, double* total_ms, int n_kinds);
+const char* ss_profile_kind_name(int kind);
 
 #ifdef __cplusplus
 }

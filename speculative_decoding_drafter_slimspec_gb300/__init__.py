@@ -53,6 +53,11 @@ _SIGS = {
     "ss_topk_rows": (_i, [_vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "spec_verify_workspace_size": (_sz, [_i, _i, _i, _f]),
     "spec_verify": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "ss_launch_count": (ctypes.c_longlong, []),
+    "ss_profile_start": (_i, []),
+    "ss_profile_stop": (_i, []),
+    "ss_profile_read": (_i, [_vp, _vp, _i]),
+    "ss_profile_kind_name": (ctypes.c_char_p, [_i]),
 }
 
 
@@ -72,7 +77,7 @@ def header_functions() -> list:
     """Names of the functions declared in include/slimspec.h."""
     src = open(_HEADER).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(?:int|size_t|const char\*)\s+(\w+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(?:int|size_t|long long|const char\*)\s+(\w+)\s*\(", src)))
 
 
 def lib() -> ctypes.CDLL:
@@ -165,14 +170,18 @@ def slimspec_head_forward(hidden, w_down, w_up, temperature=0.0, uniforms=None, 
     code = _dtype_code(hidden)
     dev = hidden.device
     o = dict(out or {})
-    o.setdefault("tokens", torch.empty(M, dtype=torch.int32, device=dev))
+    if "tokens" not in o:
+        o["tokens"] = torch.empty(M, dtype=torch.int32, device=dev)
     if want_stats:
         for k in ("logprob", "row_max", "lse"):
-            o.setdefault(k, torch.empty(M, dtype=torch.float32, device=dev))
+            if k not in o:
+                o[k] = torch.empty(M, dtype=torch.float32, device=dev)
     if want_z:
-        o.setdefault("z", torch.empty(M, r, dtype=hidden.dtype, device=dev))
+        if "z" not in o:
+            o["z"] = torch.empty(M, r, dtype=hidden.dtype, device=dev)
     if want_logits:
-        o.setdefault("logits", torch.empty(M, V, dtype=torch.float32, device=dev))
+        if "logits" not in o:
+            o["logits"] = torch.empty(M, V, dtype=torch.float32, device=dev)
     nbytes = slimspec_head_workspace_size(M, d, r, V, code)
     ws = _workspace(nbytes, dev, workspace)
     st = lib().slimspec_head_forward(
@@ -196,13 +205,17 @@ def specvocab_head_forward(hidden, w_down, w_vocab, u_full, k, temperature=0.0, 
         raise ValueError("shape mismatch")
     dev = hidden.device
     o = dict(out or {})
-    o.setdefault("tokens", torch.empty(M, dtype=torch.int32, device=dev))
+    if "tokens" not in o:
+        o["tokens"] = torch.empty(M, dtype=torch.int32, device=dev)
     if want_topk:
-        o.setdefault("topk_idx", torch.empty(M, k, dtype=torch.int32, device=dev))
+        if "topk_idx" not in o:
+            o["topk_idx"] = torch.empty(M, k, dtype=torch.int32, device=dev)
     if want_prob:
-        o.setdefault("topk_prob", torch.empty(M, k, dtype=torch.float32, device=dev))
+        if "topk_prob" not in o:
+            o["topk_prob"] = torch.empty(M, k, dtype=torch.float32, device=dev)
     if want_scores:
-        o.setdefault("scores", torch.empty(M, V, dtype=torch.float32, device=dev))
+        if "scores" not in o:
+            o["scores"] = torch.empty(M, V, dtype=torch.float32, device=dev)
     nbytes = specvocab_head_workspace_size(M, d, dp, V, k)
     ws = _workspace(nbytes, dev, workspace)
     st = lib().specvocab_head_forward(
@@ -232,8 +245,10 @@ def spec_verify(target_logits, draft_logits, draft_tokens, temperature=0.0, unif
     gamma = g1 - 1
     dev = target_logits.device
     o = dict(out or {})
-    o.setdefault("tokens", torch.empty(B, g1, dtype=torch.int32, device=dev))
-    o.setdefault("num_accepted", torch.empty(B, dtype=torch.int32, device=dev))
+    if "tokens" not in o:
+        o["tokens"] = torch.empty(B, g1, dtype=torch.int32, device=dev)
+    if "num_accepted" not in o:
+        o["num_accepted"] = torch.empty(B, dtype=torch.int32, device=dev)
     nbytes = spec_verify_workspace_size(B, gamma, V, temperature)
     ws = _workspace(nbytes, dev, workspace)
     st = lib().spec_verify(
@@ -242,6 +257,33 @@ def spec_verify(target_logits, draft_logits, draft_tokens, temperature=0.0, unif
         _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "spec_verify")
     return o
+
+
+N_KERNEL_KINDS = 11
+
+
+def launch_count() -> int:
+    """Kernels launched by the library so far in this process."""
+    return int(lib().ss_launch_count())
+
+
+def profile_start():
+    _check(lib().ss_profile_start(), "ss_profile_start")
+
+
+def profile_stop():
+    _check(lib().ss_profile_stop(), "ss_profile_stop")
+
+
+def profile_read() -> dict:
+    """{kernel name: (timed launches, summed ms)} since the last read."""
+    n = N_KERNEL_KINDS
+    launches = (ctypes.c_int * n)()
+    ms = (ctypes.c_double * n)()
+    _check(lib().ss_profile_read(ctypes.cast(launches, ctypes.c_void_p),
+                                 ctypes.cast(ms, ctypes.c_void_p), n), "ss_profile_read")
+    return {lib().ss_profile_kind_name(k).decode(): (launches[k], ms[k])
+            for k in range(n) if launches[k]}
 
 
 def ss_get_device_error(stream=None) -> int:

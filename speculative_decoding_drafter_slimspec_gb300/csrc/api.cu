@@ -36,8 +36,10 @@ static size_t head_ws_bytes(int M, int r, int V, bool bf16) {
   const HeadPlan plan = head_plan(bf16, r, M, V);
   if (!plan.ok) return 0;
   size_t s = 0;
-  s += align256((size_t)M * r * sizeof(float));
+  s += align256((size_t)M * r * (bf16 ? 2 : 4));
   s += 3 * align256((size_t)M * plan.n_sub * sizeof(float));
+  s += 3 * align256((size_t)M * plan.grid * sizeof(float));
+  s += align256((size_t)plan.n_launch * sizeof(unsigned));
   return s;
 }
 
@@ -113,18 +115,22 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
 
   const HeadPlan plan = head_plan(bf16, r, M, V);
   Carver cv(workspace);
-  float* z_ws = cv.take<float>((size_t)M * r);
+  void* z_ws = cv.take<uint8_t>((size_t)M * r * (bf16 ? 2 : 4));
   HeadPartials part;
   part.pmax = cv.take<float>((size_t)M * plan.n_sub);
   part.psum = cv.take<float>((size_t)M * plan.n_sub);
   part.parg = cv.take<int>((size_t)M * plan.n_sub);
+  part.cmax = cv.take<float>((size_t)M * plan.grid);
+  part.csum = cv.take<float>((size_t)M * plan.grid);
+  part.carg = cv.take<int>((size_t)M * plan.grid);
+  part.ctr = cv.take<unsigned>((size_t)plan.n_launch);
+  const HeadOutputs outs{uniforms, out_tokens, out_logprob, out_row_max, out_row_lse};
 
-  cudaError_t e = launch_down_proj(bf16, hidden, w_down, M, d, r, bf16, z_ws, out_z, stream);
+  cudaError_t e = launch_down_proj(bf16, hidden, w_down, M, d, r, bf16, z_ws, out_z, part.ctr,
+                                   plan.n_launch, stream);
   if (e == cudaSuccess)
-    e = launch_head_stream(plan, bf16, w_up, z_ws, M, r, V, temperature, part, out_logits, stream);
-  if (e == cudaSuccess)
-    e = launch_head_finish(plan, bf16, w_up, z_ws, M, r, V, temperature, part, uniforms,
-                           out_tokens, out_logprob, out_row_max, out_row_lse, stream);
+    e = launch_head_stream(plan, bf16, w_up, z_ws, M, r, V, temperature, part, out_logits, outs,
+                           stream);
   return cuda_status(e);
 }
 

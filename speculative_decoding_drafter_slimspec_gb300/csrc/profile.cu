@@ -1,0 +1,117 @@
+// profile.cu -- optional kernel timing and launch counting for libslimspec.
+//
+// When enabled (ss_profile_start), every kernel launch of the library is
+// bracketed by two CUDA events recorded on the launching stream; the
+// benchmark reads per-kernel launch counts and summed durations back with
+// ss_profile_read.  A launch counter runs whether or not timing is enabled.
+// Disabled, the cost is one relaxed atomic increment per launch.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <mutex>
+#include <set>
+#include <utility>
+#include <vector>
+
+#include "../../include/slimspec.h"
+#include "ss_internal.h"
+
+namespace ss {
+
+static const char* const kKindNames[kKindCount] = {
+    "k_down_proj",   "k_head_stream", "k_head_finish", "k_verify_rows", "k_verify_decide",
+    "k_verify_resid", "k_verify_finish", "k_topk",      "k_gather_logits", "k_cand_finish",
+    "k_head_mma"};
+
+namespace {
+struct Rec {
+  int kind;
+  cudaEvent_t a, b;
+};
+std::mutex g_mu;
+std::atomic<bool> g_on{false};
+std::atomic<long long> g_launches{0};
+std::vector<Rec> g_recs;
+std::vector<cudaEvent_t> g_pool;
+
+cudaEvent_t take_event() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  cudaEventCreate(&e);
+  return e;
+}
+}  // namespace
+
+cudaError_t set_smem_once(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(mu);
+  if (done.count({kernel, dev})) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done.insert({kernel, dev});
+  return e;
+}
+
+ProfScope::ProfScope(int kind, cudaStream_t st) : slot(-1), stream(st) {
+  g_launches.fetch_add(1, std::memory_order_relaxed);
+  if (!g_on.load(std::memory_order_relaxed)) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  Rec r{kind, take_event(), take_event()};
+  if (!r.a || !r.b) return;
+  cudaEventRecord(r.a, st);
+  g_recs.push_back(r);
+  slot = (int)g_recs.size() - 1;
+}
+
+ProfScope::~ProfScope() {
+  if (slot < 0) return;
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (slot < (int)g_recs.size()) cudaEventRecord(g_recs[slot].b, stream);
+}
+
+}  // namespace ss
+
+using namespace ss;
+
+extern "C" {
+
+int ss_profile_start(void) {
+  g_on.store(true);
+  return SS_OK;
+}
+
+int ss_profile_stop(void) {
+  g_on.store(false);
+  return SS_OK;
+}
+
+long long ss_launch_count(void) { return g_launches.load(); }
+
+int ss_profile_read(int* launches, double* total_ms, int n_kinds) {
+  if (!launches || !total_ms || n_kinds < 1) return SS_ERR_INVALID_ARG;
+  std::lock_guard<std::mutex> lk(g_mu);
+  for (int k = 0; k < n_kinds; ++k) { launches[k] = 0; total_ms[k] = 0.0; }
+  int status = SS_OK;
+  for (const Rec& r : g_recs) {
+    if (cudaEventSynchronize(r.b) != cudaSuccess) { status = SS_ERR_CUDA; continue; }
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) { status = SS_ERR_CUDA; continue; }
+    if (r.kind < n_kinds) { launches[r.kind] += 1; total_ms[r.kind] += ms; }
+  }
+  for (const Rec& r : g_recs) { g_pool.push_back(r.a); g_pool.push_back(r.b); }
+  g_recs.clear();
+  return status;
+}
+
+const char* ss_profile_kind_name(int kind) {
+  return (kind >= 0 && kind < kKindCount) ? kKindNames[kind] : "unknown";
+}
+
+}  // extern "C"

@@ -283,6 +283,7 @@ size_t topk_ws_bytes(int M, int V, int k) { return 0; }
 cudaError_t launch_topk(const float* scores, int M, int V, int k, int32_t* out_idx, void* ws,
                         cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
+  ProfScope ps(kKTopk, st);
   k_topk<<<M, 1024, 0, st>>>(scores, V, k, out_idx);
   return cudaGetLastError();
 }
@@ -291,9 +292,12 @@ size_t specvocab_ws_bytes(int M, int d, int d_prime, int V, int k) {
   const HeadPlan plan = head_plan(true, d_prime, M, V);
   if (!plan.ok) return 0;
   size_t s = 0;
-  s += align256((size_t)M * d_prime * sizeof(float));      // h'
+  s += align256((size_t)M * d_prime * 2);                  // h' (bf16)
+  s += 3 * align256((size_t)M * plan.grid * sizeof(float));   // router CTA partials
   s += align256((size_t)M * V * sizeof(float));            // scores
   s += 3 * align256((size_t)M * plan.n_sub * sizeof(float));  // router partials (unused values)
+  s += align256((size_t)plan.n_launch * sizeof(unsigned));    // router completion counters
+  s += align256((size_t)M * sizeof(int32_t));                 // router argmax (unused)
   s += align256((size_t)M * k * sizeof(int32_t));          // candidates
   s += align256((size_t)M * k * sizeof(float));            // candidate logits
   return s;
@@ -307,24 +311,34 @@ cudaError_t launch_specvocab(const void* h, const void* w_down, const void* w_vo
   if (M <= 0) return cudaSuccess;
   const HeadPlan plan = head_plan(true, d_prime, M, V);
   Carver cv(ws);
-  float* hp = cv.take<float>((size_t)M * d_prime);
+  void* hp = cv.take<uint8_t>((size_t)M * d_prime * 2);
   float* scores = cv.take<float>((size_t)M * V);
   HeadPartials part;
   part.pmax = cv.take<float>((size_t)M * plan.n_sub);
   part.psum = cv.take<float>((size_t)M * plan.n_sub);
   part.parg = cv.take<int>((size_t)M * plan.n_sub);
+  part.cmax = cv.take<float>((size_t)M * plan.grid);
+  part.csum = cv.take<float>((size_t)M * plan.grid);
+  part.carg = cv.take<int>((size_t)M * plan.grid);
+  part.ctr = cv.take<unsigned>((size_t)plan.n_launch);
+  int32_t* router_arg = cv.take<int32_t>((size_t)M);
   int32_t* cand = cv.take<int32_t>((size_t)M * k);
   float* zc = cv.take<float>((size_t)M * k);
   if (out_scores) scores = out_scores;
+  const HeadOutputs router_out{nullptr, router_arg, nullptr, nullptr, nullptr};
 
-  cudaError_t e = launch_down_proj(true, h, w_down, M, d, d_prime, true, hp, nullptr, st);
+  cudaError_t e = launch_down_proj(true, h, w_down, M, d, d_prime, true, hp, nullptr, part.ctr,
+                                   plan.n_launch, st);
   if (e != cudaSuccess) return e;
-  e = launch_head_stream(plan, true, w_vocab, hp, M, d_prime, V, 0.f, part, scores, st);
+  e = launch_head_stream(plan, true, w_vocab, hp, M, d_prime, V, 0.f, part, scores, router_out,
+                         st);
   if (e != cudaSuccess) return e;
   e = launch_topk(scores, M, V, k, cand, nullptr, st);
   if (e != cudaSuccess) return e;
   const dim3 grid(M, (k + 63) / 64);
   const int cpl = (d + 255) / 256;
+  {
+  ProfScope ps(kKGather, st);
   if (cpl <= 4)
     k_gather_logits<4><<<grid, 256, 0, st>>>((const uint8_t*)h, (const uint8_t*)u_full, cand, M,
                                               d, k, V, zc);
@@ -334,7 +348,9 @@ cudaError_t launch_specvocab(const void* h, const void* w_down, const void* w_vo
   else
     k_gather_logits<16><<<grid, 256, 0, st>>>((const uint8_t*)h, (const uint8_t*)u_full, cand,
                                                M, d, k, V, zc);
+  }
   const float c = temperature > 0.f ? (float)(1.4426950408889634 / (double)temperature) : 0.f;
+  ProfScope ps(kKCandFinish, st);
   k_cand_finish<<<M, 256, 0, st>>>(zc, cand, k, c, uniforms, out_tokens, out_idx, out_prob);
   return cudaGetLastError();
 }

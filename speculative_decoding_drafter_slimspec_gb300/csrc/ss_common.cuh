@@ -91,9 +91,40 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       : "memory");
 }
 
+// ----------------------------------------------- programmatic dependent launch --
+// The producer lets its dependent grid start early; the dependent waits for
+// the producer's memory operations before its first read of them.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_producer() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // --------------------------------------------------------------- numerics --
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// d = a * b + c with a, b the low (or high) bf16 halves of two 32-bit words and
+// c, d fp32, rounded once (fma.rn.f32.bf16, sm_100+).  A bf16 x bf16 product
+// is exact in fp32, so this equals fmaf on the widened operands; it saves the
+// widening instructions and issues at the scalar FFMA rate.
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
+      : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
+      "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
+      : "=f"(d) : "r"(a), "r"(b), "f"(c));
+  return d;
+}
 
 // Round-to-nearest-even of an fp32 value to bf16, returned as fp32 and as bits.
 __device__ __forceinline__ uint16_t f32_to_bf16_bits(float x) {
@@ -190,6 +221,47 @@ struct ReduceScatter {
 };
 
 constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x / 2); }
+
+// Select-free reduce-scatter.  Each lane must hold its N values in the
+// lane-permuted slot order slot s <-> index s ^ mask, with
+//   mask = ((l % G) >> (log2 G - s)) << log2(max(N/G, 1))
+// (s, G as for ReduceScatter): at every step the half a lane keeps is then
+// its first half, and the partner's second half holds the same indices.
+// Afterwards v[i], i < max(N/G,1), holds the group-wide sum of index mask + i.
+template <int N, int O>
+struct ReduceScatterP {
+  static __device__ __forceinline__ void run(float* v) {
+    if constexpr (O == 0) {
+      return;
+    } else if constexpr (N > 1) {
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i)
+        v[i] = __fadd_rn(v[i], __shfl_xor_sync(0xFFFFFFFFu, v[i + N / 2], O));
+      ReduceScatterP<N / 2, O / 2>::run(v);
+    } else {
+      v[0] = __fadd_rn(v[0], __shfl_xor_sync(0xFFFFFFFFu, v[0], O));
+      ReduceScatterP<1, O / 2>::run(v);
+    }
+  }
+};
+
+// Fixed-order warp sum: tree toward lane 0, result broadcast from lane 0, so
+// every lane holds the same bits.
+__device__ __forceinline__ float warp_sum_fixed(float x) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) x = __fadd_rn(x, __shfl_down_sync(0xFFFFFFFFu, x, o));
+  return __shfl_sync(0xFFFFFFFFu, x, 0);
+}
+
+// Inclusive prefix sum across the 32 lanes in lane order (fixed order).
+__device__ __forceinline__ float warp_incl_scan(float x, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xFFFFFFFFu, x, o);
+    if (lane >= o) x = __fadd_rn(y, x);
+  }
+  return x;
+}
 
 // Orderable 32-bit key of a float: larger float <=> larger key; -0 == +0.
 __device__ __forceinline__ uint32_t float_key(float f) {

@@ -14,6 +14,25 @@ int sm_count();
 // Device address of the current device's error word (cached per device).
 unsigned* error_word();
 
+// Kernel kinds known to the optional profiler (profile.cu).
+enum KernelKind {
+  kKDownProj = 0, kKHeadStream, kKHeadFinish, kKVerifyRows, kKVerifyDecide, kKVerifyResid,
+  kKVerifyFinish, kKTopk, kKGather, kKCandFinish, kKHeadMma, kKindCount
+};
+
+// Counts one launch and, while profiling is on, brackets it with two events
+// recorded on `st`.  Construct immediately before the launch, destroy after.
+struct ProfScope {
+  int slot;
+  cudaStream_t stream;
+  ProfScope(int kind, cudaStream_t st);
+  ~ProfScope();
+};
+
+// Sets a kernel's dynamic shared memory limit once per (kernel, device), so
+// that no attribute call happens while a stream is being captured later.
+cudaError_t set_smem_once(const void* kernel, int bytes);
+
 // Rounds a byte count up to the 256-byte workspace granule.
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -33,32 +52,45 @@ struct Carver {
 // ------------------------------------------------------------------- head --
 // Geometry of the streaming up-projection for one (dtype, r, M) request.
 struct HeadPlan {
-  int lpr, cpl, mt;     // lanes per row, 16-byte chunks per lane, rows of z per pass
+  int lpr, cpl;         // lanes per row, 16-byte chunks per lane
+  int mtw, split, mt;   // rows of z per warp, warps per ring, rows of z per launch
   int sub_rows;         // vocabulary rows per partial (the recompute unit)
-  int n_sub;            // ceil(V / sub_rows)
+  int units;            // row ranges (one ring each) per CTA
+  int grid;             // CTAs of the stream kernel (at most one per SM)
+  int n_sub;            // partials per row of z: 8 * grid warp ranges x sub-tiles each
+  int n_launch;         // ceil(M / mt) launches of the stream kernel
   bool ok;
 };
 HeadPlan head_plan(bool bf16, int r, int M, int V);
 
-// Down-projection z = h W^T (M x r), written as fp32 to z_ws (rounded to bf16
-// values when `round_bf16`), and in the input dtype to out_z when non-null.
+// Down-projection z = h W^T (M x r), written in the input dtype (rounded to
+// nearest-even bf16 when `round_bf16`) to z_ws, and to out_z when non-null.
+// Also zeroes the n_ctr completion counters the stream kernel uses.
 cudaError_t launch_down_proj(bool bf16, const void* h, const void* w, int M, int d, int r,
-                             bool round_bf16, float* z_ws, void* out_z, cudaStream_t st);
+                             bool round_bf16, void* z_ws, void* out_z, unsigned* ctr, int n_ctr,
+                             cudaStream_t st);
 
-// Up-projection over all V rows with per-(row, sub-tile) softmax partials,
-// then the per-row merge and draw.
+// Up-projection over all V rows with per-(row, sub-tile) softmax partials;
+// the last CTA of each launch merges them and draws the tokens.
 struct HeadPartials {
-  float* pmax;
+  float* pmax;    // [M][n_sub] per vocabulary sub-tile
   float* psum;
   int* parg;
+  float* cmax;    // [M][grid] per CTA
+  float* csum;
+  int* carg;
+  unsigned* ctr;  // one completion counter per launch (zeroed by the down-projection)
+};
+struct HeadOutputs {
+  const float* uniforms;
+  int32_t* tokens;
+  float* logprob;
+  float* row_max;
+  float* row_lse;
 };
 cudaError_t launch_head_stream(const HeadPlan& plan, bool bf16, const void* w_up,
-                               const float* z_ws, int M, int r, int V, float temperature,
-                               HeadPartials part, float* out_logits, cudaStream_t st);
-cudaError_t launch_head_finish(const HeadPlan& plan, bool bf16, const void* w_up,
-                               const float* z_ws, int M, int r, int V, float temperature,
-                               HeadPartials part, const float* uniforms, int32_t* out_tokens,
-                               float* out_logprob, float* out_row_max, float* out_row_lse,
+                               const void* z_ws, int M, int r, int V, float temperature,
+                               HeadPartials part, float* out_logits, const HeadOutputs& out,
                                cudaStream_t st);
 
 // ---------------------------------------------------------------- verify --

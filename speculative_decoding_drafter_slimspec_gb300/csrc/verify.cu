@@ -21,7 +21,7 @@
 
 namespace ss {
 
-constexpr int kVChunk = 4096;  // floats per partial
+constexpr int kVChunk = 2048;  // floats per partial (8 KB: one round trip of 16 B x 16 per lane)
 
 struct VerifyInfo {
   int n;        // accepted drafted tokens
@@ -69,18 +69,16 @@ __global__ void __launch_bounds__(512)
     if (vec) {
       const float4* p4 = reinterpret_cast<const float4*>(src);
       const int q0 = lo >> 2, q1 = hi >> 2;
-      for (int base = q0; base < q1; base += 128) {
-        float4 a[4];
+      float4 a[16];
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int q = base + lane + 32 * k;
-          if (q < q1) a[k] = __ldcs(p4 + q);
-        }
+      for (int k = 0; k < 16; ++k) {
+        const int q = q0 + lane + 32 * k;
+        if (q < q1) a[k] = __ldcs(p4 + q);
+      }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int q = base + lane + 32 * k;
-          if (q < q1) push4<kSample>(s, a[k], q * 4, c);
-        }
+      for (int k = 0; k < 16; ++k) {
+        const int q = q0 + lane + 32 * k;
+        if (q < q1) push4<kSample>(s, a[k], q * 4, c);
       }
     } else {
       for (int i = lo + lane; i < hi; i += 32) row_state_push<kSample>(s, __ldcs(src + i), i, c);
@@ -113,56 +111,58 @@ __device__ __forceinline__ RowState warp_row_state(int row, int n_chunks, const 
 }
 
 // ------------------------------------------------------------------- K9 ----
+// One CTA per sequence.  Its warps merge the chunk partials of the sequence's
+// gamma+1 target rows (and gamma draft rows) in parallel; lane j of warp 0
+// then takes position j's decision, and the first failing position is found
+// with a ballot.
+constexpr int kMaxGamma = 32;
 template <bool kSample>
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(512)
     k_verify_decide(const float* __restrict__ target, const float* __restrict__ draft,
                     const int32_t* __restrict__ tokens, int B, int gamma, int V, float c,
                     int n_chunks, const float* __restrict__ vmax, const float* __restrict__ vsum,
                     const int* __restrict__ varg, const float* __restrict__ uniforms,
                     int32_t* __restrict__ out_tokens, int32_t* __restrict__ out_nacc,
                     VerifyInfo* __restrict__ info, unsigned* err) {
-  const int lane = threadIdx.x & 31;
-  const int b = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (b >= B) return;
+  __shared__ float s_mx[2 * kMaxGamma + 1], s_sum[2 * kMaxGamma + 1];
+  __shared__ int s_arg[2 * kMaxGamma + 1];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int b = blockIdx.x;
   const int g1 = gamma + 1;
   const int n_target_rows = B * g1;
-  int n = gamma, last = -1;
-  RowState P{}, Q{};
-  // every drafted token must be a vocabulary id, including those past the
-  // first rejection that the decision never reads
-  for (int i = lane; i < gamma; i += 32) {
-    const int x = tokens[(size_t)b * gamma + i];
-    if (x < 0 || x >= V) raise_error(err, kErrIndex);
+  const int rows = kSample ? g1 + gamma : g1;
+  for (int i = warp; i < rows; i += nw) {
+    const int row = i < g1 ? b * g1 + i : n_target_rows + b * gamma + (i - g1);
+    const RowState st = warp_row_state<kSample>(row, n_chunks, vmax, vsum, varg, c, lane);
+    if (lane == 0) { s_mx[i] = st.mx; s_sum[i] = st.sum; s_arg[i] = st.arg; }
   }
-  for (int j = 0; j < gamma; ++j) {
-    const int x = tokens[(size_t)b * gamma + j];
+  __syncthreads();
+  if (warp != 0) return;
+  // lane j < gamma: the decision at drafted position j
+  bool ok = true;
+  int x = 0;
+  if (lane < gamma) {
+    x = tokens[(size_t)b * gamma + lane];
     const bool bad = (x < 0 || x >= V);
-    P = warp_row_state<kSample>(b * g1 + j, n_chunks, vmax, vsum, varg, c, lane);
-    if (!kSample) {
-      if (bad || x != P.arg) { n = j; last = P.arg; break; }
+    if (bad) raise_error(err, kErrIndex);
+    if (bad) {
+      ok = false;
+    } else if (!kSample) {
+      ok = (x == s_arg[lane]);
     } else {
-      Q = warp_row_state<kSample>(n_target_rows + b * gamma + j, n_chunks, vmax, vsum, varg, c,
-                                  lane);
-      bool accept = false;
-      if (!bad) {
-        const float lp = target[((size_t)b * g1 + j) * V + x];
-        const float lq = draft[((size_t)b * gamma + j) * V + x];
-        const float px = __fdiv_rn(fast_exp2((lp - P.mx) * c), P.sum);
-        const float qx = __fdiv_rn(fast_exp2((lq - Q.mx) * c), Q.sum);
-        const float u = uniforms[(size_t)b * g1 + j];
-        accept = u * qx < px;
-      }
-      if (!accept) { n = j; break; }
+      const float lp = target[((size_t)b * g1 + lane) * V + x];
+      const float lq = draft[((size_t)b * gamma + lane) * V + x];
+      const float px = __fdiv_rn(fast_exp2((lp - s_mx[lane]) * c), s_sum[lane]);
+      const float qx = __fdiv_rn(fast_exp2((lq - s_mx[g1 + lane]) * c), s_sum[g1 + lane]);
+      ok = uniforms[(size_t)b * g1 + lane] * qx < px;
     }
   }
-  if (n == gamma) {
-    P = warp_row_state<kSample>(b * g1 + gamma, n_chunks, vmax, vsum, varg, c, lane);
-    last = P.arg;
-  }
+  const unsigned fail = __ballot_sync(0xFFFFFFFFu, lane < gamma && !ok);
+  const int n = fail ? __ffs(fail) - 1 : gamma;
   for (int i = lane; i < g1; i += 32) {
     int32_t t = -1;
     if (i < n) t = tokens[(size_t)b * gamma + i];
-    else if (i == n) t = kSample ? -1 : last;
+    else if (i == n) t = kSample ? -1 : s_arg[n];
     out_tokens[(size_t)b * g1 + i] = t;
   }
   if (lane == 0) {
@@ -171,10 +171,10 @@ __global__ void __launch_bounds__(128)
       VerifyInfo in{};
       in.n = n;
       in.mode = (n == gamma) ? 1 : 0;
-      in.pmx = P.mx;
-      in.pinv = __frcp_rn(P.sum);
-      in.qmx = (n == gamma) ? 0.f : Q.mx;
-      in.qinv = (n == gamma) ? 0.f : __frcp_rn(Q.sum);
+      in.pmx = s_mx[n];
+      in.pinv = __frcp_rn(s_sum[n]);
+      in.qmx = (n == gamma) ? 0.f : s_mx[g1 + n];
+      in.qinv = (n == gamma) ? 0.f : __frcp_rn(s_sum[g1 + n]);
       info[b] = in;
     }
   }
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(256)
                     const float* __restrict__ vsum, const VerifyInfo* __restrict__ info,
                     const float* __restrict__ rmass, const float* __restrict__ uniforms,
                     int32_t* __restrict__ out_tokens) {
-  constexpr int NT = 256, PER = kVChunk / NT;  // 16 elements per thread
+  constexpr int NT = 256, PER = kVChunk / NT;  // contiguous elements per thread
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g1 = gamma + 1;
   const VerifyInfo in = info[b];
@@ -357,26 +357,37 @@ cudaError_t launch_verify(const float* target, const float* draft, const int32_t
 
   const long long units = (long long)n_rows * n_chunks;
   const int grid = (int)std::max<long long>(1, std::min<long long>((units + 15) / 16, 4LL * sm_count()));
+  {
+  ProfScope ps(kKVerifyRows, st);
   if (sample)
     k_verify_rows<true><<<grid, 512, 0, st>>>(target, draft, n_target_rows, n_rows, V, c,
                                               n_chunks, vmax, vsum, varg);
   else
     k_verify_rows<false><<<grid, 512, 0, st>>>(target, draft, n_target_rows, n_rows, V, c,
                                                n_chunks, vmax, vsum, varg);
-  const int dgrid = (B + 3) / 4;
+  }
+  {
+  const int rows = sample ? 2 * gamma + 1 : gamma + 1;
+  const int dthreads = 32 * std::min(16, rows);
+  ProfScope ps(kKVerifyDecide, st);
   if (sample)
-    k_verify_decide<true><<<dgrid, 128, 0, st>>>(target, draft, tokens, B, gamma, V, c, n_chunks,
+    k_verify_decide<true><<<B, dthreads, 0, st>>>(target, draft, tokens, B, gamma, V, c, n_chunks,
                                                  vmax, vsum, varg, uniforms, out_tokens, out_nacc,
                                                  info, error_word());
   else
-    k_verify_decide<false><<<dgrid, 128, 0, st>>>(target, draft, tokens, B, gamma, V, c,
+    k_verify_decide<false><<<B, dthreads, 0, st>>>(target, draft, tokens, B, gamma, V, c,
                                                   n_chunks, vmax, vsum, varg, uniforms,
                                                   out_tokens, out_nacc, info, error_word());
+  }
   if (sample) {
     const long long ru = (long long)B * n_chunks;
     const int rgrid = (int)std::max<long long>(1, std::min<long long>((ru + 15) / 16, 4LL * sm_count()));
-    k_verify_resid<<<rgrid, 512, 0, st>>>(target, draft, B, gamma, V, c, n_chunks, vmax, vsum,
+    {
+      ProfScope ps(kKVerifyResid, st);
+      k_verify_resid<<<rgrid, 512, 0, st>>>(target, draft, B, gamma, V, c, n_chunks, vmax, vsum,
                                           info, rmass);
+    }
+    ProfScope ps(kKVerifyFinish, st);
     k_verify_finish<<<B, 256, 0, st>>>(target, draft, B, gamma, V, c, n_chunks, vmax, vsum, info,
                                        rmass, uniforms, out_tokens);
   }
