@@ -214,11 +214,10 @@ class Round:
 
 
 def head_stream_bytes(x) -> float:
-    """Algorithmic bytes of one k_head_stream launch: the W_up stream (V*r*2),
-    the z rows it multiplies (M*r*2) and its partials (M * ceil(V/32) * 12)."""
+    """Algorithmic bytes of one k_head_stream launch: the W_up stream (V*r*2)
+    and the bf16 z rows it multiplies (M*r*2).  Partials are overhead."""
     M, r, V = x["M"], x["r"], x["V"]
-    n_sub = -(-V // 32)
-    return V * r * 2 + M * r * 2 + M * n_sub * 12
+    return V * r * 2 + M * r * 2
 
 
 def profiled_traffic(kernel: str, workload: str):
