@@ -100,6 +100,32 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
                           size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * slimspec_head_forward without a workspace.  The articles have no
+ * counterpart: this serves callers that cannot allocate device memory (a
+ * runtime that fixes its device-memory budget at start-up, plugin code with
+ * no device allocator, a loop that cannot afford cudaMalloc's possible
+ * device-wide synchronisation).
+ *
+ * Same arguments, results and errors as slimspec_head_forward, minus the
+ * workspace.  The scratch is a fixed array of SS_NOALLOC_SCRATCH_BYTES inside
+ * the library, present on every GPU that loads it until the process exits.
+ * A request whose slimspec_head_workspace_size() exceeds that returns
+ * SS_ERR_WORKSPACE before anything is launched (on a 152-SM GB300 it fits up
+ * to M = 16 rows at V = 201088).  The first call on a device looks up the
+ * array's device address (cudaGetSymbolAddress) and caches it; make that
+ * first call before any stream capture.  All calls share the array and each
+ * leaves its contents behind: calls that overlap on the GPU race.  It
+ * allocates nothing.
+ * ------------------------------------------------------------------------ */
+#define SS_NOALLOC_SCRATCH_BYTES (4u << 20) /* 4 MiB */
+
+int slimspec_head_forward_noalloc(const void* hidden, const void* w_down, const void* w_up,
+                                  int M, int d, int r, int V, int dtype, float temperature,
+                                  const float* uniforms, int32_t* out_tokens,
+                                  float* out_logprob, float* out_row_max, float* out_row_lse,
+                                  void* out_z, float* out_logits, cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * SpecVocab-style dynamic-vocabulary drafter head (bf16 only).
  *
  * [SpecVocab] sections 2.2.1-2.2.3:

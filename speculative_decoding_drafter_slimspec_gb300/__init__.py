@@ -46,6 +46,8 @@ _SIGS = {
     "slimspec_head_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "slimspec_head_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp,
                                    _vp, _vp, _vp, _vp, _sz, _vp]),
+    "slimspec_head_forward_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp,
+                                           _vp, _vp, _vp, _vp, _vp, _vp]),
     "specvocab_head_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "specvocab_head_forward": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp,
                                     _vp, _vp, _vp, _sz, _vp]),
