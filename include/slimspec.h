@@ -177,7 +177,7 @@ int ss_topk_rows(const float* scores, int M, int V, int k, int32_t* out_idx,
  *  draft_logits  B x gamma x V float32 (may be NULL when T == 0)
  *  draft_tokens  B x gamma int32, each in [0, V) (checked on the device)
  *  uniforms      B x (gamma+1) floats in [0,1) (T > 0), else may be NULL
- *  1 <= gamma <= 32, V >= 1, B >= 0
+ *  1 <= gamma <= 32, 1 <= V <= 524288, B >= 0
  *  out_tokens    B x (gamma+1) int32: the n+1 emitted tokens, then -1
  *  out_num_accepted B int32: n
  * ------------------------------------------------------------------------ */
@@ -197,12 +197,14 @@ int spec_verify(const float* target_logits, const float* draft_logits,
  *   two CUDA events recorded on its stream (host cost: two event records).
  * ss_profile_read: synchronises on the recorded events and writes, for kernel
  *   kind 0 .. n_kinds-1, the number of timed launches and their summed device
- *   time in ms; then forgets the records.  ss_profile_kind_name names a kind.
+ *   time in ms; then forgets the records unless `keep` is non-zero (events
+ *   captured into a CUDA graph are re-recorded by every replay, so a caller
+ *   can read after each replay).  ss_profile_kind_name names a kind.
  * ------------------------------------------------------------------------ */
 long long ss_launch_count(void);
 int ss_profile_start(void);
 int ss_profile_stop(void);
-int ss_profile_read(int* launches, double* total_ms, int n_kinds);
+int ss_profile_read(int* launches, double* total_ms, int n_kinds, int keep);
 const char* ss_profile_kind_name(int kind);
 
 #ifdef __cplusplus

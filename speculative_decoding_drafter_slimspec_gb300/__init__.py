@@ -58,7 +58,7 @@ _SIGS = {
     "ss_launch_count": (ctypes.c_longlong, []),
     "ss_profile_start": (_i, []),
     "ss_profile_stop": (_i, []),
-    "ss_profile_read": (_i, [_vp, _vp, _i]),
+    "ss_profile_read": (_i, [_vp, _vp, _i, _i]),
     "ss_profile_kind_name": (ctypes.c_char_p, [_i]),
 }
 
@@ -277,13 +277,15 @@ def profile_stop():
     _check(lib().ss_profile_stop(), "ss_profile_stop")
 
 
-def profile_read() -> dict:
-    """{kernel name: (timed launches, summed ms)} since the last read."""
+def profile_read(keep: bool = False) -> dict:
+    """{kernel name: (timed launches, summed ms)} of the recorded launches;
+    the records are dropped unless ``keep``."""
     n = N_KERNEL_KINDS
     launches = (ctypes.c_int * n)()
     ms = (ctypes.c_double * n)()
     _check(lib().ss_profile_read(ctypes.cast(launches, ctypes.c_void_p),
-                                 ctypes.cast(ms, ctypes.c_void_p), n), "ss_profile_read")
+                                 ctypes.cast(ms, ctypes.c_void_p), n, 1 if keep else 0),
+           "ss_profile_read")
     return {lib().ss_profile_kind_name(k).decode(): (launches[k], ms[k])
             for k in range(n) if launches[k]}
 

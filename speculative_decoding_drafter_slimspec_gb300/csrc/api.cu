@@ -32,7 +32,20 @@ static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 static bool temp_ok(float t) { return isfinite(t) && t >= 0.f; }
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SS_OK : SS_ERR_CUDA; }
 
+// Blocks of more than 8 bf16 rows of z run the up-projection on the tensor
+// cores; smaller blocks (and fp32) stream it through the CUDA cores.
+static bool use_mma(bool bf16, int M, int r, int V) {
+  return bf16 && M > 8 && mma_plan(r, M, V).ok;
+}
+
 static size_t head_ws_bytes(int M, int r, int V, bool bf16) {
+  if (use_mma(bf16, M, r, V)) {
+    const MmaPlan p = mma_plan(r, M, V);
+    size_t s = align256((size_t)M * r * 2);
+    s += 3 * align256((size_t)M * p.n_sub * sizeof(float));
+    s += 3 * align256((size_t)M * p.grid * sizeof(float));
+    return s;
+  }
   const HeadPlan plan = head_plan(bf16, r, M, V);
   if (!plan.ok) return 0;
   size_t s = 0;
@@ -84,7 +97,7 @@ static int head_check(int M, int d, int r, int V, int dtype) {
   const bool bf16 = dtype == SS_BF16;
   if (d % 8 != 0 || r % (bf16 ? 8 : 4) != 0) return SS_ERR_INVALID_ARG;
   if ((long long)V * r * (bf16 ? 2 : 4) >= (1LL << 40)) return SS_ERR_UNSUPPORTED;
-  if (!head_plan(bf16, r, M, V).ok) return SS_ERR_UNSUPPORTED;
+  if (!use_mma(bf16, M, r, V) && !head_plan(bf16, r, M, V).ok) return SS_ERR_UNSUPPORTED;
   return SS_OK;
 }
 
@@ -113,6 +126,26 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
   const size_t need = head_ws_bytes(M, r, V, bf16);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return SS_ERR_WORKSPACE;
 
+  if (use_mma(bf16, M, r, V)) {
+    const MmaPlan mp = mma_plan(r, M, V);
+    Carver cv(workspace);
+    void* z_ws = cv.take<uint8_t>((size_t)M * r * 2);
+    MmaWork wk;
+    wk.pmax = cv.take<float>((size_t)M * mp.n_sub);
+    wk.psum = cv.take<float>((size_t)M * mp.n_sub);
+    wk.parg = cv.take<int>((size_t)M * mp.n_sub);
+    wk.cmax = cv.take<float>((size_t)M * mp.grid);
+    wk.csum = cv.take<float>((size_t)M * mp.grid);
+    wk.carg = cv.take<int>((size_t)M * mp.grid);
+    const HeadOutputs outs{uniforms, out_tokens, out_logprob, out_row_max, out_row_lse};
+    cudaError_t e = launch_down_proj(bf16, hidden, w_down, M, d, r, true, z_ws, out_z, nullptr, 0,
+                                     stream);
+    if (e == cudaSuccess && out_logits != nullptr)
+      e = launch_head_mma(mp, z_ws, w_up, M, r, V, 0.f, wk, outs, out_logits, stream);
+    if (e == cudaSuccess)
+      e = launch_head_mma(mp, z_ws, w_up, M, r, V, temperature, wk, outs, nullptr, stream);
+    return cuda_status(e);
+  }
   const HeadPlan plan = head_plan(bf16, r, M, V);
   Carver cv(workspace);
   void* z_ws = cv.take<uint8_t>((size_t)M * r * (bf16 ? 2 : 4));
@@ -200,6 +233,7 @@ int spec_verify(const float* target_logits, const float* draft_logits, const int
   if (B < 0 || gamma < 1 || gamma > 32 || V <= 0 || !temp_ok(temperature))
     return SS_ERR_INVALID_ARG;
   if ((long long)B * (gamma + 1) * V >= (1LL << 40)) return SS_ERR_UNSUPPORTED;
+  if (V > 524288) return SS_ERR_UNSUPPORTED;  // the final draw scans at most 256 chunks
   if (B == 0) return SS_OK;
   const bool sample = temperature > 0.f;
   if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SS_ERR_INVALID_ARG;

@@ -72,6 +72,8 @@ struct Gemv {
   static_assert(SPLIT == 1 || SPLIT == 2, "one or two warps per ring");
   static_assert(WARPS <= 32, "at most 1024 threads");
   static_assert(SMEM <= 220 * 1024, "shared memory");
+  static_assert(SMEM >= MTL * 24576, "the finish reuses the rings: 24 KB per finishing warp");
+  static_assert(12288 / MAX_ROW_BYTES >= PASS_ROWS, "a finish chunk holds at least one pass");
 };
 
 // Lane-dependent slot permutation of the select-free reduce-scatter.
@@ -312,62 +314,38 @@ struct HeadPart {
   int* carg;
 };
 
-// First index i in [0, n) (ascending) whose running total of mass(i) passes
-// `target`, with the running total before it; the last index with positive
-// mass if rounding leaves none.  Chunks of 32 with a fixed-order warp scan.
-template <class F>
-__device__ __forceinline__ int ordered_crossing(int n, float target, F mass, float& before,
-                                                int lane) {
-  float run = 0.f, before_last = 0.f;
-  int sel = -1, last = -1;
-  for (int i0 = 0; i0 < n && sel < 0; i0 += 32) {
-    const float mt = (i0 + lane < n) ? mass(i0 + lane) : 0.f;
-    const float cum = __fadd_rn(run, warp_incl_scan(mt, lane));
-    const unsigned pos = __ballot_sync(0xFFFFFFFFu, mt > 0.f);
-    const unsigned hit = __ballot_sync(0xFFFFFFFFu, mt > 0.f && cum > target);
-    if (hit) {
-      const int l = __ffs(hit) - 1;
-      sel = i0 + l;
-      before = __shfl_sync(0xFFFFFFFFu, __fsub_rn(cum, mt), l);
-    } else if (pos) {
-      const int l = 31 - __clz(pos);
-      last = i0 + l;
-      before_last = __shfl_sync(0xFFFFFFFFu, __fsub_rn(cum, mt), l);
-    }
-    run = __shfl_sync(0xFFFFFFFFu, cum, 31);
-  }
-  if (sel < 0) {
-    sel = last < 0 ? 0 : last;
-    before = before_last;
-  }
-  return sel;
-}
+constexpr int kFinChunks = 8;       // per-CTA partials scanned by the finish: up to 256 CTAs
+constexpr int kFinBytes = 24576;    // shared memory per finishing warp for the recompute
 
 // One warp reduces the partials of row m and draws its token: the maximum
 // and W from the per-CTA partials, then (sampling) the CTA and, inside it, the
-// sub-tile where the inverse CDF crosses u * W, whose logits are recomputed.
+// sub-tile where the inverse CDF crosses u * W, whose logits are recomputed
+// from a copy of its rows in shared memory (fsmem, kFinBytes, two halves each
+// tracked by one of the mbarriers fbar[0..1]).
 template <class G, bool kSample>
 __device__ __forceinline__ void finish_row(int m, const uint8_t* __restrict__ w,
                                            const uint8_t* __restrict__ z, int M, int r, int V,
                                            float c, float inv_t, int n_sub, int grid,
                                            const HeadPart& part, const HeadOut& out,
-                                           float* s_logit, int lane) {
+                                           float* s_logit, uint8_t* fsmem, uint64_t* fbar,
+                                           unsigned* err, int lane) {
   const float* cm = part.cmax + (size_t)m * grid;
   const int* ca = part.carg + (size_t)m * grid;
-  // 1. maximum and its lowest index over the CTA partials
-  RowState st = row_state_empty();
-  for (int t0 = 0; t0 < grid; t0 += 128) {
-    float mx[4];
-    int ag[4];
+  const float* cs = part.csum + (size_t)m * grid;
+  // 1. all CTA partials of the row in registers (one round trip)
+  float pmx[kFinChunks], psm[kFinChunks];
+  int pag[kFinChunks];
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int t = t0 + lane + 32 * k;
-      mx[k] = t < grid ? __ldcg(cm + t) : kNegInf;
-      ag[k] = t < grid ? __ldcg(ca + t) : 0x7FFFFFFF;
-    }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) st = row_state_merge<false>(st, RowState{mx[k], 0.f, ag[k]}, c);
+  for (int k = 0; k < kFinChunks; ++k) {
+    const int t = lane + 32 * k;
+    const bool ok = t < grid;
+    pmx[k] = ok ? __ldcg(cm + t) : kNegInf;
+    pag[k] = ok ? __ldcg(ca + t) : 0x7FFFFFFF;
+    psm[k] = (ok && kSample) ? __ldcg(cs + t) : 0.f;
   }
+  RowState st = row_state_empty();
+#pragma unroll
+  for (int k = 0; k < kFinChunks; ++k) st = row_state_merge<false>(st, RowState{pmx[k], 0.f, pag[k]}, c);
 #pragma unroll
   for (int b = 0; b < 5; ++b) st = shfl_merge<false>(st, 1 << b, c);
   const float gmax = st.mx;
@@ -380,24 +358,33 @@ __device__ __forceinline__ void finish_row(int m, const uint8_t* __restrict__ w,
     }
     return;
   }
-  const float* cs = part.csum + (size_t)m * grid;
-  auto cta_mass = [&](int t) -> float { return __ldcg(cs + t) * fast_exp2((__ldcg(cm + t) - gmax) * c); };
-  // 2. total mass W (fixed order)
+  // 2. CTA masses relative to the row maximum and their total W (fixed order)
+  float cmass[kFinChunks];
   float acc = 0.f;
-  for (int t = lane; t < grid; t += 32) acc = __fadd_rn(acc, cta_mass(t));
+#pragma unroll
+  for (int k = 0; k < kFinChunks; ++k) {
+    cmass[k] = psm[k] * fast_exp2((pmx[k] - gmax) * c);
+    acc = __fadd_rn(acc, cmass[k]);
+  }
   const float W = warp_sum_fixed(acc);
   const float target = __ldg(out.uniforms + m) * W;
   // 3. the CTA, then the sub-tile inside it, where the running mass passes u * W
   float before1 = 0.f, before2 = 0.f;
-  const int cta = ordered_crossing(grid, target, cta_mass, before1, lane);
+  const int cta = ordered_crossing_regs<kFinChunks>(grid, target, cmass, before1, lane);
   const int per_cta = n_sub / grid;  // UNITS * spw sub-tiles, contiguous per CTA
   const float* pm = part.pmax + (size_t)m * n_sub + (size_t)cta * per_cta;
   const float* ps = part.psum + (size_t)m * n_sub + (size_t)cta * per_cta;
-  auto sub_mass = [&](int t) -> float { return __ldcg(ps + t) * fast_exp2((__ldcg(pm + t) - gmax) * c); };
+  float smass[kFinChunks];
+#pragma unroll
+  for (int k = 0; k < kFinChunks; ++k) {
+    const int t = lane + 32 * k;
+    smass[k] = t < per_cta ? __ldcg(ps + t) * fast_exp2((__ldcg(pm + t) - gmax) * c) : 0.f;
+  }
   const float resid1 = target - before1;
-  const int tstar = cta * per_cta + ordered_crossing(per_cta, resid1, sub_mass, before2, lane);
+  const int tstar = cta * per_cta + ordered_crossing_regs<kFinChunks>(per_cta, resid1, smass, before2, lane);
   const float resid = resid1 - before2;
-  // 4. recompute the logits of sub-tile tstar with the stream's arithmetic
+  // 4. recompute the logits of sub-tile tstar with the stream's arithmetic,
+  //    its rows copied to shared memory in chunks (two in flight)
   const int m0 = (m / G::MT) * G::MT;   // the warp slice of the stream that held row m
   uint32_t zr[G::MT][G::CPL][4];
   load_z<G>(zr, z, M, m0, r, lane);
@@ -410,16 +397,50 @@ __device__ __forceinline__ void finish_row(int m, const uint8_t* __restrict__ w,
   const int n = max(0, min(G::SUB_ROWS, wstart + wcount - trow0));
   const uint8_t* base = w + (size_t)trow0 * row_bytes;
   const bool dup_leader = (lane & ((1 << G::DUP_BITS) - 1)) == 0;
+  const int crows = ((kFinBytes / 2) / row_bytes) / G::PASS_ROWS * G::PASS_ROWS;  // >= PASS_ROWS
+  if (lane == 0) {
+    mbar_init(&fbar[0], 1);
+    mbar_init(&fbar[1], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const int n_chunks = (n + crows - 1) / crows;
+  auto issue_chunk = [&](int k) {
+    const int r0 = k * crows, nr = min(crows, n - r0);
+    const uint32_t bytes = (uint32_t)(nr * row_bytes);
+    mbar_arrive_expect_tx(&fbar[k & 1], bytes);
+    bulk_g2s(fsmem + (k & 1) * (kFinBytes / 2), base + (size_t)r0 * row_bytes, bytes, &fbar[k & 1]);
+  };
+  if (lane == 0) {
+    if (n_chunks > 0) issue_chunk(0);
+    if (n_chunks > 1) issue_chunk(1);
+  }
+  bool ok = true;
+  for (int k = 0; k < n_chunks; ++k) {
+    ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&fbar[k & 1], (k >> 1) & 1, err));
+    if (!ok) break;
+    const int r0 = k * crows, nr = min(crows, n - r0);
+    const uint32_t sb = smem_u32(fsmem + (k & 1) * (kFinBytes / 2));
 #pragma unroll 1
-  for (int p = 0; p < n; p += G::PASS_ROWS) {
-    float v[G::N];
-    pass_dots<G, false>(base + (size_t)p * row_bytes, 0u, row_bytes, n - p, nch, zr, v, lane);
+    for (int p = 0; p < nr; p += G::PASS_ROWS) {
+      float v[G::N];
+      pass_dots<G, true>(nullptr, sb + p * row_bytes, row_bytes, nr - p, nch, zr, v, lane);
 #pragma unroll
-    for (int j = 0; j < G::NF; ++j) {
-      int rip, mm;
-      slot_of<G>(lane, j, rip, mm);
-      if (dup_leader && m0 + mm == m && p + rip < n) s_logit[p + rip] = v[j];
+      for (int j = 0; j < G::NF; ++j) {
+        int rip, mm;
+        slot_of<G>(lane, j, rip, mm);
+        if (dup_leader && m0 + mm == m && p + rip < nr) s_logit[r0 + p + rip] = v[j];
+      }
     }
+    __syncwarp();
+    if (lane == 0 && k + 2 < n_chunks) {
+      fence_proxy_async_smem();
+      issue_chunk(k + 2);
+    }
+  }
+  if (!ok) {  // a copy did not arrive in time: leave the row's token invalid
+    if (lane == 0) out.tokens[m] = -1;
+    return;
   }
   __syncwarp();
   // 5. walk the sub-tile in row order: lane i holds rows i and i + 32
@@ -465,6 +486,7 @@ __global__ void __launch_bounds__(32 * G::WARPS, 1)
   __shared__ int s_last;
   __shared__ int s_abort[G::UNITS];
   __shared__ RowState s_tot[G::UNITS][G::MTL];
+  __shared__ uint64_t s_fbar[G::MTL][2];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int unit = warp / G::SPLIT;               // ring / row range of this warp
   const int half = warp % G::SPLIT;               // its slice of the launch's rows of z
@@ -633,7 +655,7 @@ __global__ void __launch_bounds__(32 * G::WARPS, 1)
   const int m = m0 + warp;
   if (warp < G::MTL && m < M)
     finish_row<G, kSample>(m, w, z, M, r, V, c, inv_t, n_sub, grid, part, out, s_fin[warp],
-                           lane);
+                           smem + warp * kFinBytes, s_fbar[warp], err, lane);
 }
 
 // ------------------------------------------------------------- host side ----

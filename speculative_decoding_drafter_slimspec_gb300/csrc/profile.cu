@@ -3,7 +3,10 @@
 // When enabled (ss_profile_start), every kernel launch of the library is
 // bracketed by two CUDA events recorded on the launching stream; the
 // benchmark reads per-kernel launch counts and summed durations back with
-// ss_profile_read.  A launch counter runs whether or not timing is enabled.
+// ss_profile_read.  Events recorded while a stream is captured become graph
+// nodes; each replay re-records them, so reading with `keep` after every
+// replay accumulates per-replay kernel times.  A launch counter runs whether
+// or not timing is enabled.
 // Disabled, the cost is one relaxed atomic increment per launch.
 #include <cuda_runtime.h>
 
@@ -44,6 +47,16 @@ cudaEvent_t take_event() {
   cudaEventCreate(&e);
   return e;
 }
+// While `st` is being captured, the record must become an event-record node
+// of the graph (cudaEventRecordExternal) so that each replay re-records it.
+void record(cudaEvent_t e, cudaStream_t st) {
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaStreamIsCapturing(st, &cs);
+  if (cs == cudaStreamCaptureStatusActive)
+    cudaEventRecordWithFlags(e, st, cudaEventRecordExternal);
+  else
+    cudaEventRecord(e, st);
+}
 }  // namespace
 
 cudaError_t set_smem_once(const void* kernel, int bytes) {
@@ -65,7 +78,7 @@ ProfScope::ProfScope(int kind, cudaStream_t st) : slot(-1), stream(st) {
   std::lock_guard<std::mutex> lk(g_mu);
   Rec r{kind, take_event(), take_event()};
   if (!r.a || !r.b) return;
-  cudaEventRecord(r.a, st);
+  record(r.a, st);
   g_recs.push_back(r);
   slot = (int)g_recs.size() - 1;
 }
@@ -73,7 +86,7 @@ ProfScope::ProfScope(int kind, cudaStream_t st) : slot(-1), stream(st) {
 ProfScope::~ProfScope() {
   if (slot < 0) return;
   std::lock_guard<std::mutex> lk(g_mu);
-  if (slot < (int)g_recs.size()) cudaEventRecord(g_recs[slot].b, stream);
+  if (slot < (int)g_recs.size()) record(g_recs[slot].b, stream);
 }
 
 }  // namespace ss
@@ -94,7 +107,7 @@ int ss_profile_stop(void) {
 
 long long ss_launch_count(void) { return g_launches.load(); }
 
-int ss_profile_read(int* launches, double* total_ms, int n_kinds) {
+int ss_profile_read(int* launches, double* total_ms, int n_kinds, int keep) {
   if (!launches || !total_ms || n_kinds < 1) return SS_ERR_INVALID_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   for (int k = 0; k < n_kinds; ++k) { launches[k] = 0; total_ms[k] = 0.0; }
@@ -105,8 +118,10 @@ int ss_profile_read(int* launches, double* total_ms, int n_kinds) {
     if (cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) { status = SS_ERR_CUDA; continue; }
     if (r.kind < n_kinds) { launches[r.kind] += 1; total_ms[r.kind] += ms; }
   }
-  for (const Rec& r : g_recs) { g_pool.push_back(r.a); g_pool.push_back(r.b); }
-  g_recs.clear();
+  if (!keep) {
+    for (const Rec& r : g_recs) { g_pool.push_back(r.a); g_pool.push_back(r.b); }
+    g_recs.clear();
+  }
   return status;
 }
 

@@ -263,6 +263,42 @@ __device__ __forceinline__ float warp_incl_scan(float x, int lane) {
   return x;
 }
 
+// First index in [0, n) (ascending) whose running total passes `target`, with
+// the running total before it; the last index with a positive value if
+// rounding leaves none.  Lane l holds the value of index l + 32 k in mass[k];
+// chunks of 32 are scanned in order with the fixed-order warp scan.
+template <int NC>
+__device__ __forceinline__ int ordered_crossing_regs(int n, float target, const float (&mass)[NC],
+                                                     float& before, int lane) {
+  float run = 0.f, before_last = 0.f;
+  int sel = -1, last = -1;
+#pragma unroll
+  for (int k = 0; k < NC; ++k) {
+    const int i0 = 32 * k;
+    if (i0 < n && sel < 0) {
+      const float mt = mass[k];
+      const float cum = __fadd_rn(run, warp_incl_scan(mt, lane));
+      const unsigned pos = __ballot_sync(0xFFFFFFFFu, mt > 0.f);
+      const unsigned hit = __ballot_sync(0xFFFFFFFFu, mt > 0.f && cum > target);
+      if (hit) {
+        const int l = __ffs(hit) - 1;
+        sel = i0 + l;
+        before = __shfl_sync(0xFFFFFFFFu, __fsub_rn(cum, mt), l);
+      } else if (pos) {
+        const int l = 31 - __clz(pos);
+        last = i0 + l;
+        before_last = __shfl_sync(0xFFFFFFFFu, __fsub_rn(cum, mt), l);
+      }
+      run = __shfl_sync(0xFFFFFFFFu, cum, 31);
+    }
+  }
+  if (sel < 0) {
+    sel = last < 0 ? 0 : last;
+    before = before_last;
+  }
+  return sel;
+}
+
 // Orderable 32-bit key of a float: larger float <=> larger key; -0 == +0.
 __device__ __forceinline__ uint32_t float_key(float f) {
   uint32_t b = __float_as_uint(f);

@@ -93,6 +93,32 @@ cudaError_t launch_head_stream(const HeadPlan& plan, bool bf16, const void* w_up
                                HeadPartials part, float* out_logits, const HeadOutputs& out,
                                cudaStream_t st);
 
+// Tensor-core up-projection (head_mma.cu) for more than 8 rows of z.
+struct MmaPlan {
+  int mt;       // 128-row tiles of z (1 or 2)
+  int kb;       // 64-wide K blocks of r
+  int nst;      // W_up stages in shared memory
+  int smem;     // dynamic shared memory bytes
+  int n_tiles;  // 128-row vocabulary tiles
+  int grid;     // CTAs (one per SM)
+  int n_sub;    // 64-row partials per row of z (2 per tile)
+  bool ok;
+};
+MmaPlan mma_plan(int r, int M, int V);
+struct MmaWork {
+  float* pmax;  // [M][n_sub]
+  float* psum;
+  int* parg;
+  float* cmax;  // [M][grid]
+  float* csum;
+  int* carg;
+};
+// z_ws: M x r bf16.  With `scores` non-null the fp32 products z W_up^T are
+// written there (M x V) instead of being reduced.
+cudaError_t launch_head_mma(const MmaPlan& plan, const void* z_ws, const void* w_up, int M, int r,
+                            int V, float temperature, const MmaWork& work,
+                            const HeadOutputs& out, float* scores, cudaStream_t st);
+
 // ---------------------------------------------------------------- verify --
 size_t verify_ws_bytes(int B, int gamma, int V, bool sample);
 cudaError_t launch_verify(const float* target, const float* draft, const int32_t* tokens, int B,

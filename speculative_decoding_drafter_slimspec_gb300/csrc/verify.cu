@@ -94,16 +94,28 @@ __global__ void __launch_bounds__(512)
   }
 }
 
-// Merged state of one row from its chunk partials (result in every lane).
+// Merged state of one row from its chunk partials (result in every lane);
+// all loads of a lane are issued before the merges.
 template <bool kSample>
 __device__ __forceinline__ RowState warp_row_state(int row, int n_chunks, const float* vmax,
                                                    const float* vsum, const int* varg, float c,
                                                    int lane) {
+  constexpr int NC = 8;
+  float mx[NC], sm[NC];
+  int ag[NC];
   RowState s = row_state_empty();
-  for (int ch = lane; ch < n_chunks; ch += 32) {
-    const size_t o = (size_t)row * n_chunks + ch;
-    RowState t{vmax[o], kSample ? vsum[o] : 0.f, varg[o]};
-    s = row_state_merge<kSample>(s, t, c);
+  for (int c0 = 0; c0 < n_chunks; c0 += 32 * NC) {
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      const int ch = c0 + lane + 32 * k;
+      const size_t o = (size_t)row * n_chunks + ch;
+      const bool ok = ch < n_chunks;
+      mx[k] = ok ? vmax[o] : kNegInf;
+      sm[k] = (ok && kSample) ? vsum[o] : 0.f;
+      ag[k] = ok ? varg[o] : 0x7FFFFFFF;
+    }
+#pragma unroll
+    for (int k = 0; k < NC; ++k) s = row_state_merge<kSample>(s, RowState{mx[k], sm[k], ag[k]}, c);
   }
 #pragma unroll
   for (int b = 0; b < 5; ++b) s = shfl_merge<kSample>(s, 1 << b, c);
@@ -190,6 +202,9 @@ __device__ __forceinline__ float final_weight(const VerifyInfo& in, int mode, fl
 }
 
 // ------------------------------------------------------------------ K10 ----
+// One warp per (sequence, chunk): mass of the final draw's distribution over
+// the chunk.  Residual rows are read with 16 x 16-byte loads of each of the
+// two rows in flight per lane; bonus rows come straight from the partials.
 __global__ void __launch_bounds__(512)
     k_verify_resid(const float* __restrict__ target, const float* __restrict__ draft, int B,
                    int gamma, int V, float c, int n_chunks, const float* __restrict__ vmax,
@@ -199,6 +214,7 @@ __global__ void __launch_bounds__(512)
   const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int nw = gridDim.x * (blockDim.x >> 5);
   const int g1 = gamma + 1;
+  const bool vec = (V & 3) == 0;
   const long long units = (long long)B * n_chunks;
   for (long long u = gw; u < units; u += nw) {
     const int b = (int)(u / n_chunks), ch = (int)(u % n_chunks);
@@ -214,16 +230,39 @@ __global__ void __launch_bounds__(512)
       const float* t = target + (size_t)trow * V;
       const float* q = draft + ((size_t)b * gamma + in.n) * V;
       const int lo = ch * kVChunk, hi = min(V, lo + kVChunk);
-      for (int i = lo + lane; i < hi; i += 32)
-        s = __fadd_rn(s, final_weight(in, 0, __ldg(t + i), __ldg(q + i), c));
+      if (vec) {
+        const float4* t4 = reinterpret_cast<const float4*>(t);
+        const float4* q4 = reinterpret_cast<const float4*>(q);
+        const int q0 = lo >> 2, q1 = hi >> 2;
+        float4 a[16], bq[16];
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) s = __fadd_rn(s, __shfl_xor_sync(0xFFFFFFFFu, s, o));
+        for (int k = 0; k < 16; ++k) {
+          const int i = q0 + lane + 32 * k;
+          if (i < q1) { a[k] = __ldg(t4 + i); bq[k] = __ldg(q4 + i); }
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int i = q0 + lane + 32 * k;
+          if (i < q1) {
+            s = __fadd_rn(s, final_weight(in, 0, a[k].x, bq[k].x, c));
+            s = __fadd_rn(s, final_weight(in, 0, a[k].y, bq[k].y, c));
+            s = __fadd_rn(s, final_weight(in, 0, a[k].z, bq[k].z, c));
+            s = __fadd_rn(s, final_weight(in, 0, a[k].w, bq[k].w, c));
+          }
+        }
+      } else {
+        for (int i = lo + lane; i < hi; i += 32)
+          s = __fadd_rn(s, final_weight(in, 0, __ldg(t + i), __ldg(q + i), c));
+      }
     }
+    s = warp_sum_fixed(s);
     if (lane == 0) rmass[(size_t)b * n_chunks + ch] = s;
   }
 }
 
 // ------------------------------------------------------------------ K11 ----
+constexpr int kMaxChunkRegs = 8;  // up to 256 chunks of 2048 floats: V <= 524288
+
 __global__ void __launch_bounds__(256)
     k_verify_finish(const float* __restrict__ target, const float* __restrict__ draft, int B,
                     int gamma, int V, float c, int n_chunks, const float* __restrict__ vmax,
@@ -237,34 +276,41 @@ __global__ void __launch_bounds__(256)
   const int trow = b * g1 + in.n;
   __shared__ int s_ch, s_mode;
   __shared__ float s_resid;
-  if (tid == 0) {
-    int mode = in.mode;
-    float R = 0.f;
-    for (int ch = 0; ch < n_chunks; ++ch) R = __fadd_rn(R, rmass[(size_t)b * n_chunks + ch]);
-    auto mass = [&](int ch) -> float {
-      if (mode == 0) return rmass[(size_t)b * n_chunks + ch];
+  if (warp == 0) {
+    // chunk masses (up to 32 * kMaxChunkRegs chunks) in registers, one round trip
+    constexpr int NC = kMaxChunkRegs;
+    float rm[NC], pmass[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) {
+      const int ch = lane + 32 * k;
+      const bool ok = ch < n_chunks;
+      rm[k] = ok ? __ldcg(rmass + (size_t)b * n_chunks + ch) : 0.f;
       const size_t o = (size_t)trow * n_chunks + ch;
-      return vsum[o] * fast_exp2((vmax[o] - in.pmx) * c) * in.pinv;
-    };
+      pmass[k] = ok ? __ldcg(vsum + o) * fast_exp2((__ldcg(vmax + o) - in.pmx) * c) * in.pinv : 0.f;
+    }
+    int mode = in.mode;
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < NC; ++k) acc = __fadd_rn(acc, mode == 0 ? rm[k] : pmass[k]);
+    float R = warp_sum_fixed(acc);
     if (!(R > 0.f) && mode == 0) {  // residual vanished: draw from p_n
       mode = 1;
-      R = 0.f;
-      for (int ch = 0; ch < n_chunks; ++ch) R = __fadd_rn(R, mass(ch));
+      acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < NC; ++k) acc = __fadd_rn(acc, pmass[k]);
+      R = warp_sum_fixed(acc);
     }
+    float mass[NC];
+#pragma unroll
+    for (int k = 0; k < NC; ++k) mass[k] = mode == 0 ? rm[k] : pmass[k];
     const float target_mass = uniforms[(size_t)b * g1 + gamma] * R;
-    float cum = 0.f, before = 0.f;
-    int sel = -1, lastp = -1;
-    for (int ch = 0; ch < n_chunks; ++ch) {
-      const float mc = mass(ch);
-      if (mc > 0.f) { lastp = ch; before = cum; }
-      const float nc = __fadd_rn(cum, mc);
-      if (mc > 0.f && nc > target_mass) { sel = ch; before = cum; break; }
-      cum = nc;
+    float before = 0.f;
+    const int sel = ordered_crossing_regs<NC>(n_chunks, target_mass, mass, before, lane);
+    if (lane == 0) {
+      s_ch = sel;
+      s_mode = mode;
+      s_resid = target_mass - before;
     }
-    if (sel < 0) sel = lastp < 0 ? 0 : lastp;
-    s_ch = sel;
-    s_mode = mode;
-    s_resid = target_mass - before;
   }
   __syncthreads();
   const int ch = s_ch, mode = s_mode;
