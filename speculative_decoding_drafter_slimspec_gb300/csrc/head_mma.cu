@@ -18,9 +18,9 @@
 //               CTA) go to workspace (or, in the scores mode, the fp32 values
 //               are written out)
 //
-// k_head_mma_finish then reduces the partials, one warp per row of z:
-// greedy argmax, or the inverse-CDF draw with the one sub-tile it lands in
-// recomputed on CUDA cores.
+// k_head_mma_finish then reduces the partials, one CTA per row of z: greedy
+// argmax, or the inverse-CDF draw with the one sub-tile it lands in recomputed
+// on CUDA cores.
 #include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched at run time
 
 #include <algorithm>
@@ -138,6 +138,58 @@ struct MmaPart {
   float* csum;
   int* carg;
 };
+
+// One chunk of 32 logits of a thread's row pushed into its running state.
+// Out-of-range columns (only in the last vocabulary tile) are masked to -inf.
+// Greedy: a max tree, and the lowest index of the maximum is looked up only
+// when it beats the running maximum.  Sampling: the maximum (no index: the
+// draw does not need it), then sum of 2^(x*c - max*c) in four fixed-order
+// partial sums.
+template <bool kSample>
+__device__ __forceinline__ void epi_chunk(const uint32_t (&v)[32], int vid0, int V, RowState& st,
+                                          float c) {
+  float x[32];
+  const bool full = vid0 + 32 <= V;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    x[j] = __uint_as_float(v[j]);
+    if (!full && vid0 + j >= V) x[j] = kNegInf;
+  }
+  float t16[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) t16[j] = fmaxf(x[j], x[j + 16]);
+#pragma unroll
+  for (int w = 8; w > 0; w >>= 1)
+#pragma unroll
+    for (int j = 0; j < w; ++j) t16[j] = fmaxf(t16[j], t16[j + w]);
+  const float cm = t16[0];
+  if (!kSample) {
+    if (cm > st.mx) {
+      int idx = 31;
+#pragma unroll
+      for (int j = 31; j >= 0; --j)
+        if (x[j] == cm) idx = j;
+      st.mx = cm;
+      st.arg = vid0 + idx;
+    }
+    return;
+  }
+  if (cm > st.mx) {
+    st.sum = st.mx == kNegInf ? 0.f : st.sum * fast_exp2((st.mx - cm) * c);
+    st.mx = cm;
+  }
+  if (st.mx == kNegInf) return;  // nothing in range yet: -max*c would be +inf
+  const float off = -st.mx * c;
+  float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; j += 4) {
+    a0 = __fadd_rn(a0, fast_exp2(__fmaf_rn(x[j], c, off)));
+    a1 = __fadd_rn(a1, fast_exp2(__fmaf_rn(x[j + 1], c, off)));
+    a2 = __fadd_rn(a2, fast_exp2(__fmaf_rn(x[j + 2], c, off)));
+    a3 = __fadd_rn(a3, fast_exp2(__fmaf_rn(x[j + 3], c, off)));
+  }
+  st.sum = __fadd_rn(st.sum, __fadd_rn(__fadd_rn(a0, a1), __fadd_rn(a2, a3)));
+}
 
 // ------------------------------------------------------------------ kernel --
 // MT: M tiles of 128 rows of z (1 or 2).  kMode 0: softmax partials; kMode 1:
@@ -259,6 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = MT == 2 ? 0 : ew / 4;
     const int row = mt * kTileM + quad * 32 + lane;  // row of z owned by this thread
     const bool live = row < M;
+    const bool warp_live = mt * kTileM + quad * 32 < M;  // any live row in this warp
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     RowState tot = row_state_empty();
     for (int i = 0; i < nt; ++i) {
@@ -271,52 +324,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int hh = 0; hh < (MT == 2 ? 2 : 1); ++hh) {
         const int h = MT == 2 ? hh : half;
         RowState st = row_state_empty();
+        if (warp_live) {
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int col = h * kSubW + cc * 32;
-          uint32_t v[32];
-          tmem_ld32(tmem + lane_addr + (uint32_t)((buf * MT + mt) * kTileN + col), v);
-          const int vid0 = t * kTileN + col;
-          if (kMode == 1) {
-            if (live) {
-              float* dst = out_scores + (size_t)row * V + vid0;
-              if (vid0 + 32 <= V && (V & 3) == 0) {
+          for (int cc = 0; cc < 2; ++cc) {
+            const int col = h * kSubW + cc * 32;
+            uint32_t v[32];
+            tmem_ld32(tmem + lane_addr + (uint32_t)((buf * MT + mt) * kTileN + col), v);
+            const int vid0 = t * kTileN + col;
+            if (kMode == 1) {
+              if (live) {
+                float* dst = out_scores + (size_t)row * V + vid0;
+                if (vid0 + 32 <= V && (V & 3) == 0) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                  *reinterpret_cast<float4*>(dst + j) =
-                      make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
-                                  __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
-              } else {
-                for (int j = 0; j < 32; ++j)
-                  if (vid0 + j < V) dst[j] = __uint_as_float(v[j]);
+                  for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4*>(dst + j) =
+                        make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]),
+                                    __uint_as_float(v[j + 2]), __uint_as_float(v[j + 3]));
+                } else {
+                  for (int j = 0; j < 32; ++j)
+                    if (vid0 + j < V) dst[j] = __uint_as_float(v[j]);
+                }
               }
+            } else {
+              epi_chunk<kSample>(v, vid0, V, st, c);
             }
-          } else if (!kSample) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float x = __uint_as_float(v[j]);
-              if (vid0 + j < V && x > st.mx) { st.mx = x; st.arg = vid0 + j; }
-            }
-          } else {
-            float cm = kNegInf;
-            int ca = 0x7FFFFFFF;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float x = __uint_as_float(v[j]);
-              if (vid0 + j < V && x > cm) { cm = x; ca = vid0 + j; }
-            }
-            if (cm > st.mx) {
-              st.sum = st.sum * fast_exp2((st.mx - cm) * c);
-              st.mx = cm;
-              st.arg = ca;
-            }
-            float add = 0.f;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float x = __uint_as_float(v[j]);
-              add = __fadd_rn(add, vid0 + j < V ? fast_exp2((x - st.mx) * c) : 0.f);
-            }
-            st.sum = __fadd_rn(st.sum, add);
           }
         }
         if (kMode == 0) {
@@ -356,124 +387,138 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ------------------------------------------------------------------ finish --
-// One warp per row of z: the maximum, W and (sampling) the CTA and the 64-row
-// sub-tile where the inverse CDF crosses u * W, whose logits are recomputed
-// here with CUDA cores (fp32 accumulation of the same bf16 products).
+// One CTA of 8 warps per row of z.  Warp 0 merges the partials: the maximum,
+// W and (sampling) the CTA and the 64-row sub-tile where the inverse CDF
+// crosses u * W.  The 8 warps then recompute that sub-tile's logits (8 rows
+// each, every load issued up front; CUDA-core fp32 accumulation of the same
+// bf16 products) and warp 0 walks them in row order.
 template <bool kSample>
 __global__ void __launch_bounds__(256)
     k_head_mma_finish(const uint8_t* __restrict__ w_up, const uint8_t* __restrict__ z, int M,
                       int r, int V, float c, float inv_t, int n_tiles, int grid, MmaPart part,
                       HeadOutputs out) {
-  __shared__ float s_logit[8][kSubW];
+  __shared__ float s_logit[kSubW];
+  __shared__ float s_f[4];  // gmax, W, resid
+  __shared__ int s_i[2];    // sub-tile, token (greedy)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m = blockIdx.x * 8 + warp;
+  const int m = blockIdx.x;
   pdl_wait_producer();
   if (m >= M) return;
   const int n_sub = 2 * n_tiles;
-  const float* cm = part.cmax + (size_t)m * grid;
-  const int* ca = part.carg + (size_t)m * grid;
-  const float* cs = part.csum + (size_t)m * grid;
-  constexpr int NC = 8;  // up to 256 CTAs
-  float pmx[NC], psm[NC];
-  int pag[NC];
+  if (warp == 0) {
+    const float* cm = part.cmax + (size_t)m * grid;
+    const int* ca = part.carg + (size_t)m * grid;
+    const float* cs = part.csum + (size_t)m * grid;
+    constexpr int NC = 8;  // up to 256 CTAs
+    float pmx[NC], psm[NC];
+    int pag[NC];
 #pragma unroll
-  for (int k = 0; k < NC; ++k) {
-    const int t = lane + 32 * k;
-    const bool ok = t < grid;
-    pmx[k] = ok ? __ldcg(cm + t) : kNegInf;
-    pag[k] = ok ? __ldcg(ca + t) : 0x7FFFFFFF;
-    psm[k] = (ok && kSample) ? __ldcg(cs + t) : 0.f;
-  }
-  RowState st = row_state_empty();
-#pragma unroll
-  for (int k = 0; k < NC; ++k) st = row_state_merge<false>(st, RowState{pmx[k], 0.f, pag[k]}, c);
-#pragma unroll
-  for (int b = 0; b < 5; ++b) st = shfl_merge<false>(st, 1 << b, c);
-  const float gmax = st.mx;
-  if (!kSample) {
-    if (lane == 0) {
-      out.tokens[m] = st.arg;
-      if (out.logprob) out.logprob[m] = 0.f;
-      if (out.row_max) out.row_max[m] = gmax;
-      if (out.row_lse) out.row_lse[m] = gmax;
+    for (int k = 0; k < NC; ++k) {
+      const int t = lane + 32 * k;
+      const bool ok = t < grid;
+      pmx[k] = ok ? __ldcg(cm + t) : kNegInf;
+      pag[k] = ok ? __ldcg(ca + t) : 0x7FFFFFFF;
+      psm[k] = (ok && kSample) ? __ldcg(cs + t) : 0.f;
     }
-    return;
-  }
-  float cmass[NC];
-  float acc = 0.f;
+    RowState st = row_state_empty();
 #pragma unroll
-  for (int k = 0; k < NC; ++k) {
-    cmass[k] = psm[k] * fast_exp2((pmx[k] - gmax) * c);
-    acc = __fadd_rn(acc, cmass[k]);
-  }
-  const float W = warp_sum_fixed(acc);
-  const float target = __ldg(out.uniforms + m) * W;
-  float before1 = 0.f, before2 = 0.f;
-  const int cta = ordered_crossing_regs<NC>(grid, target, cmass, before1, lane);
-  int ct0, cnt;
-  cta_tiles(n_tiles, grid, cta, ct0, cnt);
-  const int s0 = 2 * ct0, ns = 2 * cnt;  // this CTA's sub-tiles, contiguous
-  const float* pm = part.pmax + (size_t)m * n_sub + s0;
-  const float* ps = part.psum + (size_t)m * n_sub + s0;
-  float smass[NC];
+    for (int k = 0; k < NC; ++k)
+      st = row_state_merge<false>(st, RowState{pmx[k], 0.f, pag[k]}, c);
 #pragma unroll
-  for (int k = 0; k < NC; ++k) {
-    const int t = lane + 32 * k;
-    smass[k] = t < ns ? __ldcg(ps + t) * fast_exp2((__ldcg(pm + t) - gmax) * c) : 0.f;
+    for (int b = 0; b < 5; ++b) st = shfl_merge<false>(st, 1 << b, c);
+    const float gmax = st.mx;
+    if (!kSample) {
+      if (lane == 0) {
+        out.tokens[m] = st.arg;
+        if (out.logprob) out.logprob[m] = 0.f;
+        if (out.row_max) out.row_max[m] = gmax;
+        if (out.row_lse) out.row_lse[m] = gmax;
+      }
+    } else {
+      float cmass[NC];
+      float acc = 0.f;
+#pragma unroll
+      for (int k = 0; k < NC; ++k) {
+        cmass[k] = psm[k] * fast_exp2((pmx[k] - gmax) * c);
+        acc = __fadd_rn(acc, cmass[k]);
+      }
+      const float W = warp_sum_fixed(acc);
+      const float target = __ldg(out.uniforms + m) * W;
+      float before1 = 0.f, before2 = 0.f;
+      const int cta = ordered_crossing_regs<NC>(grid, target, cmass, before1, lane);
+      int ct0, cnt;
+      cta_tiles(n_tiles, grid, cta, ct0, cnt);
+      const int s0 = 2 * ct0, ns = 2 * cnt;  // this CTA's sub-tiles, contiguous
+      const float* pm = part.pmax + (size_t)m * n_sub + s0;
+      const float* ps = part.psum + (size_t)m * n_sub + s0;
+      float smass[NC];
+#pragma unroll
+      for (int k = 0; k < NC; ++k) {
+        const int t = lane + 32 * k;
+        smass[k] = t < ns ? __ldcg(ps + t) * fast_exp2((__ldcg(pm + t) - gmax) * c) : 0.f;
+      }
+      const float resid1 = target - before1;
+      const int sid = s0 + ordered_crossing_regs<NC>(ns, resid1, smass, before2, lane);
+      if (lane == 0) {
+        s_f[0] = gmax;
+        s_f[1] = W;
+        s_f[2] = resid1 - before2;
+        s_i[0] = sid;
+      }
+    }
   }
-  const float resid1 = target - before1;
-  const int sid = s0 + ordered_crossing_regs<NC>(ns, resid1, smass, before2, lane);
-  const float resid = resid1 - before2;
-  // recompute the sub-tile's logits: lanes over the K chunks of a row
-  const int v0 = sid * kSubW;
+  if (!kSample) return;
+  __syncthreads();
+  const float gmax = s_f[0], W = s_f[1], resid = s_f[2];
+  const int v0 = s_i[0] * kSubW;
   const int n = max(0, min(kSubW, V - v0));
+  // recompute: warp w takes rows 8w .. 8w+7 of the sub-tile, lanes over K
   const int nch = r / 8;
-  uint4 zc[2];
+  uint4 zc[2], wv[8][2];
 #pragma unroll
   for (int q = 0; q < 2; ++q) {
     const int ch = lane + 32 * q;
     zc[q] = ch < nch ? __ldg(reinterpret_cast<const uint4*>(z + ((size_t)m * r + ch * 8) * 2))
                      : make_uint4(0u, 0u, 0u, 0u);
   }
-  for (int i0 = 0; i0 < n; i0 += 4) {
-    uint4 wv[4][2];
 #pragma unroll
-    for (int ii = 0; ii < 4; ++ii)
+  for (int ii = 0; ii < 8; ++ii) {
+    const int i = warp * 8 + ii;
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int ch = lane + 32 * q;
-        wv[ii][q] = (i0 + ii < n && ch < nch)
-                        ? __ldg(reinterpret_cast<const uint4*>(
-                              w_up + ((size_t)(v0 + i0 + ii) * r + ch * 8) * 2))
-                        : make_uint4(0u, 0u, 0u, 0u);
-      }
-#pragma unroll
-    for (int ii = 0; ii < 4; ++ii) {
-      float a = 0.f;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint32_t ww[4] = {wv[ii][q].x, wv[ii][q].y, wv[ii][q].z, wv[ii][q].w};
-        const uint32_t zz[4] = {zc[q].x, zc[q].y, zc[q].z, zc[q].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          a = fma_bf16_lo(ww[e], zz[e], a);
-          a = fma_bf16_hi(ww[e], zz[e], a);
-        }
-      }
-      a = warp_sum_fixed(a);
-      if (lane == 0 && i0 + ii < n) s_logit[warp][i0 + ii] = a;
+    for (int q = 0; q < 2; ++q) {
+      const int ch = lane + 32 * q;
+      wv[ii][q] = (i < n && ch < nch) ? __ldg(reinterpret_cast<const uint4*>(
+                                            w_up + ((size_t)(v0 + i) * r + ch * 8) * 2))
+                                      : make_uint4(0u, 0u, 0u, 0u);
     }
   }
-  __syncwarp();
+#pragma unroll
+  for (int ii = 0; ii < 8; ++ii) {
+    float a = 0.f;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t ww[4] = {wv[ii][q].x, wv[ii][q].y, wv[ii][q].z, wv[ii][q].w};
+      const uint32_t zz[4] = {zc[q].x, zc[q].y, zc[q].z, zc[q].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        a = fma_bf16_lo(ww[e], zz[e], a);
+        a = fma_bf16_hi(ww[e], zz[e], a);
+      }
+    }
+    a = warp_sum_fixed(a);
+    if (lane == 0) s_logit[warp * 8 + ii] = a;
+  }
+  __syncthreads();
+  if (warp != 0) return;
   float cum = 0.f;
   int tok = -1, lastp = -1;
 #pragma unroll
   for (int h = 0; h < kSubW; h += 32) {
     const int i = h + lane;
-    const float wv = i < n ? fast_exp2((s_logit[warp][i] - gmax) * c) : 0.f;
-    const float csum = __fadd_rn(cum, warp_incl_scan(wv, lane));
-    const unsigned pos = __ballot_sync(0xFFFFFFFFu, wv > 0.f);
-    const unsigned hit = __ballot_sync(0xFFFFFFFFu, wv > 0.f && csum > resid);
+    const float wv1 = i < n ? fast_exp2((s_logit[i] - gmax) * c) : 0.f;
+    const float csum = __fadd_rn(cum, warp_incl_scan(wv1, lane));
+    const unsigned pos = __ballot_sync(0xFFFFFFFFu, wv1 > 0.f);
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, wv1 > 0.f && csum > resid);
     if (tok < 0 && hit) tok = h + __ffs(hit) - 1;
     if (pos) lastp = h + 31 - __clz(pos);
     cum = __shfl_sync(0xFFFFFFFFu, csum, 31);
@@ -482,7 +527,7 @@ __global__ void __launch_bounds__(256)
   if (lane == 0) {
     const float lW = logf(W);
     out.tokens[m] = v0 + tok;
-    if (out.logprob) out.logprob[m] = (s_logit[warp][tok] - gmax) * inv_t - lW;
+    if (out.logprob) out.logprob[m] = (s_logit[tok] - gmax) * inv_t - lW;
     if (out.row_max) out.row_max[m] = gmax;
     if (out.row_lse) out.row_lse[m] = gmax * inv_t + lW;
   }
@@ -590,7 +635,7 @@ cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up
   if (e != cudaSuccess) return e;
   // the per-row finish, launched to overlap the tail of the MMA grid
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((M + 7) / 8);
+  cfg.gridDim = dim3(M);
   cfg.blockDim = dim3(256);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];

@@ -72,6 +72,22 @@ cudaError_t set_smem_once(const void* kernel, int bytes) {
   return e;
 }
 
+int resident_blocks(const void* kernel, int threads, size_t smem) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> seen;
+  static std::vector<std::pair<std::pair<const void*, int>, int>> values;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lk(mu);
+  for (const auto& kv : values)
+    if (kv.first.first == kernel && kv.first.second == dev) return kv.second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess || n < 1)
+    n = 1;
+  values.push_back({{kernel, dev}, n});
+  return n;
+}
+
 ProfScope::ProfScope(int kind, cudaStream_t st) : slot(-1), stream(st) {
   g_launches.fetch_add(1, std::memory_order_relaxed);
   if (!g_on.load(std::memory_order_relaxed)) return;

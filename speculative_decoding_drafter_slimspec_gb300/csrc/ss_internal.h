@@ -29,6 +29,10 @@ struct ProfScope {
   ~ProfScope();
 };
 
+// CTAs of `kernel` (threads per CTA, dynamic shared memory) resident per SM,
+// from the occupancy calculator, cached per (kernel, device).
+int resident_blocks(const void* kernel, int threads, size_t smem);
+
 // Sets a kernel's dynamic shared memory limit once per (kernel, device), so
 // that no attribute call happens while a stream is being captured later.
 cudaError_t set_smem_once(const void* kernel, int bytes);

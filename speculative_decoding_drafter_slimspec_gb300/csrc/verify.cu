@@ -51,7 +51,7 @@ __device__ __forceinline__ void push4(RowState& s, const float4 a, int v0, float
 
 // ------------------------------------------------------------------- K8 ----
 template <bool kSample>
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(256)
     k_verify_rows(const float* __restrict__ target, const float* __restrict__ draft,
                   int n_target_rows, int n_rows, int V, float c, int n_chunks,
                   float* __restrict__ vmax, float* __restrict__ vsum, int* __restrict__ varg) {
@@ -205,7 +205,7 @@ __device__ __forceinline__ float final_weight(const VerifyInfo& in, int mode, fl
 // One warp per (sequence, chunk): mass of the final draw's distribution over
 // the chunk.  Residual rows are read with 16 x 16-byte loads of each of the
 // two rows in flight per lane; bonus rows come straight from the partials.
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(256)
     k_verify_resid(const float* __restrict__ target, const float* __restrict__ draft, int B,
                    int gamma, int V, float c, int n_chunks, const float* __restrict__ vmax,
                    const float* __restrict__ vsum, const VerifyInfo* __restrict__ info,
@@ -401,16 +401,21 @@ cudaError_t launch_verify(const float* target, const float* draft, const int32_t
   VerifyInfo* info = cv.take<VerifyInfo>(B);
   float* rmass = cv.take<float>((size_t)B * n_chunks);
 
+  // one warp per unit; the grid is what fits on the GPU at once (one wave)
   const long long units = (long long)n_rows * n_chunks;
-  const int grid = (int)std::max<long long>(1, std::min<long long>((units + 15) / 16, 4LL * sm_count()));
   {
+  constexpr int kThr = 256;
+  const void* kern = sample ? reinterpret_cast<const void*>(k_verify_rows<true>)
+                            : reinterpret_cast<const void*>(k_verify_rows<false>);
+  const long long cap = (long long)resident_blocks(kern, kThr, 0) * sm_count();
+  const int grid = (int)std::max<long long>(1, std::min<long long>((units + 7) / 8, cap));
   ProfScope ps(kKVerifyRows, st);
   if (sample)
-    k_verify_rows<true><<<grid, 512, 0, st>>>(target, draft, n_target_rows, n_rows, V, c,
-                                              n_chunks, vmax, vsum, varg);
-  else
-    k_verify_rows<false><<<grid, 512, 0, st>>>(target, draft, n_target_rows, n_rows, V, c,
+    k_verify_rows<true><<<grid, kThr, 0, st>>>(target, draft, n_target_rows, n_rows, V, c,
                                                n_chunks, vmax, vsum, varg);
+  else
+    k_verify_rows<false><<<grid, kThr, 0, st>>>(target, draft, n_target_rows, n_rows, V, c,
+                                                n_chunks, vmax, vsum, varg);
   }
   {
   const int rows = sample ? 2 * gamma + 1 : gamma + 1;
@@ -427,10 +432,12 @@ cudaError_t launch_verify(const float* target, const float* draft, const int32_t
   }
   if (sample) {
     const long long ru = (long long)B * n_chunks;
-    const int rgrid = (int)std::max<long long>(1, std::min<long long>((ru + 15) / 16, 4LL * sm_count()));
+    const long long rcap = (long long)resident_blocks(reinterpret_cast<const void*>(k_verify_resid),
+                                                      256, 0) * sm_count();
+    const int rgrid = (int)std::max<long long>(1, std::min<long long>((ru + 7) / 8, rcap));
     {
       ProfScope ps(kKVerifyResid, st);
-      k_verify_resid<<<rgrid, 512, 0, st>>>(target, draft, B, gamma, V, c, n_chunks, vmax, vsum,
+      k_verify_resid<<<rgrid, 256, 0, st>>>(target, draft, B, gamma, V, c, n_chunks, vmax, vsum,
                                           info, rmass);
     }
     ProfScope ps(kKVerifyFinish, st);
