@@ -32,10 +32,13 @@ static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 static bool temp_ok(float t) { return isfinite(t) && t >= 0.f; }
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SS_OK : SS_ERR_CUDA; }
 
-// Blocks of more than 8 bf16 rows of z run the up-projection on the tensor
-// cores; smaller blocks (and fp32) stream it through the CUDA cores.
+// bf16 heads run the up-projection on the tensor cores whenever the shape
+// fits the tcgen05 kernel (r a multiple of 8 up to 512, M up to 256), even for
+// a single row of z: the MMA takes the multiply-adds off the issue slots, so
+// the kernel only moves W_up.  fp32 heads, and bf16 shapes outside that range,
+// stream W_up through the CUDA cores.
 static bool use_mma(bool bf16, int M, int r, int V) {
-  return bf16 && M > 8 && mma_plan(r, M, V).ok;
+  return bf16 && M >= 1 && mma_plan(r, M, V).ok;
 }
 
 static size_t head_ws_bytes(int M, int r, int V, bool bf16) {
@@ -43,7 +46,7 @@ static size_t head_ws_bytes(int M, int r, int V, bool bf16) {
     const MmaPlan p = mma_plan(r, M, V);
     size_t s = align256((size_t)M * r * 2);
     s += 3 * align256((size_t)M * p.n_sub * sizeof(float));
-    s += 3 * align256((size_t)M * p.grid * sizeof(float));
+    s += align256(2 * sizeof(unsigned));  // tile counters of the two launches
     return s;
   }
   const HeadPlan plan = head_plan(bf16, r, M, V);
@@ -134,16 +137,15 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
     wk.pmax = cv.take<float>((size_t)M * mp.n_sub);
     wk.psum = cv.take<float>((size_t)M * mp.n_sub);
     wk.parg = cv.take<int>((size_t)M * mp.n_sub);
-    wk.cmax = cv.take<float>((size_t)M * mp.grid);
-    wk.csum = cv.take<float>((size_t)M * mp.grid);
-    wk.carg = cv.take<int>((size_t)M * mp.grid);
+    unsigned* ctr = cv.take<unsigned>(2);
     const HeadOutputs outs{uniforms, out_tokens, out_logprob, out_row_max, out_row_lse};
-    cudaError_t e = launch_down_proj(bf16, hidden, w_down, M, d, r, true, z_ws, out_z, nullptr, 0,
+    cudaError_t e = launch_down_proj(bf16, hidden, w_down, M, d, r, true, z_ws, out_z, ctr, 2,
                                      stream);
     if (e == cudaSuccess && out_logits != nullptr)
-      e = launch_head_mma(mp, z_ws, w_up, M, r, V, 0.f, wk, outs, out_logits, stream);
+      e = launch_head_mma(mp, z_ws, w_up, M, r, V, 0.f, wk, outs, out_logits, ctr, stream);
     if (e == cudaSuccess)
-      e = launch_head_mma(mp, z_ws, w_up, M, r, V, temperature, wk, outs, nullptr, stream);
+      e = launch_head_mma(mp, z_ws, w_up, M, r, V, temperature, wk, outs, nullptr, ctr + 1,
+                          stream);
     return cuda_status(e);
   }
   const HeadPlan plan = head_plan(bf16, r, M, V);

@@ -684,8 +684,13 @@ cudaError_t launch_down_proj(bool bf16, const void* h, const void* w, int M, int
   uint8_t* oz = (uint8_t*)out_z;
   const int rnd = round_bf16_z ? 1 : 0;
   ProfScope ps(kKDownProj, st);
-#define SS_DOWN(B, Q) \
-  k_down_proj<B, Q><<<grid, 256, 0, st>>>(hp, wp, M, d, r, rnd, (uint8_t*)z_ws, oz, ctr, n_ctr)
+#define SS_DOWN(B, Q)                                                                     \
+  do {                                                                                      \
+    cudaError_t e0 = set_smem_once(reinterpret_cast<const void*>(k_down_proj<B, Q>), 0);    \
+    if (e0 != cudaSuccess) return e0;                                                       \
+    k_down_proj<B, Q><<<grid, 256, 0, st>>>(hp, wp, M, d, r, rnd, (uint8_t*)z_ws, oz, ctr,  \
+                                            n_ctr);                                         \
+  } while (0)
   if (bf16) {
     if (q <= 1) SS_DOWN(true, 1);
     else if (q <= 2) SS_DOWN(true, 2);

@@ -1,26 +1,45 @@
 // head_mma.cu -- the low-rank head's up-projection on the 5th-generation tensor
-// cores (tcgen05), for blocks of more than 8 rows of z.
+// cores (tcgen05), for bf16 heads with up to 256 rows of z.
 //
 // SlimSpec article (荷兰Nebius团队：给AI“起草员“瘦身…), section 三: logits = z W_up^T
-// over the full vocabulary.  With tens to hundreds of rows of z this is a real
-// dense contraction (M x r times r x V), so it runs as a warp-specialised,
-// persistent tcgen05 GEMM whose epilogue is the per-row softmax reduction:
+// over the full vocabulary.  The product is a skinny dense contraction
+// (M x r times r x V).  Even for a single row of z it runs on the tensor
+// cores: they take the multiply-adds off the issue slots, and the kernel is
+// left to move W_up at the speed of HBM.  One persistent CTA per SM,
+// warp-specialised, with the per-row softmax reduction as the GEMM epilogue:
 //
-//   warp 0      TMA producer: z (A, 128-row tiles, once) and W_up (B, 128-row
-//               vocabulary tiles, one 64-wide K block per stage) into
-//               128B-swizzled shared memory
+//   warp 0      producer.  It takes 128-row vocabulary tiles (two fixed ones,
+//               then the next free tile from a global counter, so that SMs
+//               that stream faster take more tiles; under a full HBM queue an
+//               atomic takes microseconds, so two claims stay in flight),
+//               hands their ids to the other warps through a small ring in
+//               shared memory,
+//               and loads W_up (B, one 64-wide K block of a tile per 16 KB
+//               stage, 128B-swizzled) with TMA.  One issuing thread keeps only
+//               about one box per 800 cycles under way, short of this SM's
+//               share of HBM bandwidth, so lane 0 waits for a group of up to
+//               four free stages and that many lanes issue together.
 //   warp 1      TMEM owner and MMA issuer: tcgen05.mma kind::f16 (bf16 x bf16
 //               -> fp32) into a double-buffered TMEM accumulator
 //               D[m, v] (lanes = rows of z, columns = vocabulary rows)
-//   warps 2-9   epilogue: tcgen05.ld of 32 columns at a time; every thread owns
-//               one row of z and keeps its online (max, sum of exp, argmax)
-//               state; one partial per (row, 64-row sub-tile) and per (row,
-//               CTA) go to workspace (or, in the scores mode, the fp32 values
-//               are written out)
+//   warps 2-9   epilogue.  First, once the down-projection is complete, they
+//               copy z (A, 128-row tiles) into shared memory with ordinary
+//               loads, in the 128B-swizzled layout, so that it does not queue
+//               behind the W_up boxes already in flight.  Then, per tile,
+//               tcgen05.ld of 32 columns at a time; every thread owns one row
+//               of z and reduces each 64-row sub-tile to one partial
+//               (max, sum of exp, argmax), written to workspace (or, in the
+//               scores mode, writes the fp32 values out)
 //
-// k_head_mma_finish then reduces the partials, one CTA per row of z: greedy
-// argmax, or the inverse-CDF draw with the one sub-tile it lands in recomputed
-// on CUDA cores.
+// z is stored compactly: a 128-row tile of z with only M' live rows keeps
+// ceil(M'/8) swizzle atoms (8 rows x 128 bytes) per K block.  The MMA still
+// reads 128 rows; rows past the live ones come from whatever follows in shared
+// memory and only reach rows of D that nothing reads.  For a few rows of z
+// this frees almost all of shared memory for W_up stages.
+//
+// k_head_mma_finish then reduces the partials, one CTA per row of z, in
+// vocabulary order: greedy argmax, or the inverse-CDF draw with the one
+// sub-tile it lands in recomputed on CUDA cores.
 #include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched at run time
 
 #include <algorithm>
@@ -36,9 +55,16 @@ constexpr int kTileM = 128;               // rows of z per M tile (MMA M)
 constexpr int kBlockBytes = 128 * 128;    // one [128 rows x 64 K] bf16 block
 constexpr int kSubW = 64;                 // vocabulary rows per partial
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);
-constexpr int kMaxStages = 8;
-constexpr int kSmemCap = 223 * 1024;   // dynamic; static barriers and merge buffers use the rest
+constexpr int kProdGroup = 4;             // stages the producer issues together
+constexpr int kMmaWarp = 1;               // TMEM owner and MMA issuer
+constexpr int kEpiWarp0 = 2;              // first epilogue warp
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kMaxStages = 16;
+constexpr int kTileRing = 8;              // tile ids in flight between the warps
+constexpr int kStaticTiles = 2;           // tiles b, b + grid of CTA b; the rest are claimed
+constexpr int kSmemCap = 223 * 1024;      // dynamic; static barriers use the rest
+constexpr int kFinThreads = 256;
+constexpr int kFinPer = 24;               // partials per finish thread: n_sub <= 6144
 
 // ------------------------------------------------------------- PTX wrappers --
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
@@ -85,11 +111,21 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
           smem_u32(bar))
       : "memory");
 }
+// 16-byte asynchronous global -> shared copy; src_bytes < 16 zero-fills the rest.
+__device__ __forceinline__ void cp_async16_zfill(void* dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+// 32 consecutive fp32 columns of this thread's TMEM lane; the registers are
+// valid after tmem_ld_wait().
+__device__ __forceinline__ void tmem_ld32_issue(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
       "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
@@ -100,6 +136,8 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
         "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
         "=r"(v[31])
       : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
@@ -122,10 +160,17 @@ constexpr uint32_t idesc_bf16(int m, int n) {
          | ((uint32_t)(m >> 4) << 24); // M / 16
 }
 
-__device__ __forceinline__ void cta_tiles(int n_tiles, int grid, int cta, int& t0, int& nt) {
-  const int base = n_tiles / grid, extra = n_tiles % grid;
-  t0 = cta * base + min(cta, extra);
-  nt = base + (cta < extra ? 1 : 0);
+// Swizzle atoms (8 rows of z) kept per K block of M tile mt, and the byte
+// offset of block (mt, kb) of z in shared memory.
+__host__ __device__ __forceinline__ int z_atoms(int M, int mt) {
+  const int rows = M - mt * kTileM;
+  return rows >= kTileM ? kTileM / 8 : (rows + 7) / 8;
+}
+__host__ __device__ __forceinline__ int z_block_off(int M, int KB, int mt, int kb) {
+  return (mt * KB * (kTileM / 8) + kb * z_atoms(M, mt)) * 1024;
+}
+__host__ __device__ __forceinline__ int z_bytes(int M, int KB, int MT) {
+  return MT == 1 ? KB * z_atoms(M, 0) * 1024 : KB * (kTileM / 8 + z_atoms(M, 1)) * 1024;
 }
 
 }  // namespace
@@ -134,9 +179,6 @@ struct MmaPart {
   float* pmax;  // [M][n_sub]  per 64-row vocabulary sub-tile
   float* psum;
   int* parg;
-  float* cmax;  // [M][grid]   per CTA
-  float* csum;
-  int* carg;
 };
 
 // One chunk of 32 logits of a thread's row pushed into its running state.
@@ -193,41 +235,48 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&v)[32], int vid0, int
 
 // ------------------------------------------------------------------ kernel --
 // MT: M tiles of 128 rows of z (1 or 2).  kMode 0: softmax partials; kMode 1:
-// the fp32 scores D[m, v] are written to out_scores (M x V).
+// the fp32 scores D[m, v] are written to out_scores (M x V).  tile_ctr is
+// zeroed by the down-projection that precedes this grid.
 template <bool kSample, int MT, int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_head_mma(const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_w,
-               int M, int V, int KB, int NST, float c, int n_tiles, MmaPart part,
-               float* __restrict__ out_scores, unsigned* err) {
+    k_head_mma(const uint16_t* __restrict__ z, const __grid_constant__ CUtensorMap tm_w, int M,
+               int R, int V, int KB, int NST, float c, int n_tiles, MmaPart part,
+               float* __restrict__ out_scores, unsigned* __restrict__ tile_ctr, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;                                 // MT * KB blocks of z
-  uint8_t* sB = smem + (size_t)MT * KB * kBlockBytes; // NST stages of W_up
+  uint8_t* sA = smem;                          // MT * KB compact blocks of z
+  uint8_t* sB = smem + z_bytes(M, KB, MT);     // NST stages of W_up
   __shared__ uint64_t full[kMaxStages], empty[kMaxStages], a_full, acc_full[2], acc_empty[2];
+  __shared__ uint64_t tile_full[kTileRing], tile_empty[kTileRing], mma_done;
+  __shared__ int s_tile[kTileRing];    // vocabulary tile ids, -1 = no more
+  __shared__ int s_fills[kMaxStages];  // TMA fills issued per stage (drained before exit)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  __shared__ RowState s_half[kTileM];
   constexpr uint32_t kCols = 2 * MT * kTileN;  // double-buffered accumulators
   constexpr uint32_t kIdesc = idesc_bf16(kTileM, kTileN);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int t0, nt;
-  cta_tiles(n_tiles, gridDim.x, blockIdx.x, t0, nt);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < NST; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
+      s_fills[s] = 0;
     }
-    mbar_init(&a_full, 1);
+    for (int s = 0; s < kTileRing; ++s) {
+      mbar_init(&tile_full[s], 1);
+      mbar_init(&tile_empty[s], 1 + kEpiWarps);  // the MMA thread and each epilogue warp
+    }
+    mbar_init(&a_full, kEpiWarps);
     mbar_init(&acc_full[0], 1);
     mbar_init(&acc_full[1], 1);
     mbar_init(&acc_empty[0], kEpiWarps);
     mbar_init(&acc_empty[1], kEpiWarps);
+    mbar_init(&mma_done, 1);
     s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 1) tmem_alloc(&s_tmem, kCols);
+  if (warp == kMmaWarp) tmem_alloc(&s_tmem, kCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -236,48 +285,81 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer --
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_w);
-      tma_prefetch_desc(&tm_z);
-      int it = 0;
-      bool a_issued = false;
-      const int total = nt * KB;
-      for (; it < total; ++it) {
-        const int s = it % NST;
-        if (it >= NST && !a_issued) {
-          // z is written by the down-projection that precedes this grid
-          pdl_wait_producer();
-          mbar_arrive_expect_tx(&a_full, (uint32_t)(MT * KB * kBlockBytes));
-          for (int mt = 0; mt < MT; ++mt)
-            for (int kb = 0; kb < KB; ++kb)
-              tma_load_2d(sA + (size_t)(mt * KB + kb) * kBlockBytes, &tm_z, kb * 64,
-                          mt * kTileM, &a_full);
-          a_issued = true;
+    // Stage `it` (counted over all tiles in order) lives in slot it % NST.
+    // Lane 0 waits until the last stage of a group of G is free: the MMA
+    // frees stages in order, so the earlier ones are free too, and with
+    // G <= NST the parity of that slot's barrier names the round waited for.
+    if (lane == 0) tma_prefetch_desc(&tm_w);
+    // Waiting for the last of G stages leaves NST - G + 1 in flight when a
+    // group goes out: a short ring (a large z) issues in pairs.
+    const int G = NST >= 2 * kProdGroup ? kProdGroup : 2;
+    int it = 0;
+    bool ok = true;
+    // Tiles b and b + grid are this CTA's own (the first is loaded while the
+    // down-projection runs); tile kStaticTiles * grid + k goes to whoever
+    // draws k from the counter.  Lane 0 keeps two draws in flight.
+    unsigned q0 = 0, q1 = 0;
+    for (int i = 0; ok; ++i) {
+      int t;
+      if (i < kStaticTiles) {
+        t = blockIdx.x + i * gridDim.x;
+      } else {
+        t = kStaticTiles * gridDim.x + (int)__shfl_sync(0xFFFFFFFFu, q0, 0);
+        if (lane == 0 && t < n_tiles) {  // no new draw once they run past the end
+          q0 = q1;
+          q1 = atomicAdd(tile_ctr, 1u);
         }
-        if (!mbar_wait_bounded(&empty[s], ((it / NST) & 1) ^ 1, err)) {
-          s_abort = 1;
-          break;
-        }
-        const int t = t0 + it / KB, kb = it % KB;
-        mbar_arrive_expect_tx(&full[s], (uint32_t)kBlockBytes);
-        tma_load_2d(sB + (size_t)s * kBlockBytes, &tm_w, kb * 64, t * kTileN, &full[s]);
       }
-      if (!a_issued && it >= total) {
-        pdl_wait_producer();
-        mbar_arrive_expect_tx(&a_full, (uint32_t)(MT * KB * kBlockBytes));
-        for (int mt = 0; mt < MT; ++mt)
-          for (int kb = 0; kb < KB; ++kb)
-            tma_load_2d(sA + (size_t)(mt * KB + kb) * kBlockBytes, &tm_z, kb * 64, mt * kTileM,
-                        &a_full);
+      if (t >= n_tiles) t = -1;
+      const int slot = i % kTileRing;
+      if (lane == 0) {
+        ok = mbar_wait_bounded(&tile_empty[slot], ((i / kTileRing) & 1) ^ 1, err);
+        if (ok) {
+          s_tile[slot] = t;
+          mbar_arrive(&tile_full[slot]);
+        } else {
+          s_abort = 1;
+        }
+      }
+      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+      if (t < 0) break;
+      for (int kb0 = 0; kb0 < KB && ok; kb0 += G) {
+        const int g = KB - kb0 < G ? KB - kb0 : G;
+        const int last = it + g - 1;
+        if (lane == 0 && !mbar_wait_bounded(&empty[last % NST], ((last / NST) & 1) ^ 1, err)) {
+          ok = false;
+          s_abort = 1;
+        }
+        ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+        if (!ok) break;
+        if (lane < g) {
+          const int s = (it + lane) % NST;
+          mbar_arrive_expect_tx(&full[s], (uint32_t)kBlockBytes);
+          tma_load_2d(sB + (size_t)s * kBlockBytes, &tm_w, (kb0 + lane) * 64, t * kTileN,
+                      &full[s]);
+          atomicAdd(&s_fills[s], 1);
+        }
+        __syncwarp();
+        it += g;
+      }
+      if (i == 0 && lane == 0) {
+        pdl_wait_producer();  // the counter is zeroed by the down-projection
+        q0 = atomicAdd(tile_ctr, 1u);
+        q1 = atomicAdd(tile_ctr, 1u);
       }
     }
-  } else if (warp == 1) {
+  } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer --
     if (lane == 0) {
       bool ok = mbar_wait_bounded(&a_full, 0, err);
       tc_fence_after();
       int it = 0;
-      for (int i = 0; i < nt && ok; ++i) {
+      for (int i = 0; ok; ++i) {
+        const int slot = i % kTileRing;
+        if (!mbar_wait_bounded(&tile_full[slot], (i / kTileRing) & 1, err)) { ok = false; break; }
+        const int t = *(volatile int*)&s_tile[slot];
+        mbar_arrive(&tile_empty[slot]);
+        if (t < 0) break;
         const int buf = i & 1;
         if (!mbar_wait_bounded(&acc_empty[buf], ((i >> 1) & 1) ^ 1, err)) { ok = false; break; }
         tc_fence_after();
@@ -290,8 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k4 = 0; k4 < 4; ++k4) {
 #pragma unroll
             for (int mt = 0; mt < MT; ++mt) {
-              const uint64_t adesc =
-                  sw128_desc(smem_u32(sA + (size_t)(mt * KB + kb) * kBlockBytes));
+              const uint64_t adesc = sw128_desc(smem_u32(sA + z_block_off(M, KB, mt, kb)));
               mma_bf16(tmem + (uint32_t)((buf * MT + mt) * kTileN), adesc + 2 * k4,
                        bdesc + 2 * k4, kIdesc, (kb | k4) != 0 ? 1u : 0u);
             }
@@ -302,34 +383,72 @@ __global__ void __launch_bounds__(kThreads, 1)
         mma_commit(&acc_full[buf]);
       }
       if (!ok) s_abort = 1;
+      // every MMA this thread issued has completed before TMEM is freed
+      mma_commit(&mma_done);
+      mbar_wait_bounded(&mma_done, 0, err);
     }
+    __syncwarp();
   } else {
     // ------------------------------------------------------------ epilogue --
-    const int ew = warp - 2;             // 0 .. 7
+    const int ew = warp - kEpiWarp0;     // 0 .. 7
     const int quad = warp & 3;           // the TMEM lane quadrant this warp may read
+    {
+      // z is written by the down-projection that precedes this grid.  Block
+      // (mt, kb) holds rows mt*128 .. +127 and columns kb*64 .. +63 of z; row
+      // i of a block is 128 bytes at i*128, its 16-byte chunk c stored at
+      // chunk c ^ (i % 8) (the 128-byte swizzle).  Columns past r are zero.
+      // Every 16-byte piece is an asynchronous copy, all of a thread's in
+      // flight at once (under a full memory queue each round trip takes
+      // microseconds); pieces past r are zero-filled by the copy itself.
+      pdl_wait_producer();
+      const int n_items = M * KB * 8;  // (row m, K block, 16-byte chunk), chunk fastest
+      for (int it = ew * 32 + lane; it < n_items; it += 32 * kEpiWarps) {
+        const int c8 = it & 7, q = it >> 3;
+        const int m = q / KB, kb = q - m * KB;
+        const int i = m & (kTileM - 1), k0 = kb * 64 + c8 * 8;
+        const bool in = k0 < R;
+        cp_async16_zfill(sA + z_block_off(M, KB, m >> 7, kb) + i * 128 + ((c8 ^ (i & 7)) * 16),
+                         z + (size_t)m * R + (in ? k0 : 0), in ? 16u : 0u);
+      }
+      cp_async_wait_all();
+      fence_proxy_async_smem();  // visible to the tensor cores (async proxy)
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&a_full);
+    }
     const int mt = MT == 2 ? ew / 4 : 0;
     const int half = MT == 2 ? 0 : ew / 4;
     const int row = mt * kTileM + quad * 32 + lane;  // row of z owned by this thread
     const bool live = row < M;
     const bool warp_live = mt * kTileM + quad * 32 < M;  // any live row in this warp
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
-    RowState tot = row_state_empty();
-    for (int i = 0; i < nt; ++i) {
+    const int n_sub = 2 * n_tiles;
+    for (int i = 0;; ++i) {
+      const int slot = i % kTileRing;
+      bool ok = mbar_wait_bounded(&tile_full[slot], (i / kTileRing) & 1, err);
+      const int t = ok ? *(volatile int*)&s_tile[slot] : -1;
+      __syncwarp();
+      if (lane == 0 && ok) mbar_arrive(&tile_empty[slot]);
+      if (!__all_sync(0xFFFFFFFFu, ok) || t < 0) break;
       const int buf = i & 1;
-      const bool ok = mbar_wait_bounded(&acc_full[buf], (i >> 1) & 1, err);
+      ok = mbar_wait_bounded(&acc_full[buf], (i >> 1) & 1, err);
       if (!__all_sync(0xFFFFFFFFu, ok) || *(volatile int*)&s_abort) break;
       tc_fence_after();
-      const int t = t0 + i;
 #pragma unroll
       for (int hh = 0; hh < (MT == 2 ? 2 : 1); ++hh) {
         const int h = MT == 2 ? hh : half;
         RowState st = row_state_empty();
         if (warp_live) {
+          // both 32-column loads of the sub-tile in flight, one wait
+          uint32_t v2[2][32];
+#pragma unroll
+          for (int cc = 0; cc < 2; ++cc)
+            tmem_ld32_issue(tmem + lane_addr + (uint32_t)((buf * MT + mt) * kTileN + h * kSubW + cc * 32),
+                            v2[cc]);
+          tmem_ld_wait();
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc) {
             const int col = h * kSubW + cc * 32;
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_addr + (uint32_t)((buf * MT + mt) * kTileN + col), v);
+            const uint32_t (&v)[32] = v2[cc];
             const int vid0 = t * kTileN + col;
             if (kMode == 1) {
               if (live) {
@@ -350,127 +469,181 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (kMode == 0) {
-          if (live) {
-            const size_t o = (size_t)row * (2 * n_tiles) + 2 * t + h;
-            part.pmax[o] = st.mx;
-            part.parg[o] = st.arg;
-            if (kSample) part.psum[o] = st.sum;
-          }
-          tot = row_state_merge<kSample>(tot, st, c);
+        if (kMode == 0 && live) {
+          const size_t o = (size_t)row * n_sub + 2 * t + h;
+          part.pmax[o] = st.mx;
+          part.parg[o] = st.arg;
+          if (kSample) part.psum[o] = st.sum;
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
     }
-    if (kMode == 0) {
-      // one partial per (row, CTA); with MT == 1 two warps hold the two
-      // column halves of each row and are merged in a fixed order
-      if (MT == 1) {
-        if (half == 1) s_half[quad * 32 + lane] = tot;
-        asm volatile("bar.sync 1, %0;" ::"r"(32 * kEpiWarps) : "memory");
-        if (half == 0) tot = row_state_merge<kSample>(tot, s_half[quad * 32 + lane], c);
-      }
-      if (live && (MT == 2 || half == 0)) {
-        const size_t o = (size_t)row * gridDim.x + blockIdx.x;
-        part.cmax[o] = tot.mx;
-        part.carg[o] = tot.arg;
-        if (kSample) part.csum[o] = tot.sum;
-      }
-    }
   }
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  if (warp == 1) tmem_dealloc(tmem, kCols);
+  if (warp == kMmaWarp) {
+    // No copy may still be landing in shared memory when the CTA exits.  On
+    // the normal path the MMA thread waited for every fill; after an abort it
+    // stopped early, so wait for each stage's last fill (every fill has been
+    // issued by now).  Not the producer's lane 0: a claim it no longer needs
+    // may still be in flight there.
+    if (lane == 0 && *(volatile int*)&s_abort)
+      for (int s = 0; s < NST; ++s)
+        if (s_fills[s] > 0) mbar_wait_bounded(&full[s], (s_fills[s] - 1) & 1, err);
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
 }
 
 // ------------------------------------------------------------------ finish --
-// One CTA of 8 warps per row of z.  Warp 0 merges the partials: the maximum,
-// W and (sampling) the CTA and the 64-row sub-tile where the inverse CDF
-// crosses u * W.  The 8 warps then recompute that sub-tile's logits (8 rows
-// each, every load issued up front; CUDA-core fp32 accumulation of the same
-// bf16 products) and warp 0 walks them in row order.
+// Fixed-order block reductions over the 256 threads of the finish.
+struct BlockArg {
+  float v;
+  int i;
+};
+__device__ __forceinline__ BlockArg better(BlockArg a, BlockArg b) {
+  return (b.v > a.v || (b.v == a.v && b.i < a.i)) ? b : a;  // larger value, then lower index
+}
+// Maximum (lowest index among equals) over the block; every thread gets it.
+__device__ __forceinline__ BlockArg block_argmax(BlockArg x, BlockArg* sh) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    BlockArg y{__shfl_xor_sync(0xFFFFFFFFu, x.v, o), __shfl_xor_sync(0xFFFFFFFFu, x.i, o)};
+    x = better(x, y);
+  }
+  if (lane == 0) sh[warp] = x;
+  __syncthreads();
+  BlockArg r = sh[0];
+#pragma unroll
+  for (int w = 1; w < kFinThreads / 32; ++w) r = better(r, sh[w]);
+  __syncthreads();
+  return r;
+}
+
+// One CTA of 8 warps per row of z.  Thread j owns the contiguous run of
+// sub-tile partials [j*per, (j+1)*per) in vocabulary order, per <= kFinPer,
+// loaded once into registers (all loads of the CTA in flight together).
+//   greedy: the maximum over all sub-tiles, ties to the lowest vocabulary id.
+//   sampling: the maximum g, then each thread's mass sum_s psum_s 2^((pmax_s - g)c)
+//   in order, an ordered block scan of those masses, and the thread whose
+//   run holds the crossing of u * W finds the sub-tile; the 8 warps then
+//   recompute that sub-tile's logits (8 rows each, every load issued up front,
+//   CUDA-core fp32 accumulation of the same bf16 products) and warp 0 walks
+//   them in row order.
 template <bool kSample>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kFinThreads)
     k_head_mma_finish(const uint8_t* __restrict__ w_up, const uint8_t* __restrict__ z, int M,
-                      int r, int V, float c, float inv_t, int n_tiles, int grid, MmaPart part,
+                      int r, int V, float c, float inv_t, int n_sub, MmaPart part,
                       HeadOutputs out) {
   __shared__ float s_logit[kSubW];
-  __shared__ float s_f[4];  // gmax, W, resid
-  __shared__ int s_i[2];    // sub-tile, token (greedy)
+  __shared__ BlockArg s_red[kFinThreads / 32];
+  __shared__ float s_wsum[kFinThreads / 32];
+  __shared__ float s_f[3];  // W, residual mass inside the chosen sub-tile
+  __shared__ int s_i[2];    // chosen thread, chosen sub-tile
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x;
   pdl_wait_producer();
   if (m >= M) return;
-  const int n_sub = 2 * n_tiles;
-  if (warp == 0) {
-    const float* cm = part.cmax + (size_t)m * grid;
-    const int* ca = part.carg + (size_t)m * grid;
-    const float* cs = part.csum + (size_t)m * grid;
-    constexpr int NC = 8;  // up to 256 CTAs
-    float pmx[NC], psm[NC];
-    int pag[NC];
+  const int per = (n_sub + kFinThreads - 1) / kFinThreads;
+  const int j0 = min(n_sub, (int)threadIdx.x * per), nj = min(n_sub, j0 + per) - j0;
+  const float* pm = part.pmax + (size_t)m * n_sub + j0;
+  const float* ps = part.psum + (size_t)m * n_sub + j0;
+  const int* pa = part.parg + (size_t)m * n_sub + j0;
+  float vmx[kFinPer], vsm[kFinPer];
+  int varg[kFinPer];
 #pragma unroll
-    for (int k = 0; k < NC; ++k) {
-      const int t = lane + 32 * k;
-      const bool ok = t < grid;
-      pmx[k] = ok ? __ldcg(cm + t) : kNegInf;
-      pag[k] = ok ? __ldcg(ca + t) : 0x7FFFFFFF;
-      psm[k] = (ok && kSample) ? __ldcg(cs + t) : 0.f;
-    }
-    RowState st = row_state_empty();
-#pragma unroll
-    for (int k = 0; k < NC; ++k)
-      st = row_state_merge<false>(st, RowState{pmx[k], 0.f, pag[k]}, c);
-#pragma unroll
-    for (int b = 0; b < 5; ++b) st = shfl_merge<false>(st, 1 << b, c);
-    const float gmax = st.mx;
-    if (!kSample) {
-      if (lane == 0) {
-        out.tokens[m] = st.arg;
-        if (out.logprob) out.logprob[m] = 0.f;
-        if (out.row_max) out.row_max[m] = gmax;
-        if (out.row_lse) out.row_lse[m] = gmax;
-      }
-    } else {
-      float cmass[NC];
-      float acc = 0.f;
-#pragma unroll
-      for (int k = 0; k < NC; ++k) {
-        cmass[k] = psm[k] * fast_exp2((pmx[k] - gmax) * c);
-        acc = __fadd_rn(acc, cmass[k]);
-      }
-      const float W = warp_sum_fixed(acc);
-      const float target = __ldg(out.uniforms + m) * W;
-      float before1 = 0.f, before2 = 0.f;
-      const int cta = ordered_crossing_regs<NC>(grid, target, cmass, before1, lane);
-      int ct0, cnt;
-      cta_tiles(n_tiles, grid, cta, ct0, cnt);
-      const int s0 = 2 * ct0, ns = 2 * cnt;  // this CTA's sub-tiles, contiguous
-      const float* pm = part.pmax + (size_t)m * n_sub + s0;
-      const float* ps = part.psum + (size_t)m * n_sub + s0;
-      float smass[NC];
-#pragma unroll
-      for (int k = 0; k < NC; ++k) {
-        const int t = lane + 32 * k;
-        smass[k] = t < ns ? __ldcg(ps + t) * fast_exp2((__ldcg(pm + t) - gmax) * c) : 0.f;
-      }
-      const float resid1 = target - before1;
-      const int sid = s0 + ordered_crossing_regs<NC>(ns, resid1, smass, before2, lane);
-      if (lane == 0) {
-        s_f[0] = gmax;
-        s_f[1] = W;
-        s_f[2] = resid1 - before2;
-        s_i[0] = sid;
-      }
-    }
+  for (int k = 0; k < kFinPer; ++k) {
+    vmx[k] = k < nj ? __ldcg(pm + k) : kNegInf;
+    if (kSample) vsm[k] = k < nj ? __ldcg(ps + k) : 0.f;
+    else varg[k] = k < nj ? __ldcg(pa + k) : 0x7FFFFFFF;
   }
-  if (!kSample) return;
+  BlockArg loc{kNegInf, 0x7FFFFFFF};
+#pragma unroll
+  for (int k = 0; k < kFinPer; ++k)
+    if (vmx[k] > loc.v) {
+      loc.v = vmx[k];
+      if (!kSample) loc.i = varg[k];
+    }
+  const BlockArg best = block_argmax(loc, s_red);
+  const float gmax = best.v;
+  if (!kSample) {
+    if (threadIdx.x == 0) {
+      out.tokens[m] = best.i;
+      if (out.logprob) out.logprob[m] = 0.f;
+      if (out.row_max) out.row_max[m] = gmax;
+      if (out.row_lse) out.row_lse[m] = gmax;
+    }
+    return;
+  }
+  // this thread's masses, in order
+  float mass = 0.f;
+#pragma unroll
+  for (int k = 0; k < kFinPer; ++k) {
+    vsm[k] = vsm[k] * fast_exp2((vmx[k] - gmax) * c);  // 0 past the run (0 * 2^-inf)
+    mass = __fadd_rn(mass, vsm[k]);
+  }
+  // ordered block scan: inclusive within the warp, then the warp totals
+  const float wincl = warp_incl_scan(mass, lane);
+  if (lane == 31) s_wsum[warp] = wincl;
   __syncthreads();
-  const float gmax = s_f[0], W = s_f[1], resid = s_f[2];
-  const int v0 = s_i[0] * kSubW;
+  float woff = 0.f, W = 0.f;
+#pragma unroll
+  for (int w = 0; w < kFinThreads / 32; ++w) {
+    if (w < warp) woff = __fadd_rn(woff, s_wsum[w]);
+    W = __fadd_rn(W, s_wsum[w]);
+  }
+  const float incl = __fadd_rn(woff, wincl);
+  const float prev = __shfl_up_sync(0xFFFFFFFFu, wincl, 1);
+  const float excl = lane > 0 ? __fadd_rn(woff, prev) : woff;
+  const float target = __ldg(out.uniforms + m) * W;
+  // the first thread whose inclusive mass passes the target; else the last
+  // thread with any mass (the target sits at the very top after rounding).
+  // Both in one reduction: the key ranks hits above misses, then by thread.
+  const int hit = mass > 0.f && incl > target;
+  const BlockArg sel_r = block_argmax(
+      BlockArg{mass > 0.f ? (hit ? 2.f * kFinThreads - (float)threadIdx.x : (float)threadIdx.x)
+                          : -1.f,
+               0},
+      s_red);
+  const int sel = sel_r.v >= (float)kFinThreads ? (int)(2.f * kFinThreads - sel_r.v)
+                                                : max(0, (int)sel_r.v);
+  if (threadIdx.x == sel) {
+    // walk the run: the first sub-tile with mass whose cumulative passes the
+    // target, else (rounding) the last one with mass
+    float cum = excl, before_sid = excl, before_last = excl;
+    int sid = -1, lastpos = -1;
+#pragma unroll
+    for (int k = 0; k < kFinPer; ++k) {
+      if (k < nj && sid < 0) {
+        const float nxt = __fadd_rn(cum, vsm[k]);
+        if (vsm[k] > 0.f) {
+          if (nxt > target) {
+            sid = j0 + k;
+            before_sid = cum;
+          } else {
+            lastpos = j0 + k;
+            before_last = cum;
+          }
+        }
+        cum = nxt;
+      }
+    }
+    if (sid < 0) {
+      sid = lastpos >= 0 ? lastpos : j0;
+      before_sid = before_last;
+    }
+    s_f[0] = W;
+    s_f[1] = target - before_sid;
+    s_i[1] = sid;
+  }
+  __syncthreads();
+  const float resid = s_f[1];
+  const int v0 = s_i[1] * kSubW;
   const int n = max(0, min(kSubW, V - v0));
   // recompute: warp w takes rows 8w .. 8w+7 of the sub-tile, lanes over K
   const int nch = r / 8;
@@ -511,21 +684,21 @@ __global__ void __launch_bounds__(256)
   __syncthreads();
   if (warp != 0) return;
   float cum = 0.f;
-  int tok = -1, lastp = -1;
+  int tok = -1, lastp2 = -1;
 #pragma unroll
   for (int h = 0; h < kSubW; h += 32) {
     const int i = h + lane;
     const float wv1 = i < n ? fast_exp2((s_logit[i] - gmax) * c) : 0.f;
     const float csum = __fadd_rn(cum, warp_incl_scan(wv1, lane));
     const unsigned pos = __ballot_sync(0xFFFFFFFFu, wv1 > 0.f);
-    const unsigned hit = __ballot_sync(0xFFFFFFFFu, wv1 > 0.f && csum > resid);
-    if (tok < 0 && hit) tok = h + __ffs(hit) - 1;
-    if (pos) lastp = h + 31 - __clz(pos);
+    const unsigned hitm = __ballot_sync(0xFFFFFFFFu, wv1 > 0.f && csum > resid);
+    if (tok < 0 && hitm) tok = h + __ffs(hitm) - 1;
+    if (pos) lastp2 = h + 31 - __clz(pos);
     cum = __shfl_sync(0xFFFFFFFFu, csum, 31);
   }
-  if (tok < 0) tok = lastp < 0 ? 0 : lastp;
+  if (tok < 0) tok = lastp2 < 0 ? 0 : lastp2;
   if (lane == 0) {
-    const float lW = logf(W);
+    const float lW = logf(s_f[0]);
     out.tokens[m] = v0 + tok;
     if (out.logprob) out.logprob[m] = (s_logit[tok] - gmax) * inv_t - lW;
     if (out.row_max) out.row_max[m] = gmax;
@@ -576,7 +749,7 @@ MmaPlan mma_plan(int r, int M, int V) {
   if (M <= 0 || M > 2 * kTileM || r % 8 != 0 || r > 512) return p;  // finish: <= 2 chunks per lane
   p.mt = M <= kTileM ? 1 : 2;
   p.kb = (r + 63) / 64;
-  const int a_bytes = p.mt * p.kb * kBlockBytes;
+  const int a_bytes = z_bytes(M, p.kb, p.mt);
   const int room = kSmemCap - 1024 - a_bytes;
   p.nst = std::min(kMaxStages, room / kBlockBytes);
   if (p.nst < 3) return p;
@@ -584,16 +757,18 @@ MmaPlan mma_plan(int r, int M, int V) {
   p.n_tiles = (V + kTileN - 1) / kTileN;
   p.grid = std::max(1, std::min(sm_count(), p.n_tiles));
   p.n_sub = 2 * p.n_tiles;
+  if (p.n_sub > kFinThreads * kFinPer) return p;  // V > 786432: beyond the finish's registers
   p.ok = true;
   return p;
 }
 
 template <bool kSample, int MT, int kMode>
-static cudaError_t launch_mma_one(const MmaPlan& p, const CUtensorMap& tz, const CUtensorMap& tw,
-                                  int M, int V, float c, const MmaPart& part, float* scores,
-                                  cudaStream_t st) {
+static cudaError_t launch_mma_one(const MmaPlan& p, const void* z, const CUtensorMap& tw, int M,
+                                  int r, int V, float c, const MmaPart& part, float* scores,
+                                  unsigned* ctr, cudaStream_t st) {
   auto kern = k_head_mma<kSample, MT, kMode>;
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), p.smem);
+  // the limit is set once per kernel: make it the largest size any plan asks for
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), kSmemCap);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
@@ -606,37 +781,37 @@ static cudaError_t launch_mma_one(const MmaPlan& p, const CUtensorMap& tz, const
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   ProfScope ps(kKHeadMma, st);
-  return cudaLaunchKernelEx(&cfg, kern, tz, tw, M, V, p.kb, p.nst, c, p.n_tiles, part, scores,
-                            error_word());
+  return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint16_t*>(z), tw, M, r, V, p.kb,
+                            p.nst, c, p.n_tiles, part, scores, ctr, error_word());
 }
 
 cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up, int M, int r,
                             int V, float temperature, const MmaWork& w, const HeadOutputs& out,
-                            float* scores, cudaStream_t st) {
+                            float* scores, unsigned* ctr, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  CUtensorMap tz, tw;
-  if (!make_map(&tz, z_ws, M, r) || !make_map(&tw, w_up, V, r)) return cudaErrorInvalidValue;
+  CUtensorMap tw;
+  if (!make_map(&tw, w_up, V, r)) return cudaErrorInvalidValue;
   const bool sample = temperature > 0.f && scores == nullptr;
   const double inv = sample ? 1.0 / (double)temperature : 0.0;
   const float c = (float)(1.4426950408889634 * inv), inv_t = (float)inv;
-  const MmaPart part{w.pmax, w.psum, w.parg, w.cmax, w.csum, w.carg};
+  const MmaPart part{w.pmax, w.psum, w.parg};
   cudaError_t e;
   if (scores != nullptr) {
-    e = p.mt == 1 ? launch_mma_one<false, 1, 1>(p, tz, tw, M, V, c, part, scores, st)
-                  : launch_mma_one<false, 2, 1>(p, tz, tw, M, V, c, part, scores, st);
+    e = p.mt == 1 ? launch_mma_one<false, 1, 1>(p, z_ws, tw, M, r, V, c, part, scores, ctr, st)
+                  : launch_mma_one<false, 2, 1>(p, z_ws, tw, M, r, V, c, part, scores, ctr, st);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   if (sample)
-    e = p.mt == 1 ? launch_mma_one<true, 1, 0>(p, tz, tw, M, V, c, part, nullptr, st)
-                  : launch_mma_one<true, 2, 0>(p, tz, tw, M, V, c, part, nullptr, st);
+    e = p.mt == 1 ? launch_mma_one<true, 1, 0>(p, z_ws, tw, M, r, V, c, part, nullptr, ctr, st)
+                  : launch_mma_one<true, 2, 0>(p, z_ws, tw, M, r, V, c, part, nullptr, ctr, st);
   else
-    e = p.mt == 1 ? launch_mma_one<false, 1, 0>(p, tz, tw, M, V, c, part, nullptr, st)
-                  : launch_mma_one<false, 2, 0>(p, tz, tw, M, V, c, part, nullptr, st);
+    e = p.mt == 1 ? launch_mma_one<false, 1, 0>(p, z_ws, tw, M, r, V, c, part, nullptr, ctr, st)
+                  : launch_mma_one<false, 2, 0>(p, z_ws, tw, M, r, V, c, part, nullptr, ctr, st);
   if (e != cudaSuccess) return e;
   // the per-row finish, launched to overlap the tail of the MMA grid
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(M);
-  cfg.blockDim = dim3(256);
+  cfg.blockDim = dim3(kFinThreads);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -646,10 +821,10 @@ cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up
   ProfScope ps(kKHeadFinish, st);
   if (sample)
     e = cudaLaunchKernelEx(&cfg, k_head_mma_finish<true>, (const uint8_t*)w_up,
-                           (const uint8_t*)z_ws, M, r, V, c, inv_t, p.n_tiles, p.grid, part, out);
+                           (const uint8_t*)z_ws, M, r, V, c, inv_t, p.n_sub, part, out);
   else
     e = cudaLaunchKernelEx(&cfg, k_head_mma_finish<false>, (const uint8_t*)w_up,
-                           (const uint8_t*)z_ws, M, r, V, c, inv_t, p.n_tiles, p.grid, part, out);
+                           (const uint8_t*)z_ws, M, r, V, c, inv_t, p.n_sub, part, out);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

@@ -68,6 +68,11 @@ cudaError_t set_smem_once(const void* kernel, int bytes) {
   std::lock_guard<std::mutex> lk(mu);
   if (done.count({kernel, dev})) return cudaSuccess;
   e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  // every kernel of the head asks for the same (largest) shared-memory split,
+  // so that the next kernel's CTAs can join an SM without reconfiguring it
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
   if (e == cudaSuccess) done.insert({kernel, dev});
   return e;
 }

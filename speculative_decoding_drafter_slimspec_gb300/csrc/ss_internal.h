@@ -33,8 +33,9 @@ struct ProfScope {
 // from the occupancy calculator, cached per (kernel, device).
 int resident_blocks(const void* kernel, int threads, size_t smem);
 
-// Sets a kernel's dynamic shared memory limit once per (kernel, device), so
-// that no attribute call happens while a stream is being captured later.
+// Sets a kernel's dynamic shared memory limit and the largest shared-memory
+// carveout once per (kernel, device), so that no attribute call happens while
+// a stream is being captured later.
 cudaError_t set_smem_once(const void* kernel, int bytes);
 
 // Rounds a byte count up to the 256-byte workspace granule.
@@ -97,7 +98,7 @@ cudaError_t launch_head_stream(const HeadPlan& plan, bool bf16, const void* w_up
                                HeadPartials part, float* out_logits, const HeadOutputs& out,
                                cudaStream_t st);
 
-// Tensor-core up-projection (head_mma.cu) for more than 8 rows of z.
+// Tensor-core up-projection (head_mma.cu) for bf16 heads.
 struct MmaPlan {
   int mt;       // 128-row tiles of z (1 or 2)
   int kb;       // 64-wide K blocks of r
@@ -113,15 +114,14 @@ struct MmaWork {
   float* pmax;  // [M][n_sub]
   float* psum;
   int* parg;
-  float* cmax;  // [M][grid]
-  float* csum;
-  int* carg;
 };
 // z_ws: M x r bf16.  With `scores` non-null the fp32 products z W_up^T are
-// written there (M x V) instead of being reduced.
+// written there (M x V) instead of being reduced.  ctr: the launch's tile
+// counter, zeroed by the down-projection that precedes it in the stream.
 cudaError_t launch_head_mma(const MmaPlan& plan, const void* z_ws, const void* w_up, int M, int r,
                             int V, float temperature, const MmaWork& work,
-                            const HeadOutputs& out, float* scores, cudaStream_t st);
+                            const HeadOutputs& out, float* scores, unsigned* ctr,
+                            cudaStream_t st);
 
 // ---------------------------------------------------------------- verify --
 size_t verify_ws_bytes(int B, int gamma, int V, bool sample);
