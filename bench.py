@@ -233,7 +233,8 @@ def profiled_traffic(kernel: str, workload: str):
         if ":" in line:
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    src = os.path.join(ROOT, "speculative_decoding_drafter_slimspec_gb300", "csrc", "head.cu")
+    src_file = {"k_head_mma": "head_mma.cu", "k_head_stream": "head.cu"}.get(kernel, "head.cu")
+    src = os.path.join(ROOT, "speculative_decoding_drafter_slimspec_gb300", "csrc", src_file)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     if fields.get("source_sha256") != sha:
         return None
@@ -435,8 +436,8 @@ def run_ours(args, world, rank, local):
     for name, (n, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
         kern[name] = {"launches_per_step": n / n_prof, "us_per_launch": 1000.0 * ms / n,
                       "share": ms / total_ms}
-    # the dominant kernel: the head's up-projection (CUDA-core stream for up to
-    # 8 rows of z, tcgen05 GEMM above)
+    # the dominant kernel: the head's up-projection (the tcgen05 kernel for
+    # bf16 heads, the CUDA-core stream otherwise)
     head_kernel = "k_head_mma" if "k_head_mma" in prof else "k_head_stream"
     hs = prof.get(head_kernel)
     peak, peak_kind = measured_peaks()
