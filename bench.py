@@ -47,11 +47,15 @@ WORKLOADS = {
     "llama8b": (4096, 512, 128256, 8, 6, 0.0),
     "gptoss20b": (2880, 360, 201088, 16, 6, 0.7),
     "qwen30b": (2048, 256, 151936, 256, 4, 1.0),
+    # SpecVocab: r here is the router width d' (router W_down d' x d, W_vocab V x d')
+    "specvocab8b": (4096, 256, 151936, 32, 6, 1.0),
 }
+SPECVOCAB_K = 2048
 WORKLOAD_DESC = {
     "llama8b": "Llama-3.1-8B-shaped speculative round: 6 low-rank head calls (M=8) + greedy verify (B=8)",
     "gptoss20b": "GPT-OSS-20B-shaped speculative round: 6 low-rank head calls (M=16, T=0.7) + sampling verify (B=16)",
     "qwen30b": "Qwen3-30B-A3B-shaped speculative round: 1 low-rank head call (M=256, T=1) + sampling verify (B=64)",
+    "specvocab8b": "Qwen3-8B-shaped SpecVocab round: 6 dynamic-vocabulary head calls (M=32, d'=256, k=2048, T=1) + sampling verify (B=32)",
 }
 
 
@@ -160,12 +164,16 @@ def make_inputs(name: str, seed: int, dev):
     n_calls = gamma if name != "qwen30b" else 1
     n_copies = max(n_calls, 2)
     w_down = (torch.randn(r, d, generator=g, device=dev) / d ** 0.5).to(torch.bfloat16)
+    # the low-rank head's W_up, or SpecVocab's router matrix W_vocab (V x d')
     w_ups = [(torch.randn(V, r, generator=g, device=dev) / r ** 0.5).to(torch.bfloat16)
              for _ in range(n_copies)]
+    # SpecVocab's full head U (V x d, 1.2 GB: one copy, each call gathers its own rows)
+    u_full = ((torch.randn(V, d, generator=g, device=dev) / d ** 0.5).to(torch.bfloat16)
+              if name == "specvocab8b" else None)
     hidden = [torch.randn(M, d, generator=g, device=dev).to(torch.bfloat16)
               for _ in range(n_calls)]
     u_head = [torch.rand(M, generator=g, device=dev) for _ in range(n_calls)]
-    B = M if name != "qwen30b" else 64
+    B = {"qwen30b": 64}.get(name, M)
     ranks = torch.argsort(torch.rand(B * (gamma + 1), V, generator=g, device=dev), dim=1)
     target = (-1.1 * torch.log(ranks.float() + 1.0)
               + 0.5 * torch.randn(B * (gamma + 1), V, generator=g, device=dev))
@@ -179,8 +187,9 @@ def make_inputs(name: str, seed: int, dev):
     else:
         tokens = torch.argmax(draft, dim=2).to(torch.int32)
     u_verify = torch.rand(B, gamma + 1, generator=g, device=dev)
-    return dict(d=d, r=r, V=V, M=M, B=B, gamma=gamma, T=T, n_calls=n_calls, w_down=w_down,
-                w_ups=w_ups, hidden=hidden, u_head=u_head, target=target,
+    return dict(name=name, d=d, r=r, V=V, M=M, B=B, gamma=gamma, T=T, n_calls=n_calls,
+                w_down=w_down, w_ups=w_ups, u_full=u_full, hidden=hidden, u_head=u_head,
+                target=target,
                 draft=draft if T > 0 else None, tokens=tokens, u_verify=u_verify)
 
 
@@ -193,8 +202,10 @@ class Round:
         self.x, self.ss = x, ss
         dev = x["w_down"].device
         M, d, r, V, B, gamma = x["M"], x["d"], x["r"], x["V"], x["B"], x["gamma"]
-        self.head_ws = torch.empty(ss.slimspec_head_workspace_size(M, d, r, V, ss.SS_BF16),
-                                   dtype=torch.uint8, device=dev)
+        self.specvocab = x["u_full"] is not None
+        hw = (ss.specvocab_head_workspace_size(M, d, r, V, SPECVOCAB_K) if self.specvocab
+              else ss.slimspec_head_workspace_size(M, d, r, V, ss.SS_BF16))
+        self.head_ws = torch.empty(hw, dtype=torch.uint8, device=dev)
         self.ver_ws = torch.empty(max(256, ss.spec_verify_workspace_size(B, gamma, V, x["T"])),
                                   dtype=torch.uint8, device=dev)
         self.head_out = [{"tokens": torch.empty(M, dtype=torch.int32, device=dev)}
@@ -202,13 +213,24 @@ class Round:
         self.ver_out = {"tokens": torch.empty(B, gamma + 1, dtype=torch.int32, device=dev),
                         "num_accepted": torch.empty(B, dtype=torch.int32, device=dev)}
 
+    def head_call(self, j, hidden, u):
+        """Head call j of the round (the low-rank head or the SpecVocab head)."""
+        x, ss = self.x, self.ss
+        T = x["T"]
+        if self.specvocab:
+            return ss.specvocab_head_forward(hidden, x["w_down"], x["w_ups"][j % len(x["w_ups"])],
+                                             x["u_full"], SPECVOCAB_K, T, u if T > 0 else None,
+                                             want_topk=False, workspace=self.head_ws,
+                                             out=self.head_out[j])
+        return ss.slimspec_head_forward(hidden, x["w_down"], x["w_ups"][j % len(x["w_ups"])], T,
+                                        u if T > 0 else None, want_stats=False,
+                                        workspace=self.head_ws, out=self.head_out[j])
+
     def step(self):
         x, ss = self.x, self.ss
         T = x["T"]
         for j in range(x["n_calls"]):
-            ss.slimspec_head_forward(x["hidden"][j], x["w_down"], x["w_ups"][j % len(x["w_ups"])],
-                                     T, x["u_head"][j] if T > 0 else None, want_stats=False,
-                                     workspace=self.head_ws, out=self.head_out[j])
+            self.head_call(j, x["hidden"][j], x["u_head"][j])
         ss.spec_verify(x["target"], x["draft"], x["tokens"], T,
                        x["u_verify"] if T > 0 else None, workspace=self.ver_ws,
                        out=self.ver_out)
@@ -220,6 +242,74 @@ def head_stream_bytes(x) -> float:
     (M*r*2).  Partials are overhead."""
     M, r, V = x["M"], x["r"], x["V"]
     return V * r * 2 + M * r * 2
+
+
+def kernel_bytes(x, union_rows: float) -> dict:
+    """Algorithmic bytes of one launch of each hot kernel (what the step must
+    move at least once; partials and workspaces are overhead)."""
+    M, d, r, V, B, gamma = x["M"], x["d"], x["r"], x["V"], x["B"], x["gamma"]
+    rows = B * (gamma + 1) + (B * gamma if x["T"] > 0 else 0)
+    out = {"k_head_mma": head_stream_bytes(x), "k_head_stream": head_stream_bytes(x),
+           "k_down_proj": r * d * 2 + M * d * 2 + M * r * 2,
+           "k_verify_rows": rows * V * 4}
+    if x["u_full"] is not None:
+        out["k_gather_logits"] = union_rows * d * 2 + M * d * 2
+        out["k_topk"] = M * V * 4
+    return out
+
+
+def specvocab_union_rows(x, rnd, ss) -> float:
+    """Mean number of distinct U rows one SpecVocab call gathers (the union of
+    its rows' top-k sets)."""
+    import torch
+    if x["u_full"] is None:
+        return 0.0
+    sizes = []
+    for j in range(x["n_calls"]):
+        o = ss.specvocab_head_forward(x["hidden"][j], x["w_down"], x["w_ups"][j % len(x["w_ups"])],
+                                      x["u_full"], SPECVOCAB_K, x["T"], x["u_head"][j],
+                                      want_topk=True, workspace=rnd.head_ws)
+        sizes.append(torch.unique(o["topk_idx"]).numel())
+    return float(sum(sizes)) / len(sizes)
+
+
+def roofline_for(kernel, prof, nbytes, peak, peak_kind, workload):
+    n, ms = prof[kernel]
+    dur = ms / n / 1000.0
+    ach = nbytes / dur / 1e9
+    return {"kernel": kernel, "bound": "hbm", "achieved": ach, "peak": peak, "unit": "GB/s",
+            "frac": ach / peak, "traffic": profiled_traffic(kernel, workload),
+            "algorithmic_bytes_per_launch": nbytes, "peak_source": peak_kind,
+            "us_per_launch": dur * 1e6}
+
+
+def dense_head_comparison(x, head_us):
+    """The dense V x d head the low-rank head replaces, as one cuBLAS bf16 GEMM
+    (torch.matmul, logits only, no reduction) on the same GPU."""
+    import torch
+    dev = x["w_down"].device
+    M, d, V = x["M"], x["d"], x["V"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(99)
+    w = (torch.randn(V, d, generator=g, device=dev) / d ** 0.5).to(torch.bfloat16)
+    h = x["hidden"][0]
+    for _ in range(3):
+        torch.matmul(h, w.t())
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    n = 20
+    e0.record()
+    for _ in range(n):
+        torch.matmul(h, w.t())
+    e1.record()
+    torch.cuda.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / n
+    nbytes = V * d * 2
+    del w
+    return {"kernel": "cuBLAS bf16 GEMM via torch.matmul (dense V x d logits, no reduction)",
+            "us_per_call": us, "bytes": nbytes, "GB/s": nbytes / us / 1e3,
+            "low_rank_up_projection_us": head_us,
+            "speedup_vs_dense": (us / head_us) if head_us else None}
 
 
 def profiled_traffic(kernel: str, workload: str):
@@ -275,8 +365,14 @@ def oracle_round_rate(x_np: dict, budget_s: float, max_steps: int | None = None,
 
     def sample(S):
         t0 = time.perf_counter()
-        oracle.slimspec_head(x_np["hidden"][:1], x_np["w_down"], x_np["w_up"][:S], "bf16", T,
-                             x_np["u_head"][:1] if T > 0 else None)
+        if x_np.get("u_full") is not None:   # SpecVocab: router, top-k, gather over S entries
+            k_s = max(16, SPECVOCAB_K * S // V)
+            oracle.specvocab_head(x_np["hidden"][:1], x_np["w_down"], x_np["w_up"][:S],
+                                  x_np["u_full"][:S], k_s, T,
+                                  x_np["u_head"][:1] if T > 0 else None)
+        else:
+            oracle.slimspec_head(x_np["hidden"][:1], x_np["w_down"], x_np["w_up"][:S], "bf16", T,
+                                 x_np["u_head"][:1] if T > 0 else None)
         t1 = time.perf_counter()
         tg = x_np["target"][:1, :, :S]
         dr = x_np["draft"][:1, :, :S] if T > 0 else None
@@ -285,10 +381,11 @@ def oracle_round_rate(x_np: dict, budget_s: float, max_steps: int | None = None,
         t2 = time.perf_counter()
         return t1 - t0, t2 - t1
 
-    th, tv = sample(V)          # calibration on the full row (untimed)
-    full = th + tv
+    cal = V if x_np.get("u_full") is None else x_np["u_full"].shape[0]
+    th, tv = sample(cal)        # calibration (untimed), on the full row when it is held
+    full = (th + tv) * V / cal
     per_step = budget_s if steps_exact is None else budget_s / max(1, steps_exact)
-    S = V if full <= per_step else max(1024, int(V * per_step / full))
+    S = min(cal, V if full <= per_step else max(1024, int(V * per_step / full)))
     steps = steps_exact if steps_exact is not None else max(1, min(max_steps or 10 ** 9,
                                                                   int(budget_s / max(1e-9, full * S / V))))
     tot_h = tot_v = 0.0
@@ -309,7 +406,10 @@ def numpy_inputs(x):
                 u_head=x["u_head"][0].cpu().numpy(),
                 target=x["target"].cpu().numpy(),
                 draft=x["draft"].cpu().numpy() if x["draft"] is not None else None,
-                tokens=x["tokens"].cpu().numpy(), u_verify=x["u_verify"].cpu().numpy())
+                tokens=x["tokens"].cpu().numpy(), u_verify=x["u_verify"].cpu().numpy(),
+                # SpecVocab's U: the first 32768 rows are as far as a CPU sample reaches
+                u_full=(x["u_full"][:32768].float().cpu().numpy()
+                        if x["u_full"] is not None else None))
 
 
 def cores():
@@ -349,6 +449,11 @@ def run_reference(args, world, rank):
 
 def config_dict(workload):
     d, r, V, M, gamma, T = WORKLOADS[workload]
+    if workload == "specvocab8b":
+        return {"workload": WORKLOAD_DESC[workload], "d": d, "d_prime": r, "V": V, "k": SPECVOCAB_K,
+                "M": M, "gamma": gamma, "temperature": T, "parallelism": "replicas",
+                "l2": "W_vocab rotated over one copy per head call, U (1.2 GB) and the gathered "
+                      "rows (~0.4 GB per call) larger than L2"}
     return {"workload": WORKLOAD_DESC[workload], "d": d, "r": r, "V": V, "M": M,
             "gamma": gamma, "temperature": T, "parallelism": "replicas",
             "l2": "W_up rotated over one copy per head call and the round reads "
@@ -373,6 +478,9 @@ def run_ours(args, world, rank, local):
             rnd.step()
     stream.synchronize()
     assert ss.ss_get_device_error() == ss.SS_OK
+    with torch.cuda.stream(stream):
+        union_rows = specvocab_union_rows(x, rnd, ss)
+    stream.synchronize()
 
     graph = torch.cuda.CUDAGraph()
     n0 = ss.launch_count()
@@ -436,27 +544,30 @@ def run_ours(args, world, rank, local):
     for name, (n, ms) in sorted(prof.items(), key=lambda kv: -kv[1][1]):
         kern[name] = {"launches_per_step": n / n_prof, "us_per_launch": 1000.0 * ms / n,
                       "share": ms / total_ms}
-    # the dominant kernel: the head's up-projection (the tcgen05 kernel for
-    # bf16 heads, the CUDA-core stream otherwise)
-    head_kernel = "k_head_mma" if "k_head_mma" in prof else "k_head_stream"
-    hs = prof.get(head_kernel)
+    # the dominant kernel (largest share of the step among the kernels with
+    # algorithmic bytes), the head's up-projection, and the verifier's row pass
     peak, peak_kind = measured_peaks()
-    roof = None
-    if hs:
-        dur = hs[1] / hs[0] / 1000.0
-        nbytes = head_stream_bytes(x)
-        ach = nbytes / dur / 1e9
-        roof = {"kernel": head_kernel, "bound": "hbm", "achieved": ach, "peak": peak,
-                "unit": "GB/s", "frac": ach / peak,
-                "traffic": profiled_traffic(head_kernel, args.workload),
-                "algorithmic_bytes_per_launch": nbytes, "peak_source": peak_kind,
-                "us_per_launch": dur * 1e6}
+    kb = kernel_bytes(x, union_rows)
+    cands = [k for k in prof if k in kb]
+    roof = head_roof = ver_roof = None
+    if cands:
+        dom = max(cands, key=lambda k: prof[k][1])
+        roof = roofline_for(dom, prof, kb[dom], peak, peak_kind, args.workload)
+    head_kernel = next((k for k in ("k_head_mma", "k_head_stream") if k in prof), None)
+    if head_kernel:
+        head_roof = roofline_for(head_kernel, prof, kb[head_kernel], peak, peak_kind, args.workload)
         if head_kernel == "k_head_mma":
             flops = 2.0 * x["M"] * x["V"] * x["r"]
             tpeak = measured_tensor_peak()
-            roof["tensor"] = {"achieved": flops / dur / 1e12, "peak": tpeak, "unit": "TFLOP/s",
-                              "frac": flops / dur / 1e12 / tpeak,
-                              "algorithmic_flops_per_launch": flops}
+            dur = head_roof["us_per_launch"] / 1e6
+            head_roof["tensor"] = {"achieved": flops / dur / 1e12, "peak": tpeak,
+                                   "unit": "TFLOP/s", "frac": flops / dur / 1e12 / tpeak,
+                                   "algorithmic_flops_per_launch": flops}
+            if roof and roof["kernel"] == head_kernel:
+                roof["tensor"] = head_roof["tensor"]
+    if "k_verify_rows" in prof:
+        ver_roof = roofline_for("k_verify_rows", prof, kb["k_verify_rows"], peak, peak_kind,
+                                args.workload)
     ver_ms = sum(ms for name, (n, ms) in prof.items() if name.startswith("k_verify")) / n_prof
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1000.0 / args.steps,
@@ -464,6 +575,8 @@ def run_ours(args, world, rank, local):
             "data": "synthetic: seeded N(0,1/fan_in) bf16 weights, N(0,1) hidden states, "
                     "Zipf-like target logits",
             "config": config_dict(args.workload), "roofline": roof,
+            "head_roofline": head_roof, "verify_roofline": ver_roof,
+            "specvocab_union_rows": union_rows if x["u_full"] is not None else None,
             "gpu_launches": int(launches_per_step * args.steps),
             "verify_steps_per_s": (1000.0 / ver_ms) if ver_ms > 0 else None,
             "kernels": kern}
@@ -471,6 +584,10 @@ def run_ours(args, world, rank, local):
         line["clocks"] = sampler.summary(wall0, wall1)
     if e2e:
         line["e2e"] = e2e
+    if args.workload == "llama8b" and not args.no_dense:
+        # the Llama-shaped configuration also names the dense 128256 x 4096 head
+        line["dense_head"] = dense_head_comparison(
+            x, head_roof["us_per_launch"] if head_roof else None)
     if world == 1 and not args.no_cpu_baseline:
         x_np = numpy_inputs(x)
         rate, steps, S, secs_cpu = oracle_round_rate(x_np, args.cpu_budget)
@@ -517,9 +634,7 @@ def run_e2e(args, x, ss, stream, world):
             d_dev.copy_(d_host, non_blocking=True)
         off = 0
         for j in range(x["n_calls"]):
-            o = ss.slimspec_head_forward(h_dev[j], x["w_down"], x["w_ups"][j % len(x["w_ups"])],
-                                         T, u_dev[j] if T > 0 else None, want_stats=False,
-                                         workspace=rnd.head_ws, out=rnd.head_out[j])
+            o = rnd.head_call(j, h_dev[j], u_dev[j])
             res[off:off + x["M"]].copy_(o["tokens"])
             off += x["M"]
         v = ss.spec_verify(t_dev, d_dev, k_dev, T, uv_dev if T > 0 else None,
@@ -566,6 +681,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-dense", action="store_true",
+                    help="skip the dense V x d head comparison (llama8b)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -8,10 +8,10 @@
 // left to move W_up at the speed of HBM.  One persistent CTA per SM,
 // warp-specialised, with the per-row softmax reduction as the GEMM epilogue:
 //
-//   warp 0      producer.  It takes 128-row vocabulary tiles (two fixed ones,
+//   warp 0      producer.  It takes 128-row vocabulary tiles (fixed ones,
 //               then the next free tile from a global counter, so that SMs
 //               that stream faster take more tiles; under a full HBM queue an
-//               atomic takes microseconds, so two claims stay in flight),
+//               atomic takes microseconds, so each draw is made a tile ahead),
 //               hands their ids to the other warps through a small ring in
 //               shared memory,
 //               and loads W_up (B, one 64-wide K block of a tile per 16 KB
@@ -295,20 +295,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = NST >= 2 * kProdGroup ? kProdGroup : 2;
     int it = 0;
     bool ok = true;
-    // Tiles b and b + grid are this CTA's own (the first is loaded while the
-    // down-projection runs); tile kStaticTiles * grid + k goes to whoever
-    // draws k from the counter.  Lane 0 keeps two draws in flight.
-    unsigned q0 = 0, q1 = 0;
+    // Tiles b + k * grid (k < kStaticTiles) are this CTA's own (the first is
+    // loaded while the down-projection runs); tile kStaticTiles * grid + k
+    // goes to whoever draws k from the counter.  Lane 0 draws one tile ahead:
+    // the draw gets a tile's worth of loads to come back, and a CTA holds at
+    // most one tile it has not started when the counter runs out.
+    unsigned q0 = 0;
     for (int i = 0; ok; ++i) {
       int t;
       if (i < kStaticTiles) {
         t = blockIdx.x + i * gridDim.x;
       } else {
         t = kStaticTiles * gridDim.x + (int)__shfl_sync(0xFFFFFFFFu, q0, 0);
-        if (lane == 0 && t < n_tiles) {  // no new draw once they run past the end
-          q0 = q1;
-          q1 = atomicAdd(tile_ctr, 1u);
-        }
+        if (lane == 0 && t < n_tiles) q0 = atomicAdd(tile_ctr, 1u);  // none past the end
       }
       if (t >= n_tiles) t = -1;
       const int slot = i % kTileRing;
@@ -342,10 +341,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         it += g;
       }
-      if (i == 0 && lane == 0) {
+      if (i == kStaticTiles - 1 && lane == 0) {
         pdl_wait_producer();  // the counter is zeroed by the down-projection
         q0 = atomicAdd(tile_ctr, 1u);
-        q1 = atomicAdd(tile_ctr, 1u);
       }
     }
   } else if (warp == kMmaWarp) {
