@@ -176,7 +176,7 @@ static int sv_check(int M, int d, int d_prime, int V, int k) {
   if (k < 1 || k > V) return SS_ERR_INVALID_ARG;
   if (d > 4096 || d_prime > 1024 || k > 4096) return SS_ERR_UNSUPPORTED;
   if ((long long)V * d * 2 >= (1LL << 40)) return SS_ERR_UNSUPPORTED;
-  if (!head_plan(true, d_prime, M, V).ok) return SS_ERR_UNSUPPORTED;
+  if (!mma_plan(d_prime, M, V).ok && !head_plan(true, d_prime, M, V).ok) return SS_ERR_UNSUPPORTED;
   return SS_OK;
 }
 

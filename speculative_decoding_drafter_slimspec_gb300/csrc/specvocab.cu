@@ -2,7 +2,8 @@
 //
 // SpecVocab write-up (动态词汇推测加速大语言模型推理), sections 2.2.1-2.2.3:
 //   h' = bf16(W_down h)        (k_down_proj, shared with the low-rank head)
-//   s  = W_vocab h'            (the head's streaming GEMV, scores written out)
+//   s  = W_vocab h'            (the head's tcgen05 up-projection in its scores
+//                              mode, or the CUDA-core stream when it does not fit)
 //   K  = topk(s, k)            k_topk: radix select on order-preserving keys,
 //                              ties to the lowest id, ordered compaction
 //   z' = U[K] h                k_gather_logits: a warp per candidate row of U
@@ -47,33 +48,45 @@ __device__ __forceinline__ int block_scan_incl_1024(int x, int* s_warp) {
 }
 
 // ------------------------------------------------------------------- top-k --
-// One CTA of 1024 threads per row.  Three histogram passes over the keys
-// (digits of 11, 11 and 10 bits, most significant first) find the key T* of
-// the k-th largest score and how many of the keys equal to T* are kept; an
-// ordered compaction then writes the kept ids in ascending order.
-__global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores, int V, int k,
-                                               int32_t* __restrict__ out_idx) {
-  const int row = blockIdx.x, tid = threadIdx.x;
-  const float* s = scores + (size_t)row * V;
-  __shared__ int hist[2048];
-  __shared__ int s_warp[32];
-  __shared__ int s_bin, s_above;
+// Keys are order-preserving uint32 images of the fp32 scores (float_key), so
+// "largest scores" = "largest keys", and ties are broken by the lowest id.
+constexpr int kTopkThreads = 1024;
+constexpr int kTopkCap = 8192;     // candidate buffer (keys + ids) in shared memory
+constexpr int kTopkSample = 8192;  // sampled scores that estimate the threshold
+
+struct KeysFromScores {  // the row's scores, read from global memory
+  const float* s;
+  __device__ uint32_t operator()(int i) const { return float_key(s[i]); }
+};
+struct KeysInShared {
+  const uint32_t* k;
+  __device__ uint32_t operator()(int i) const { return k[i]; }
+};
+
+// Key T of the q-th largest of n keys (1 <= q <= n) and `need`, how many of
+// the keys equal to T are among the q largest.  Three histogram passes over
+// digits of 11, 11 and 10 bits, most significant first; every thread of the
+// block calls it.
+template <class Keys>
+__device__ void block_select_desc(const Keys& key_at, int n, int q, int* hist, int* s_warp,
+                                  int* s_sel, uint32_t& thr, int& need) {
+  const int tid = threadIdx.x;
   uint32_t prefix = 0, pmask = 0;
-  int need = k;
-  if (tid == 0) { s_bin = 0; s_above = 0; }
+  need = q;
 #pragma unroll 1
   for (int pass = 0; pass < 3; ++pass) {
     const int nb = pass < 2 ? 2048 : 1024;
     const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
-    for (int i = tid; i < 2048; i += 1024) hist[i] = 0;
+    for (int i = tid; i < 2048; i += kTopkThreads) hist[i] = 0;
+    if (tid == 0) { s_sel[0] = 0; s_sel[1] = 0; }
     __syncthreads();
-    for (int v = tid; v < V; v += 1024) {
-      const uint32_t key = float_key(s[v]);
+    for (int i = tid; i < n; i += kTopkThreads) {
+      const uint32_t key = key_at(i);
       if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1);
     }
     __syncthreads();
     // thread t owns bins nb-1-t*bpt-i (i < bpt): descending bin order
-    const int bpt = nb / 1024;
+    const int bpt = nb / kTopkThreads;
     int local = 0;
     for (int i = 0; i < bpt; ++i) local += hist[nb - 1 - tid * bpt - i];
     const int incl = block_scan_incl_1024(local, s_warp);
@@ -83,74 +96,168 @@ __global__ void __launch_bounds__(1024) k_topk(const float* __restrict__ scores,
       for (int i = 0; i < bpt; ++i) {
         const int bin = nb - 1 - tid * bpt - i;
         if (cum + hist[bin] >= need) {
-          s_bin = bin;
-          s_above = cum;
+          s_sel[0] = bin;
+          s_sel[1] = cum;
           break;
         }
         cum += hist[bin];
       }
     }
     __syncthreads();
-    need -= s_above;
-    prefix |= (uint32_t)s_bin << shift;
+    need -= s_sel[1];
+    prefix |= (uint32_t)s_sel[0] << shift;
     pmask |= (uint32_t)(nb - 1) << shift;
     __syncthreads();
   }
-  const uint32_t thr = prefix;  // key of the k-th largest score
-  // ordered compaction over contiguous segments
-  const int seg = (V + 1023) / 1024;
-  const int lo = min(V, tid * seg), hi = min(V, lo + seg);
+  thr = prefix;
+}
+
+// Ordered compaction of n keys against (thr, need): every key above thr and
+// the first `need` keys equal to it, in index order.  Warp w owns a
+// contiguous segment of entries and walks it 32 at a time (coalesced reads);
+// ballots rank the kept entries of a step, so the output is in index order.
+template <class Keys, class Ids>
+__device__ void block_compact(const Keys& key_at, const Ids& id_at, int n, uint32_t thr, int need,
+                              int k, int* s_cnt, int32_t* out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int segw = ((n + 1023) / 1024) * 32;  // entries per warp, a multiple of 32
+  const int lo = min(n, warp * segw), hi = min(n, lo + segw);
+  const unsigned lt = (1u << lane) - 1u;
   int gt = 0, eq = 0;
-  for (int v = lo; v < hi; ++v) {
-    const uint32_t key = float_key(s[v]);
-    gt += key > thr;
-    eq += key == thr;
+  for (int v0 = lo; v0 < hi; v0 += 32) {
+    const int v = v0 + lane;
+    const uint32_t key = v < hi ? key_at(v) : 0u;
+    gt += __popc(__ballot_sync(0xFFFFFFFFu, v < hi && key > thr));
+    eq += __popc(__ballot_sync(0xFFFFFFFFu, v < hi && key == thr));
   }
-  const int gt_incl = block_scan_incl_1024(gt, s_warp);
-  const int eq_incl = block_scan_incl_1024(eq, s_warp);
-  int pos = (gt_incl - gt) + min(eq_incl - eq, need);
-  int eq_seen = eq_incl - eq;
+  if (lane == 0) { s_cnt[warp] = gt; s_cnt[32 + warp] = eq; }
+  __syncthreads();
+  int gt_pre = 0, eq_pre = 0;
+  for (int w = 0; w < warp; ++w) { gt_pre += s_cnt[w]; eq_pre += s_cnt[32 + w]; }
+  __syncthreads();
+  int pos = gt_pre + min(eq_pre, need), eq_seen = eq_pre;
+  for (int v0 = lo; v0 < hi; v0 += 32) {
+    const int v = v0 + lane;
+    const uint32_t key = v < hi ? key_at(v) : 0u;
+    const bool is_gt = v < hi && key > thr, is_eq = v < hi && key == thr;
+    const unsigned eqb = __ballot_sync(0xFFFFFFFFu, is_eq);
+    const bool keep = is_gt || (is_eq && eq_seen + __popc(eqb & lt) < need);
+    const unsigned kb = __ballot_sync(0xFFFFFFFFu, keep);
+    const int my = pos + __popc(kb & lt);
+    if (keep && my < k) out[my] = id_at(v);
+    pos += __popc(kb);
+    eq_seen += __popc(eqb);
+  }
+}
+struct IdSelf {
+  __device__ int32_t operator()(int i) const { return i; }
+};
+struct IdInShared {
+  const int32_t* id;
+  __device__ int32_t operator()(int i) const { return id[i]; }
+};
+
+// One CTA of 1024 threads per row.
+//   1. A threshold t: the key of rank ~1.25 k V / S in a strided sample of S
+//      scores (exact rank k when the sample is the whole row).
+//   2. One ordered pass keeps every score with key >= t, in id order, in a
+//      shared buffer of kTopkCap entries.
+//   3. Exact selection among those: they hold the k largest whenever there are
+//      at least k of them, so the result is the full row's; otherwise (or on
+//      overflow) the selection runs over the whole row instead.
+__global__ void __launch_bounds__(kTopkThreads) k_topk(const float* __restrict__ scores, int V,
+                                                       int k, int32_t* __restrict__ out_idx) {
+  extern __shared__ uint32_t s_dyn[];
+  uint32_t* c_key = s_dyn;                                     // kTopkCap keys
+  int32_t* c_id = reinterpret_cast<int32_t*>(s_dyn + kTopkCap);  // kTopkCap ids
+  __shared__ int hist[2048];
+  __shared__ int s_warp[32];
+  __shared__ int s_sel[2];
+  const int row = blockIdx.x, tid = threadIdx.x;
+  const float* s = scores + (size_t)row * V;
   int32_t* out = out_idx + (size_t)row * k;
-  for (int v = lo; v < hi; ++v) {
-    const uint32_t key = float_key(s[v]);
-    if (key > thr) {
-      if (pos < k) out[pos] = v;
-      ++pos;
-    } else if (key == thr) {
-      if (eq_seen < need) {
-        if (pos < k) out[pos] = v;
-        ++pos;
+  const KeysFromScores row_keys{s};
+
+  // 1. the threshold from the sample (held in the candidate buffer for now):
+  //    S scores in blocks of 32 consecutive ones spread evenly over the row
+  const int S = min(V, kTopkSample);
+  const int lane = tid & 31, warp = tid >> 5;
+  if (S == V) {
+    for (int i = tid; i < S; i += kTopkThreads) c_key[i] = float_key(s[i]);
+  } else {
+    const int nblk = S / 32;
+    for (int b = warp; b < nblk; b += kTopkThreads / 32)
+      c_key[b * 32 + lane] = float_key(s[(int)(((long long)b * (V - 32)) / (nblk - 1)) + lane]);
+  }
+  __syncthreads();
+  int q = k;
+  if (S < V) q = min(S, (int)((5LL * k * S + 4LL * V - 1) / (4LL * V)) + 8);
+  uint32_t t_low;
+  int unused;
+  block_select_desc(KeysInShared{c_key}, S, q, hist, s_warp, s_sel, t_low, unused);
+
+  // 2. ordered filter of the row into the buffer (warp segments, coalesced)
+  const int segw = ((V + 1023) / 1024) * 32;
+  const int lo = min(V, warp * segw), hi = min(V, lo + segw);
+  const unsigned lt = (1u << lane) - 1u;
+  int cnt = 0;
+  for (int v0 = lo; v0 < hi; v0 += 32) {
+    const int v = v0 + lane;
+    cnt += __popc(__ballot_sync(0xFFFFFFFFu, v < hi && float_key(s[min(v, V - 1)]) >= t_low));
+  }
+  if (lane == 0) hist[warp] = cnt;
+  __syncthreads();
+  int pre = 0, n_c = 0;
+  for (int w = 0; w < kTopkThreads / 32; ++w) {
+    if (w < warp) pre += hist[w];
+    n_c += hist[w];
+  }
+  __syncthreads();
+  uint32_t thr;
+  int need;
+  if (n_c >= k && n_c <= kTopkCap) {
+    int pos = pre;
+    for (int v0 = lo; v0 < hi; v0 += 32) {
+      const int v = v0 + lane;
+      const uint32_t key = float_key(s[min(v, V - 1)]);
+      const bool keep = v < hi && key >= t_low;
+      const unsigned kb = __ballot_sync(0xFFFFFFFFu, keep);
+      if (keep) {
+        const int my = pos + __popc(kb & lt);
+        c_key[my] = key;
+        c_id[my] = v;
       }
-      ++eq_seen;
+      pos += __popc(kb);
     }
+    __syncthreads();
+    // 3. exact selection among the candidates
+    block_select_desc(KeysInShared{c_key}, n_c, k, hist, s_warp, s_sel, thr, need);
+    block_compact(KeysInShared{c_key}, IdInShared{c_id}, n_c, thr, need, k, hist, out);
+  } else {
+    block_select_desc(row_keys, V, k, hist, s_warp, s_sel, thr, need);
+    block_compact(row_keys, IdSelf{}, V, thr, need, k, hist, out);
   }
 }
 
 // ----------------------------------------------------------------- gather --
 // blockIdx.x = row m of h, blockIdx.y = block of 64 candidates; warp w takes
-// candidates 8w .. 8w+7 of the block.  h[m] lives in registers (CPL 16-byte
-// chunks per lane, d <= 256 * CPL).
+// candidates 8w .. 8w+7 of the block.  h[m] (bf16, d <= 256 * CPL) sits in
+// shared memory, so a thread holds only its CPL 16-byte chunks of the U row
+// in flight and several CTAs share an SM.  Products are the bf16 x bf16
+// products (exact in fp32), accumulated in chunk order, element order.
 template <int CPL>
 __global__ void __launch_bounds__(256)
     k_gather_logits(const uint8_t* __restrict__ h, const uint8_t* __restrict__ U,
                     const int32_t* __restrict__ idx, int M, int d, int k, int V,
                     float* __restrict__ cand_logits) {
+  __shared__ uint4 s_h[32 * CPL];
   const int m = blockIdx.x, lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int nch = d / 8;
   const size_t rowb = (size_t)d * 2;
-  float hr[CPL][8];
-#pragma unroll
-  for (int c = 0; c < CPL; ++c) {
-    const int ch = lane + 32 * c;
-    if (ch < nch) {
-      const uint4 w = __ldg(reinterpret_cast<const uint4*>(h + (size_t)m * rowb + ch * 16));
-      hr[c][0] = bf16lo(w.x); hr[c][1] = bf16hi(w.x); hr[c][2] = bf16lo(w.y); hr[c][3] = bf16hi(w.y);
-      hr[c][4] = bf16lo(w.z); hr[c][5] = bf16hi(w.z); hr[c][6] = bf16lo(w.w); hr[c][7] = bf16hi(w.w);
-    } else {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) hr[c][e] = 0.f;
-    }
-  }
+  for (int ch = threadIdx.x; ch < 32 * CPL; ch += blockDim.x)
+    s_h[ch] = ch < nch ? __ldg(reinterpret_cast<const uint4*>(h + (size_t)m * rowb + ch * 16))
+                       : make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
   const int j0 = blockIdx.y * 64 + warp * 8;
   for (int jj = 0; jj < 8; ++jj) {
     const int j = j0 + jj;
@@ -165,20 +272,23 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
       const int ch = lane + 32 * c;
-      wv[c] = ch < nch ? __ldg(reinterpret_cast<const uint4*>(urow + ch * 16)) : make_uint4(0, 0, 0, 0);
+      wv[c] = ch < nch ? ldg16_inflight(urow + ch * 16) : make_uint4(0, 0, 0, 0);
     }
+    // the h reads below may not move above this point: every load of the
+    // row is issued before the first product waits for one
+    asm volatile("" ::: "memory");
     float acc = 0.f;
 #pragma unroll
     for (int c = 0; c < CPL; ++c) {
-      const uint4 w = wv[c];
-      acc = __fmaf_rn(bf16lo(w.x), hr[c][0], acc);
-      acc = __fmaf_rn(bf16hi(w.x), hr[c][1], acc);
-      acc = __fmaf_rn(bf16lo(w.y), hr[c][2], acc);
-      acc = __fmaf_rn(bf16hi(w.y), hr[c][3], acc);
-      acc = __fmaf_rn(bf16lo(w.z), hr[c][4], acc);
-      acc = __fmaf_rn(bf16hi(w.z), hr[c][5], acc);
-      acc = __fmaf_rn(bf16lo(w.w), hr[c][6], acc);
-      acc = __fmaf_rn(bf16hi(w.w), hr[c][7], acc);
+      const uint4 w = wv[c], x = s_h[lane + 32 * c];
+      acc = fma_bf16_lo(w.x, x.x, acc);
+      acc = fma_bf16_hi(w.x, x.x, acc);
+      acc = fma_bf16_lo(w.y, x.y, acc);
+      acc = fma_bf16_hi(w.y, x.y, acc);
+      acc = fma_bf16_lo(w.z, x.z, acc);
+      acc = fma_bf16_hi(w.z, x.z, acc);
+      acc = fma_bf16_lo(w.w, x.w, acc);
+      acc = fma_bf16_hi(w.w, x.w, acc);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) acc = __fadd_rn(acc, __shfl_xor_sync(0xFFFFFFFFu, acc, o));
@@ -283,12 +393,27 @@ size_t topk_ws_bytes(int M, int V, int k) { return 0; }
 cudaError_t launch_topk(const float* scores, int M, int V, int k, int32_t* out_idx, void* ws,
                         cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
+  const int smem = kTopkCap * 8;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(k_topk), smem);
+  if (e != cudaSuccess) return e;
   ProfScope ps(kKTopk, st);
-  k_topk<<<M, 1024, 0, st>>>(scores, V, k, out_idx);
+  k_topk<<<M, kTopkThreads, smem, st>>>(scores, V, k, out_idx);
   return cudaGetLastError();
 }
 
+// The router runs on the tensor cores when the shape fits the tcgen05 kernel.
+static bool router_mma(int M, int d_prime, int V) { return mma_plan(d_prime, M, V).ok; }
+
 size_t specvocab_ws_bytes(int M, int d, int d_prime, int V, int k) {
+  if (router_mma(M, d_prime, V)) {
+    size_t s = 0;
+    s += align256((size_t)M * d_prime * 2);          // h' (bf16)
+    s += align256((size_t)M * V * sizeof(float));    // scores
+    s += align256(sizeof(unsigned));                 // the router's tile counter
+    s += align256((size_t)M * k * sizeof(int32_t));  // candidates
+    s += align256((size_t)M * k * sizeof(float));    // candidate logits
+    return s;
+  }
   const HeadPlan plan = head_plan(true, d_prime, M, V);
   if (!plan.ok) return 0;
   size_t s = 0;
@@ -309,10 +434,27 @@ cudaError_t launch_specvocab(const void* h, const void* w_down, const void* w_vo
                              int32_t* out_idx, float* out_prob, float* out_scores, void* ws,
                              cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  const HeadPlan plan = head_plan(true, d_prime, M, V);
   Carver cv(ws);
   void* hp = cv.take<uint8_t>((size_t)M * d_prime * 2);
   float* scores = cv.take<float>((size_t)M * V);
+  int32_t* cand = nullptr;
+  float* zc = nullptr;
+  cudaError_t e;
+  if (router_mma(M, d_prime, V)) {
+    // s = W_vocab h' as the tcgen05 kernel's fp32 scores
+    unsigned* ctr = cv.take<unsigned>(1);
+    cand = cv.take<int32_t>((size_t)M * k);
+    zc = cv.take<float>((size_t)M * k);
+    if (out_scores) scores = out_scores;
+    e = launch_down_proj(true, h, w_down, M, d, d_prime, true, hp, nullptr, ctr, 1, st);
+    if (e != cudaSuccess) return e;
+    const MmaPlan mp = mma_plan(d_prime, M, V);
+    const MmaWork none{nullptr, nullptr, nullptr};
+    const HeadOutputs no_out{nullptr, nullptr, nullptr, nullptr, nullptr};
+    e = launch_head_mma(mp, hp, w_vocab, M, d_prime, V, 0.f, none, no_out, scores, ctr, st);
+    if (e != cudaSuccess) return e;
+  } else {
+  const HeadPlan plan = head_plan(true, d_prime, M, V);
   HeadPartials part;
   part.pmax = cv.take<float>((size_t)M * plan.n_sub);
   part.psum = cv.take<float>((size_t)M * plan.n_sub);
@@ -322,17 +464,18 @@ cudaError_t launch_specvocab(const void* h, const void* w_down, const void* w_vo
   part.carg = cv.take<int>((size_t)M * plan.grid);
   part.ctr = cv.take<unsigned>((size_t)plan.n_launch);
   int32_t* router_arg = cv.take<int32_t>((size_t)M);
-  int32_t* cand = cv.take<int32_t>((size_t)M * k);
-  float* zc = cv.take<float>((size_t)M * k);
+  cand = cv.take<int32_t>((size_t)M * k);
+  zc = cv.take<float>((size_t)M * k);
   if (out_scores) scores = out_scores;
   const HeadOutputs router_out{nullptr, router_arg, nullptr, nullptr, nullptr};
 
-  cudaError_t e = launch_down_proj(true, h, w_down, M, d, d_prime, true, hp, nullptr, part.ctr,
-                                   plan.n_launch, st);
+  e = launch_down_proj(true, h, w_down, M, d, d_prime, true, hp, nullptr, part.ctr,
+                       plan.n_launch, st);
   if (e != cudaSuccess) return e;
   e = launch_head_stream(plan, true, w_vocab, hp, M, d_prime, V, 0.f, part, scores, router_out,
                          st);
   if (e != cudaSuccess) return e;
+  }
   e = launch_topk(scores, M, V, k, cand, nullptr, st);
   if (e != cudaSuccess) return e;
   const dim3 grid(M, (k + 63) / 64);

@@ -109,6 +109,16 @@ __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w &
 // c, d fp32, rounded once (fma.rn.f32.bf16, sm_100+).  A bf16 x bf16 product
 // is exact in fp32, so this equals fmaf on the widened operands; it saves the
 // widening instructions and issues at the scalar FFMA rate.
+// 16-byte read-only load that stays in program order with the other ones
+// (volatile): a run of them is issued back to back, all in flight together.
+__device__ __forceinline__ uint4 ldg16_inflight(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
 __device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
   float d;
   asm("{\n\t.reg .b16 al, ah, bl, bh;\n\t"
