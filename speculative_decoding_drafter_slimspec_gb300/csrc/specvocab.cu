@@ -56,10 +56,12 @@ constexpr int kTopkSample = 8192;  // sampled scores that estimate the threshold
 
 struct KeysFromScores {  // the row's scores, read from global memory
   const float* s;
+  __device__ bool live(int) const { return true; }
   __device__ uint32_t operator()(int i) const { return float_key(s[i]); }
 };
 struct KeysInShared {
   const uint32_t* k;
+  __device__ bool live(int) const { return true; }
   __device__ uint32_t operator()(int i) const { return k[i]; }
 };
 
@@ -81,6 +83,7 @@ __device__ void block_select_desc(const Keys& key_at, int n, int q, int* hist, i
     if (tid == 0) { s_sel[0] = 0; s_sel[1] = 0; }
     __syncthreads();
     for (int i = tid; i < n; i += kTopkThreads) {
+      if (!key_at.live(i)) continue;
       const uint32_t key = key_at(i);
       if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & (nb - 1)], 1);
     }
@@ -149,6 +152,51 @@ __device__ void block_compact(const Keys& key_at, const Ids& id_at, int n, uint3
     eq_seen += __popc(eqb);
   }
 }
+// The candidate buffer as 32 per-warp regions of kTopkRegion entries, region w
+// holding cnt[w] entries in id order.  Entry i of the buffer is live when
+// (i % kTopkRegion) < cnt[i / kTopkRegion].
+constexpr int kTopkRegion = kTopkCap / 32;
+struct KeysInRegions {
+  const uint32_t* k;
+  const int* cnt;
+  __device__ bool live(int i) const { return (i % kTopkRegion) < cnt[i / kTopkRegion]; }
+  __device__ uint32_t operator()(int i) const { return k[i]; }
+};
+
+// block_compact over the regions: warp w walks region w (its cnt[w] entries).
+template <class Ids>
+__device__ void region_compact(const uint32_t* keys, const Ids& id_at, const int* cnt, uint32_t thr,
+                               int need, int k, int* s_cnt, int32_t* out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lo = warp * kTopkRegion, hi = lo + cnt[warp];
+  const unsigned lt = (1u << lane) - 1u;
+  int gt = 0, eq = 0;
+  for (int v0 = lo; v0 < hi; v0 += 32) {
+    const int v = v0 + lane;
+    const uint32_t key = v < hi ? keys[v] : 0u;
+    gt += __popc(__ballot_sync(0xFFFFFFFFu, v < hi && key > thr));
+    eq += __popc(__ballot_sync(0xFFFFFFFFu, v < hi && key == thr));
+  }
+  if (lane == 0) { s_cnt[warp] = gt; s_cnt[32 + warp] = eq; }
+  __syncthreads();
+  int gt_pre = 0, eq_pre = 0;
+  for (int w = 0; w < warp; ++w) { gt_pre += s_cnt[w]; eq_pre += s_cnt[32 + w]; }
+  __syncthreads();
+  int pos = gt_pre + min(eq_pre, need), eq_seen = eq_pre;
+  for (int v0 = lo; v0 < hi; v0 += 32) {
+    const int v = v0 + lane;
+    const uint32_t key = v < hi ? keys[v] : 0u;
+    const bool is_gt = v < hi && key > thr, is_eq = v < hi && key == thr;
+    const unsigned eqb = __ballot_sync(0xFFFFFFFFu, is_eq);
+    const bool keep = is_gt || (is_eq && eq_seen + __popc(eqb & lt) < need);
+    const unsigned kb = __ballot_sync(0xFFFFFFFFu, keep);
+    const int my = pos + __popc(kb & lt);
+    if (keep && my < k) out[my] = id_at(v);
+    pos += __popc(kb);
+    eq_seen += __popc(eqb);
+  }
+}
+
 struct IdSelf {
   __device__ int32_t operator()(int i) const { return i; }
 };
@@ -185,9 +233,17 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float* __restrict__
   if (S == V) {
     for (int i = tid; i < S; i += kTopkThreads) c_key[i] = float_key(s[i]);
   } else {
-    const int nblk = S / 32;
-    for (int b = warp; b < nblk; b += kTopkThreads / 32)
-      c_key[b * 32 + lane] = float_key(s[(int)(((long long)b * (V - 32)) / (nblk - 1)) + lane]);
+    // kTopkSample / 32 = 256 blocks, 8 per warp, all loads in flight together
+    constexpr int kNblk = kTopkSample / 32, kPerWarp = kNblk / (kTopkThreads / 32);
+    float sv[kPerWarp];
+#pragma unroll
+    for (int j = 0; j < kPerWarp; ++j) {
+      const int b = warp + j * (kTopkThreads / 32);
+      sv[j] = s[(int)(((long long)b * (V - 32)) / (kNblk - 1)) + lane];
+    }
+#pragma unroll
+    for (int j = 0; j < kPerWarp; ++j)
+      c_key[(warp + j * (kTopkThreads / 32)) * 32 + lane] = float_key(sv[j]);
   }
   __syncthreads();
   int q = k;
@@ -196,43 +252,59 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float* __restrict__
   int unused;
   block_select_desc(KeysInShared{c_key}, S, q, hist, s_warp, s_sel, t_low, unused);
 
-  // 2. ordered filter of the row into the buffer (warp segments, coalesced)
+  // 2. (the sample's keys are no longer read: block_select_desc ended on a
+  //    barrier) one pass over the row: warp w walks a contiguous segment, 16 loads in
+  //    flight per lane, and appends the scores with key >= t, in id order, to
+  //    region w of the buffer (s_reg[w] entries; an overflow sends the row to
+  //    the full selection)
+  __shared__ int s_reg[32];
+  __shared__ int s_over;
+  if (tid == 0) s_over = 0;
   const int segw = ((V + 1023) / 1024) * 32;
   const int lo = min(V, warp * segw), hi = min(V, lo + segw);
   const unsigned lt = (1u << lane) - 1u;
   int cnt = 0;
-  for (int v0 = lo; v0 < hi; v0 += 32) {
-    const int v = v0 + lane;
-    cnt += __popc(__ballot_sync(0xFFFFFFFFu, v < hi && float_key(s[min(v, V - 1)]) >= t_low));
+  bool over = false;
+  constexpr int kDepth = 16;
+  for (int b0 = lo; b0 < hi; b0 += 32 * kDepth) {
+    float x[kDepth];
+#pragma unroll
+    for (int j = 0; j < kDepth; ++j) {
+      const int v = b0 + 32 * j + lane;
+      x[j] = v < hi ? s[v] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kDepth; ++j) {
+      const int v = b0 + 32 * j + lane;
+      const uint32_t key = float_key(x[j]);
+      const bool keep = v < hi && key >= t_low;
+      const unsigned kb = __ballot_sync(0xFFFFFFFFu, keep);
+      const int my = cnt + __popc(kb & lt);
+      if (keep && my < kTopkRegion) {
+        c_key[warp * kTopkRegion + my] = key;
+        c_id[warp * kTopkRegion + my] = v;
+      }
+      cnt += __popc(kb);
+    }
   }
-  if (lane == 0) hist[warp] = cnt;
+  over = cnt > kTopkRegion;
   __syncthreads();
-  int pre = 0, n_c = 0;
-  for (int w = 0; w < kTopkThreads / 32; ++w) {
-    if (w < warp) pre += hist[w];
-    n_c += hist[w];
+  if (lane == 0) {
+    s_reg[warp] = min(cnt, kTopkRegion);
+    if (over) s_over = 1;
+    hist[warp] = cnt;
   }
+  __syncthreads();
+  int n_c = 0;
+  for (int w = 0; w < kTopkThreads / 32; ++w) n_c += hist[w];
+  const bool ok = !s_over && n_c >= k;
   __syncthreads();
   uint32_t thr;
   int need;
-  if (n_c >= k && n_c <= kTopkCap) {
-    int pos = pre;
-    for (int v0 = lo; v0 < hi; v0 += 32) {
-      const int v = v0 + lane;
-      const uint32_t key = float_key(s[min(v, V - 1)]);
-      const bool keep = v < hi && key >= t_low;
-      const unsigned kb = __ballot_sync(0xFFFFFFFFu, keep);
-      if (keep) {
-        const int my = pos + __popc(kb & lt);
-        c_key[my] = key;
-        c_id[my] = v;
-      }
-      pos += __popc(kb);
-    }
-    __syncthreads();
+  if (ok) {
     // 3. exact selection among the candidates
-    block_select_desc(KeysInShared{c_key}, n_c, k, hist, s_warp, s_sel, thr, need);
-    block_compact(KeysInShared{c_key}, IdInShared{c_id}, n_c, thr, need, k, hist, out);
+    block_select_desc(KeysInRegions{c_key, s_reg}, kTopkCap, k, hist, s_warp, s_sel, thr, need);
+    region_compact(c_key, IdInShared{c_id}, s_reg, thr, need, k, hist, out);
   } else {
     block_select_desc(row_keys, V, k, hist, s_warp, s_sel, thr, need);
     block_compact(row_keys, IdSelf{}, V, thr, need, k, hist, out);
