@@ -75,6 +75,15 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
+// One box of a 4-D map (x, y, z, w) -- the wide stages' {64, 8, 4, 16} boxes.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z,
+                                            int w, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -141,13 +150,14 @@ __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled tile whose
-// 8-row groups are 1024 bytes apart (the layout TMA writes for a box of 64
-// bf16 x rows with SWIZZLE_128B).
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+// Shared-memory matrix descriptor of a K-major, 128-byte-swizzled tile: 8-row
+// groups (swizzle atoms of 8 x 128 bytes) `sbo` bytes apart -- 1024 for a box
+// of 64 bf16 x rows written by TMA with SWIZZLE_128B, 4096 inside a wide
+// stage where the four K blocks of each 8-row group sit side by side.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t sbo = 1024) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4)  // start address
          | ((uint64_t)1 << 16)                // leading byte offset (unused here)
-         | ((uint64_t)(1024 >> 4) << 32)      // stride byte offset: 8 rows x 128 B
+         | ((uint64_t)(sbo >> 4) << 32)       // stride byte offset between 8-row groups
          | ((uint64_t)1 << 46)                // descriptor version
          | ((uint64_t)2 << 61);               // 128-byte swizzle
 }
@@ -235,18 +245,26 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&v)[32], int vid0, int
 
 // ------------------------------------------------------------------ kernel --
 // MT: M tiles of 128 rows of z (1 or 2).  kMode 0: softmax partials; kMode 1:
-// the fp32 scores D[m, v] are written to out_scores (M x V).  tile_ctr is
-// zeroed by the down-projection that precedes this grid.
-template <bool kSample, int MT, int kMode>
+// the fp32 scores D[m, v] are written to out_scores (M x V).  kWide false: a
+// W_up stage is one K block, a 2-D box of 128 rows x 128 bytes.  kWide true:
+// a stage is KPS K blocks -- WB full ones as one 4-D box of 128 rows x WB*128
+// contiguous bytes (every row's bytes of the stage in one request run: fewer
+// DRAM page openings per byte), then, when r is not a multiple of 64, the
+// ragged last block as a 2-D box.  tile_ctr is zeroed by the down-projection
+// that precedes this grid.
+template <bool kSample, int MT, int kMode, bool kWide>
 __global__ void __launch_bounds__(kThreads, 1)
-    k_head_mma(const uint16_t* __restrict__ z, const __grid_constant__ CUtensorMap tm_w, int M,
-               int R, int V, int KB, int NST, float c, int n_tiles, MmaPart part,
-               float* __restrict__ out_scores, unsigned* __restrict__ tile_ctr, unsigned* err) {
+    k_head_mma(const uint16_t* __restrict__ z, const __grid_constant__ CUtensorMap tm_w,
+               const __grid_constant__ CUtensorMap tm_w2, int M, int R, int V, int KB, int KPS,
+               int WB, int NST, float c, int n_tiles, MmaPart part, float* __restrict__ out_scores,
+               unsigned* __restrict__ tile_ctr, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint8_t* sA = smem;                          // MT * KB compact blocks of z
   uint8_t* sB = smem + z_bytes(M, KB, MT);     // NST stages of W_up
+  const int kStageBytes = (kWide ? KPS : 1) * kBlockBytes;
+  const int SPT = kWide ? KB / KPS : KB;       // stages per vocabulary tile
   __shared__ uint64_t full[kMaxStages], empty[kMaxStages], a_full, acc_full[2], acc_empty[2];
   __shared__ uint64_t tile_full[kTileRing], tile_empty[kTileRing], mma_done;
   __shared__ int s_tile[kTileRing];    // vocabulary tile ids, -1 = no more
@@ -289,10 +307,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Lane 0 waits until the last stage of a group of G is free: the MMA
     // frees stages in order, so the earlier ones are free too, and with
     // G <= NST the parity of that slot's barrier names the round waited for.
-    if (lane == 0) tma_prefetch_desc(&tm_w);
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_w);
+      if (kWide && WB < KPS) tma_prefetch_desc(&tm_w2);
+    }
     // Waiting for the last of G stages leaves NST - G + 1 in flight when a
-    // group goes out: a short ring (a large z) issues in pairs.
-    const int G = NST >= 2 * kProdGroup ? kProdGroup : 2;
+    // group goes out: a short ring (a large z) issues in pairs, a ring of wide
+    // stages one at a time (one 64 KB box keeps ~80 B/clk under way).
+    const int G = kWide ? 1 : (NST >= 2 * kProdGroup ? kProdGroup : 2);
     int it = 0;
     bool ok = true;
     // Tiles b + k * grid (k < kStaticTiles) are this CTA's own (the first is
@@ -322,8 +344,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (t < 0) break;
-      for (int kb0 = 0; kb0 < KB && ok; kb0 += G) {
-        const int g = KB - kb0 < G ? KB - kb0 : G;
+      for (int st0 = 0; st0 < SPT && ok; st0 += G) {
+        const int g = SPT - st0 < G ? SPT - st0 : G;
         const int last = it + g - 1;
         if (lane == 0 && !mbar_wait_bounded(&empty[last % NST], ((last / NST) & 1) ^ 1, err)) {
           ok = false;
@@ -333,9 +355,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         if (lane < g) {
           const int s = (it + lane) % NST;
-          mbar_arrive_expect_tx(&full[s], (uint32_t)kBlockBytes);
-          tma_load_2d(sB + (size_t)s * kBlockBytes, &tm_w, (kb0 + lane) * 64, t * kTileN,
-                      &full[s]);
+          mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
+          uint8_t* dst = sB + (size_t)s * kStageBytes;
+          if (!kWide) {
+            tma_load_2d(dst, &tm_w, (st0 + lane) * 64, t * kTileN, &full[s]);
+          } else {
+            const int kb0 = (st0 + lane) * KPS;
+            if (WB > 0) tma_load_4d(dst, &tm_w, 0, 0, kb0, t * (kTileN / 8), &full[s]);
+            if (WB < KPS)  // the ragged last K block (columns past r read as zero)
+              tma_load_2d(dst + (size_t)WB * kBlockBytes, &tm_w2, (kb0 + WB) * 64, t * kTileN,
+                          &full[s]);
+          }
           atomicAdd(&s_fills[s], 1);
         }
         __syncwarp();
@@ -361,18 +391,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int buf = i & 1;
         if (!mbar_wait_bounded(&acc_empty[buf], ((i >> 1) & 1) ^ 1, err)) { ok = false; break; }
         tc_fence_after();
-        for (int kb = 0; kb < KB; ++kb, ++it) {
+        for (int sj = 0; sj < SPT; ++sj, ++it) {
           const int s = it % NST;
           if (!mbar_wait_bounded(&full[s], (it / NST) & 1, err)) { ok = false; break; }
           tc_fence_after();
-          const uint64_t bdesc = sw128_desc(smem_u32(sB + (size_t)s * kBlockBytes));
+          const int kps = kWide ? KPS : 1;
+          for (int kbi = 0; kbi < kps; ++kbi) {
+            const int kb = sj * kps + kbi;
+            uint8_t* stg = sB + (size_t)s * kStageBytes;
+            const uint64_t bdesc =
+                !kWide ? sw128_desc(smem_u32(stg))
+                : kbi < WB ? sw128_desc(smem_u32(stg + kbi * 1024), (uint32_t)WB * 1024u)
+                           : sw128_desc(smem_u32(stg + (size_t)WB * kBlockBytes));
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
+            for (int k4 = 0; k4 < 4; ++k4) {
 #pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              const uint64_t adesc = sw128_desc(smem_u32(sA + z_block_off(M, KB, mt, kb)));
-              mma_bf16(tmem + (uint32_t)((buf * MT + mt) * kTileN), adesc + 2 * k4,
-                       bdesc + 2 * k4, kIdesc, (kb | k4) != 0 ? 1u : 0u);
+              for (int mt = 0; mt < MT; ++mt) {
+                const uint64_t adesc = sw128_desc(smem_u32(sA + z_block_off(M, KB, mt, kb)));
+                mma_bf16(tmem + (uint32_t)((buf * MT + mt) * kTileN), adesc + 2 * k4,
+                         bdesc + 2 * k4, kIdesc, (kb | k4) != 0 ? 1u : 0u);
+              }
             }
           }
           mma_commit(&empty[s]);  // the stage is free once these MMAs complete
@@ -739,6 +777,23 @@ bool make_map(CUtensorMap* map, const void* base, int rows, int cols) {
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+
+// The same bf16 tensor [rows x cols] seen as 4-D (64 columns, 8 rows, the
+// cols/64 full K blocks, rows/8 row groups) for the wide stages: a box
+// {64, 8, wb, 16} is 128 rows x wb K blocks, landing as 16 groups x wb K blocks
+// x 8 rows x 128 B.  Needs rows % 8 == 0 (every element of an in-range group
+// exists); groups past the end read as zero.
+bool make_map_wide(CUtensorMap* map, const void* base, int rows, int cols, int wb) {
+  EncodeTiledFn enc = encoder();
+  if (!enc || rows % 8 != 0 || wb < 1 || wb > cols / 64) return false;
+  const cuuint64_t dims[4] = {64, 8, (cuuint64_t)(cols / 64), (cuuint64_t)(rows / 8)};
+  const cuuint64_t strides[3] = {(cuuint64_t)cols * 2, 128, (cuuint64_t)cols * 16};
+  const cuuint32_t box[4] = {64, 8, (cuuint32_t)wb, (cuuint32_t)(kTileN / 8)};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 }  // namespace
 
 MmaPlan mma_plan(int r, int M, int V) {
@@ -749,9 +804,25 @@ MmaPlan mma_plan(int r, int M, int V) {
   p.kb = (r + 63) / 64;
   const int a_bytes = z_bytes(M, p.kb, p.mt);
   const int room = kSmemCap - 1024 - a_bytes;
-  p.nst = std::min(kMaxStages, room / kBlockBytes);
-  if (p.nst < 3) return p;
-  p.smem = 1024 + a_bytes + p.nst * kBlockBytes;
+  // wide stages (several K blocks per request run of each row) when the 4-D
+  // view is exact (V % 8 == 0) and z leaves room for two of them: 4 K blocks
+  // when r is a multiple of 256, else a whole tile of up to 6 K blocks (the
+  // full ones by 4-D box, a ragged last one by 2-D box)
+  p.kps = 1;
+  p.wb = 0;
+  if (p.mt == 1 && V % 8 == 0) {  // (with two M tiles z leaves no room for them)
+    if (r % 256 == 0 && room / (4 * kBlockBytes) >= 2) {
+      p.kps = 4;
+      p.wb = 4;
+    } else if (p.kb <= 6 && r >= 64 && room / (p.kb * kBlockBytes) >= 2) {
+      p.kps = p.kb;
+      p.wb = r / 64;
+    }
+  }
+  const int stage = p.kps * kBlockBytes;
+  p.nst = std::min(p.kps > 1 ? 4 : kMaxStages, room / stage);
+  if (p.nst < (p.kps > 1 ? 2 : 3)) return p;
+  p.smem = 1024 + a_bytes + p.nst * stage;
   p.n_tiles = (V + kTileN - 1) / kTileN;
   p.grid = std::max(1, std::min(sm_count(), p.n_tiles));
   p.n_sub = 2 * p.n_tiles;
@@ -760,11 +831,12 @@ MmaPlan mma_plan(int r, int M, int V) {
   return p;
 }
 
-template <bool kSample, int MT, int kMode>
-static cudaError_t launch_mma_one(const MmaPlan& p, const void* z, const CUtensorMap& tw, int M,
-                                  int r, int V, float c, const MmaPart& part, float* scores,
-                                  unsigned* ctr, cudaStream_t st) {
-  auto kern = k_head_mma<kSample, MT, kMode>;
+template <bool kSample, int MT, int kMode, bool kWide>
+static cudaError_t launch_mma_kps(const MmaPlan& p, const void* z, const CUtensorMap& tw,
+                                  const CUtensorMap& tw2, int M, int r, int V, float c,
+                                  const MmaPart& part, float* scores, unsigned* ctr,
+                                  cudaStream_t st) {
+  auto kern = k_head_mma<kSample, MT, kMode, kWide>;
   // the limit is set once per kernel: make it the largest size any plan asks for
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), kSmemCap);
   if (e != cudaSuccess) return e;
@@ -779,32 +851,52 @@ static cudaError_t launch_mma_one(const MmaPlan& p, const void* z, const CUtenso
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   ProfScope ps(kKHeadMma, st);
-  return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint16_t*>(z), tw, M, r, V, p.kb,
-                            p.nst, c, p.n_tiles, part, scores, ctr, error_word());
+  return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint16_t*>(z), tw, tw2, M, r, V,
+                            p.kb, p.kps, p.wb, p.nst, c, p.n_tiles, part, scores, ctr,
+                            error_word());
+}
+// Wide stages only with one M tile (z of up to 128 rows leaves room for them).
+template <bool kSample, int MT, int kMode>
+static cudaError_t launch_mma_one(const MmaPlan& p, const void* z, const CUtensorMap& tw,
+                                  const CUtensorMap& tw2, int M, int r, int V, float c,
+                                  const MmaPart& part, float* scores, unsigned* ctr,
+                                  cudaStream_t st) {
+  if (MT == 1 && p.kps > 1)  // the plan picks wide stages only with one M tile
+    return launch_mma_kps<kSample, 1, kMode, true>(p, z, tw, tw2, M, r, V, c, part, scores, ctr,
+                                                    st);
+  return launch_mma_kps<kSample, MT, kMode, false>(p, z, tw, tw2, M, r, V, c, part, scores, ctr,
+                                                    st);
 }
 
 cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up, int M, int r,
                             int V, float temperature, const MmaWork& w, const HeadOutputs& out,
                             float* scores, unsigned* ctr, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  CUtensorMap tw;
-  if (!make_map(&tw, w_up, V, r)) return cudaErrorInvalidValue;
+  // tw: the stages' map (2-D, or 4-D for wide stages); tw2: the 2-D map, for
+  // a wide stage's ragged last K block
+  CUtensorMap tw, tw2;
+  if (!make_map(&tw2, w_up, V, r)) return cudaErrorInvalidValue;
+  if (p.kps > 1 && p.wb > 0) {
+    if (!make_map_wide(&tw, w_up, V, r, p.wb)) return cudaErrorInvalidValue;
+  } else {
+    tw = tw2;
+  }
   const bool sample = temperature > 0.f && scores == nullptr;
   const double inv = sample ? 1.0 / (double)temperature : 0.0;
   const float c = (float)(1.4426950408889634 * inv), inv_t = (float)inv;
   const MmaPart part{w.pmax, w.psum, w.parg};
   cudaError_t e;
   if (scores != nullptr) {
-    e = p.mt == 1 ? launch_mma_one<false, 1, 1>(p, z_ws, tw, M, r, V, c, part, scores, ctr, st)
-                  : launch_mma_one<false, 2, 1>(p, z_ws, tw, M, r, V, c, part, scores, ctr, st);
+    e = p.mt == 1 ? launch_mma_one<false, 1, 1>(p, z_ws, tw, tw2, M, r, V, c, part, scores, ctr, st)
+                  : launch_mma_one<false, 2, 1>(p, z_ws, tw, tw2, M, r, V, c, part, scores, ctr, st);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   if (sample)
-    e = p.mt == 1 ? launch_mma_one<true, 1, 0>(p, z_ws, tw, M, r, V, c, part, nullptr, ctr, st)
-                  : launch_mma_one<true, 2, 0>(p, z_ws, tw, M, r, V, c, part, nullptr, ctr, st);
+    e = p.mt == 1 ? launch_mma_one<true, 1, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st)
+                  : launch_mma_one<true, 2, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st);
   else
-    e = p.mt == 1 ? launch_mma_one<false, 1, 0>(p, z_ws, tw, M, r, V, c, part, nullptr, ctr, st)
-                  : launch_mma_one<false, 2, 0>(p, z_ws, tw, M, r, V, c, part, nullptr, ctr, st);
+    e = p.mt == 1 ? launch_mma_one<false, 1, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st)
+                  : launch_mma_one<false, 2, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st);
   if (e != cudaSuccess) return e;
   // the per-row finish, launched to overlap the tail of the MMA grid
   cudaLaunchConfig_t cfg = {};

@@ -102,6 +102,8 @@ cudaError_t launch_head_stream(const HeadPlan& plan, bool bf16, const void* w_up
 struct MmaPlan {
   int mt;       // 128-row tiles of z (1 or 2)
   int kb;       // 64-wide K blocks of r
+  int kps;      // K blocks per W_up stage (1 for 2-D boxes; more for wide stages)
+  int wb;       // of those, full K blocks loaded by one 4-D box (wide stages)
   int nst;      // W_up stages in shared memory
   int smem;     // dynamic shared memory bytes
   int n_tiles;  // 128-row vocabulary tiles

@@ -91,6 +91,8 @@ SMALL = [
     (20, 3, 64, 32, 31, "bf16"),      # V smaller than one tile
     (21, 130, 256, 128, 1100, "bf16"),# two 128-row tiles of z, the second with 2 rows
     (22, 40, 512, 200, 777, "bf16"),  # 5 swizzle atoms of z, last K block 8 wide
+    (23, 8, 512, 512, 4096, "bf16"),  # wide stages: 4-D boxes of 4 K blocks, 32 tiles
+    (24, 3, 256, 256, 1000, "bf16"),  # wide stages, last tile 104 rows (groups past V read 0)
 ]
 
 
