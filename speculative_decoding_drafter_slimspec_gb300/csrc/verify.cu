@@ -75,10 +75,37 @@ __global__ void __launch_bounds__(256)
         const int q = q0 + lane + 32 * k;
         if (q < q1) a[k] = __ldcs(p4 + q);
       }
+      if (!kSample) {
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        const int q = q0 + lane + 32 * k;
-        if (q < q1) push4<kSample>(s, a[k], q * 4, c);
+        for (int k = 0; k < 16; ++k) {
+          const int q = q0 + lane + 32 * k;
+          if (q < q1) push4<false>(s, a[k], q * 4, c);
+        }
+      } else {
+        // sampling needs no argmax: the lane's maximum, then one pass of
+        // 2^(x c - max c) in four fixed-order partial sums
+        float m = kNegInf;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int q = q0 + lane + 32 * k;
+          if (q < q1) m = fmaxf(m, fmaxf(fmaxf(a[k].x, a[k].y), fmaxf(a[k].z, a[k].w)));
+        }
+        if (m != kNegInf) {
+          const float off = -m * c;
+          float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const int q = q0 + lane + 32 * k;
+            if (q < q1) {
+              s0 = __fadd_rn(s0, fast_exp2(__fmaf_rn(a[k].x, c, off)));
+              s1 = __fadd_rn(s1, fast_exp2(__fmaf_rn(a[k].y, c, off)));
+              s2 = __fadd_rn(s2, fast_exp2(__fmaf_rn(a[k].z, c, off)));
+              s3 = __fadd_rn(s3, fast_exp2(__fmaf_rn(a[k].w, c, off)));
+            }
+          }
+          s.mx = m;
+          s.sum = __fadd_rn(__fadd_rn(s0, s1), __fadd_rn(s2, s3));
+        }
       }
     } else {
       for (int i = lo + lane; i < hi; i += 32) row_state_push<kSample>(s, __ldcs(src + i), i, c);
