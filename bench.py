@@ -244,14 +244,25 @@ def head_stream_bytes(x) -> float:
     return V * r * 2 + M * r * 2
 
 
-def kernel_bytes(x, union_rows: float) -> dict:
+def verify_rows_read(x, num_accepted) -> int:
+    """Rows the accept chain needs (its algorithmic bytes): the target rows of
+    positions 0..n_b of each sequence (n_b accepted), and when sampling the
+    draft rows of the drafted positions among them.  The row pass reads at
+    least these; its roofline is taken against them."""
+    n = num_accepted.to("cpu").long()
+    rows = int((n + 1).sum())
+    if x["T"] > 0:
+        rows += int((n + 1).clamp(max=x["gamma"]).sum())
+    return rows
+
+
+def kernel_bytes(x, union_rows: float, ver_rows: int) -> dict:
     """Algorithmic bytes of one launch of each hot kernel (what the step must
     move at least once; partials and workspaces are overhead)."""
-    M, d, r, V, B, gamma = x["M"], x["d"], x["r"], x["V"], x["B"], x["gamma"]
-    rows = B * (gamma + 1) + (B * gamma if x["T"] > 0 else 0)
+    M, d, r, V = x["M"], x["d"], x["r"], x["V"]
     out = {"k_head_mma": head_stream_bytes(x), "k_head_stream": head_stream_bytes(x),
            "k_down_proj": r * d * 2 + M * d * 2 + M * r * 2,
-           "k_verify_rows": rows * V * 4}
+           "k_verify_rows": ver_rows * V * 4}
     if x["u_full"] is not None:
         out["k_gather_logits"] = union_rows * d * 2 + M * d * 2
         out["k_topk"] = M * V * 4
@@ -481,6 +492,7 @@ def run_ours(args, world, rank, local):
     with torch.cuda.stream(stream):
         union_rows = specvocab_union_rows(x, rnd, ss)
     stream.synchronize()
+    ver_rows = verify_rows_read(x, rnd.ver_out["num_accepted"])
 
     graph = torch.cuda.CUDAGraph()
     n0 = ss.launch_count()
@@ -547,7 +559,11 @@ def run_ours(args, world, rank, local):
     # the dominant kernel (largest share of the step among the kernels with
     # algorithmic bytes), the head's up-projection, and the verifier's row pass
     peak, peak_kind = measured_peaks()
-    kb = kernel_bytes(x, union_rows)
+    kb = kernel_bytes(x, union_rows, ver_rows)
+    if "k_verify_rows" in prof:
+        # the row pass may be split in two launches (position 0, then the
+        # positions of the sequences that kept it): the bytes are per step
+        kb["k_verify_rows"] /= prof["k_verify_rows"][0] / n_prof
     cands = [k for k in prof if k in kb]
     roof = head_roof = ver_roof = None
     if cands:
@@ -568,6 +584,10 @@ def run_ours(args, world, rank, local):
     if "k_verify_rows" in prof:
         ver_roof = roofline_for("k_verify_rows", prof, kb["k_verify_rows"], peak, peak_kind,
                                 args.workload)
+        ver_roof["launches_per_step"] = prof["k_verify_rows"][0] / n_prof
+        ver_roof["rows_needed"] = ver_rows
+        ver_roof["rows_total"] = x["B"] * (x["gamma"] + 1) + (
+            x["B"] * x["gamma"] if x["T"] > 0 else 0)
     ver_ms = sum(ms for name, (n, ms) in prof.items() if name.startswith("k_verify")) / n_prof
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1000.0 / args.steps,

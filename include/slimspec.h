@@ -177,9 +177,14 @@ int ss_topk_rows(const float* scores, int M, int V, int k, int32_t* out_idx,
  *  draft_logits  B x gamma x V float32 (may be NULL when T == 0)
  *  draft_tokens  B x gamma int32, each in [0, V) (checked on the device)
  *  uniforms      B x (gamma+1) floats in [0,1) (T > 0), else may be NULL
- *  1 <= gamma <= 32, 1 <= V <= 524288, B >= 0
+ *  1 <= gamma <= 32, 1 <= V <= 524288, B >= 0; SS_ERR_UNSUPPORTED when
+ *    B*(gamma+1)*V >= 2^40 or B*(2*gamma+1)*ceil(V/2048) >= 2^31
  *  out_tokens    B x (gamma+1) int32: the n+1 emitted tokens, then -1
  *  out_num_accepted B int32: n
+ * A position's decision needs only its own rows, so rows of positions after
+ * a sequence's first rejection are not read once that rejection is known
+ * (rows already in flight are still reduced; the results do not depend on
+ * it).  The workspace's contents need no initialisation.
  * ------------------------------------------------------------------------ */
 size_t spec_verify_workspace_size(int B, int gamma, int V, float temperature);
 

@@ -261,7 +261,7 @@ def spec_verify(target_logits, draft_logits, draft_tokens, temperature=0.0, unif
     return o
 
 
-N_KERNEL_KINDS = 11
+N_KERNEL_KINDS = 12
 
 
 def launch_count() -> int:

@@ -236,6 +236,9 @@ int spec_verify(const float* target_logits, const float* draft_logits, const int
     return SS_ERR_INVALID_ARG;
   if ((long long)B * (gamma + 1) * V >= (1LL << 40)) return SS_ERR_UNSUPPORTED;
   if (V > 524288) return SS_ERR_UNSUPPORTED;  // the final draw scans at most 256 chunks
+  // the row pass numbers its (row, 2048-float chunk) units in 32 bits
+  if ((long long)B * (2 * gamma + 1) * ((V + 2047) / 2048) >= (1LL << 31))
+    return SS_ERR_UNSUPPORTED;
   if (B == 0) return SS_OK;
   const bool sample = temperature > 0.f;
   if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SS_ERR_INVALID_ARG;

@@ -17,7 +17,7 @@ unsigned* error_word();
 // Kernel kinds known to the optional profiler (profile.cu).
 enum KernelKind {
   kKDownProj = 0, kKHeadStream, kKHeadFinish, kKVerifyRows, kKVerifyDecide, kKVerifyResid,
-  kKVerifyFinish, kKTopk, kKGather, kKCandFinish, kKHeadMma, kKindCount
+  kKVerifyFinish, kKTopk, kKGather, kKCandFinish, kKHeadMma, kKVerifyFirst, kKindCount
 };
 
 // Counts one launch and, while profiling is on, brackets it with two events

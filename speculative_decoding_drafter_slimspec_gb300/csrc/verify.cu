@@ -1,13 +1,18 @@
 // verify.cu -- speculative verification on sm_103a.
 //
 // Explainer (大模型批改 5 个词…), sections "小模型起草，大模型批改" and "为什么答案不会变",
-// and SpecTr-GBV article, 第三步.  The verifier reads every target row
-// (B x (gamma+1) x V fp32) and, when sampling, every draft row (B x gamma x V):
-// it is an HBM streaming reduction.
+// and SpecTr-GBV article, 第三步.  The verifier reads target rows (fp32, V
+// wide) and, when sampling, draft rows: an HBM streaming reduction.  A
+// position's decision needs only its own rows, and no row after a sequence's
+// first rejection is used, so for large inputs position 0 is decided first
+// and the other positions are read only for sequences that kept it.
 //
-//   k_verify_rows    one warp per (row, 4096-float chunk): 16-byte streaming
-//                    loads, online (max, sum of exp at T, argmax) -> partials
-//   k_verify_decide  one warp per sequence: merges the partials of its rows,
+//   k_verify_rows    one warp per (row, 2048-float chunk) of the rows of a
+//                    range of positions: 16-byte streaming loads, online
+//                    (max, sum of exp at T, argmax) -> partials
+//   k_verify_first   one warp per sequence: position 0's accept test, between
+//                    a pass over the position-0 rows and one over the rest
+//   k_verify_decide  one CTA per sequence: merges the partials of its rows,
 //                    greedy prefix match or the min(1, p/q) accept tests
 //   k_verify_resid   one warp per (sequence, chunk) of the final draw's row:
 //                    chunk masses of max(0, p_n - q_n) (bonus: of p_gamma,
@@ -50,20 +55,36 @@ __device__ __forceinline__ void push4(RowState& s, const float4 a, int v0, float
 }
 
 // ------------------------------------------------------------------- K8 ----
+// One warp per (row, kVChunk-float chunk) unit over the rows of positions
+// j0..j1 of every sequence: its target rows, then (sampling) its draft rows
+// of drafted positions.  With seq_ok given, the units of sequences whose
+// seq_ok entry is 0 are skipped (their first rejection is before j0).
 template <bool kSample>
 __global__ void __launch_bounds__(256)
-    k_verify_rows(const float* __restrict__ target, const float* __restrict__ draft,
-                  int n_target_rows, int n_rows, int V, float c, int n_chunks,
-                  float* __restrict__ vmax, float* __restrict__ vsum, int* __restrict__ varg) {
+    k_verify_rows(const float* __restrict__ target, const float* __restrict__ draft, int B,
+                  int gamma, int V, float c, int n_chunks, int j0, int j1,
+                  const int* __restrict__ seq_ok, float* __restrict__ vmax,
+                  float* __restrict__ vsum, int* __restrict__ varg) {
+  pdl_launch_dependents();
+  pdl_wait_producer();
   const int lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int nw = gridDim.x * (blockDim.x >> 5);
+  const unsigned gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const unsigned nw = gridDim.x * (blockDim.x >> 5);
   const bool vec = (V & 3) == 0;
-  const long long units = (long long)n_rows * n_chunks;
-  for (long long u = gw; u < units; u += nw) {
-    const int row = (int)(u / n_chunks), ch = (int)(u % n_chunks);
-    const float* src = row < n_target_rows ? target + (size_t)row * V
-                                           : draft + (size_t)(row - n_target_rows) * V;
+  const int g1 = gamma + 1;
+  const int nt = j1 - j0 + 1;                                    // target rows per sequence
+  const int nd = kSample ? max(0, min(j1, gamma - 1) - j0 + 1) : 0;  // draft rows
+  const unsigned seq_units = (unsigned)(nt + nd) * (unsigned)n_chunks;
+  const unsigned units = (unsigned)B * seq_units;  // < 2^31: checked by the host
+  for (unsigned u = gw; u < units; u += nw) {
+    const int b = (int)(u / seq_units);
+    if (seq_ok != nullptr && __ldg(seq_ok + b) == 0) continue;  // warp-uniform
+    const unsigned rem = u - (unsigned)b * seq_units;
+    const int ri = (int)(rem / (unsigned)n_chunks);
+    const int ch = (int)(rem - (unsigned)ri * (unsigned)n_chunks);
+    const int row = ri < nt ? b * g1 + j0 + ri : B * g1 + b * gamma + j0 + (ri - nt);
+    const float* src = ri < nt ? target + (size_t)row * V
+                               : draft + ((size_t)b * gamma + j0 + (ri - nt)) * V;
     const int lo = ch * kVChunk, hi = min(V, lo + kVChunk);
     RowState s = row_state_empty();
     if (vec) {
@@ -111,7 +132,7 @@ __global__ void __launch_bounds__(256)
       for (int i = lo + lane; i < hi; i += 32) row_state_push<kSample>(s, __ldcs(src + i), i, c);
     }
 #pragma unroll
-    for (int b = 0; b < 5; ++b) s = shfl_merge<kSample>(s, 1 << b, c);
+    for (int bit = 0; bit < 5; ++bit) s = shfl_merge<kSample>(s, 1 << bit, c);
     if (lane == 0) {
       const size_t o = (size_t)row * n_chunks + ch;
       vmax[o] = s.mx;
@@ -149,28 +170,117 @@ __device__ __forceinline__ RowState warp_row_state(int row, int n_chunks, const 
   return s;
 }
 
+// What the accept test of drafted position j of sequence b reads besides
+// the row states: the drafted token, its target and draft logits and the
+// uniform (loaded apart from, and in parallel with, the partial merges).
+struct PosInputs {
+  int x;
+  float lp, lq, u;
+};
+template <bool kSample>
+__device__ __forceinline__ PosInputs load_position(const float* __restrict__ target,
+                                                   const float* __restrict__ draft,
+                                                   const int32_t* __restrict__ tokens,
+                                                   const float* __restrict__ uniforms, int b,
+                                                   int j, int gamma, int V) {
+  const int g1 = gamma + 1;
+  PosInputs in{tokens[(size_t)b * gamma + j], 0.f, 0.f, 0.f};
+  if (kSample) {
+    in.u = uniforms[(size_t)b * g1 + j];
+    if (in.x >= 0 && in.x < V) {
+      in.lp = target[((size_t)b * g1 + j) * V + in.x];
+      in.lq = draft[((size_t)b * gamma + j) * V + in.x];
+    }
+  }
+  return in;
+}
+
+// Accept test of a drafted position from its merged target row state
+// (pmx, psum, parg) and, when sampling, draft row state (qmx, qsum): greedy
+// keeps the token iff it is the target argmax; sampling keeps it iff
+// u * q(x) < p(x).  An out-of-range token rejects.
+template <bool kSample>
+__device__ __forceinline__ bool position_accepts(const PosInputs& in, int V, float c, float pmx,
+                                                 float psum, int parg, float qmx, float qsum) {
+  if (in.x < 0 || in.x >= V) return false;
+  if (!kSample) return in.x == parg;
+  const float px = __fdiv_rn(fast_exp2((in.lp - pmx) * c), psum);
+  const float qx = __fdiv_rn(fast_exp2((in.lq - qmx) * c), qsum);
+  return in.u * qx < px;
+}
+
+// ---------------------------------------------------------------- K8b ----
+// Position 0 of every sequence, decided between the two row passes: one CTA
+// per sequence, warp 0 merging the partials of the target row, warp 1 those
+// of the draft row (sampling) and warp 2 loading the token-side inputs;
+// seq_ok[b] = 1 iff the drafted token is kept (the later positions are read
+// only for those sequences).
+template <bool kSample>
+__global__ void __launch_bounds__(96)
+    k_verify_first(const float* __restrict__ target, const float* __restrict__ draft,
+                   const int32_t* __restrict__ tokens, int B, int gamma, int V, float c,
+                   int n_chunks, const float* __restrict__ vmax, const float* __restrict__ vsum,
+                   const int* __restrict__ varg, const float* __restrict__ uniforms,
+                   int* __restrict__ seq_ok) {
+  __shared__ RowState s_st[2];
+  __shared__ PosInputs s_in;
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int b = blockIdx.x;
+  if (warp == 2) {  // inputs that do not depend on the row pass
+    if (lane == 0) s_in = load_position<kSample>(target, draft, tokens, uniforms, b, 0, gamma, V);
+  }
+  pdl_wait_producer();
+  if (warp == 0 || (kSample && warp == 1)) {
+    const int row = warp == 0 ? b * (gamma + 1) : B * (gamma + 1) + b * gamma;
+    const RowState st = warp_row_state<kSample>(row, n_chunks, vmax, vsum, varg, c, lane);
+    if (lane == 0) s_st[warp] = st;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const RowState pt = s_st[0];
+    const RowState pq = kSample ? s_st[1] : row_state_empty();
+    seq_ok[b] = position_accepts<kSample>(s_in, V, c, pt.mx, pt.sum, pt.arg, pq.mx, pq.sum) ? 1
+                                                                                            : 0;
+  }
+}
+
 // ------------------------------------------------------------------- K9 ----
-// One CTA per sequence.  Its warps merge the chunk partials of the sequence's
-// gamma+1 target rows (and gamma draft rows) in parallel; lane j of warp 0
-// then takes position j's decision, and the first failing position is found
-// with a ballot.
+// One CTA per sequence.  All warps but the last merge the chunk partials of
+// the sequence's gamma+1 target rows (and gamma draft rows) in parallel; the
+// last warp loads each position's token-side inputs meanwhile.  Lane j of
+// warp 0 then takes position j's decision, and the first failing position is
+// found with a ballot.  With seq_ok given, position 0 was decided between
+// the row passes (the same test on the same partials) and rows after a
+// rejection there were not read.
 constexpr int kMaxGamma = 32;
 template <bool kSample>
-__global__ void __launch_bounds__(512)
+__global__ void __launch_bounds__(544)
     k_verify_decide(const float* __restrict__ target, const float* __restrict__ draft,
                     const int32_t* __restrict__ tokens, int B, int gamma, int V, float c,
                     int n_chunks, const float* __restrict__ vmax, const float* __restrict__ vsum,
                     const int* __restrict__ varg, const float* __restrict__ uniforms,
-                    int32_t* __restrict__ out_tokens, int32_t* __restrict__ out_nacc,
-                    VerifyInfo* __restrict__ info, unsigned* err) {
+                    const int* __restrict__ seq_ok, int32_t* __restrict__ out_tokens,
+                    int32_t* __restrict__ out_nacc, VerifyInfo* __restrict__ info,
+                    unsigned* err) {
   __shared__ float s_mx[2 * kMaxGamma + 1], s_sum[2 * kMaxGamma + 1];
   __shared__ int s_arg[2 * kMaxGamma + 1];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __shared__ PosInputs s_in[kMaxGamma];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int n_merge = (blockDim.x >> 5) - 1;  // merging warps; the last one loads
   const int b = blockIdx.x;
   const int g1 = gamma + 1;
   const int n_target_rows = B * g1;
   const int rows = kSample ? g1 + gamma : g1;
-  for (int i = warp; i < rows; i += nw) {
+  if (warp == n_merge) {
+    if (lane < gamma) {
+      const PosInputs in = load_position<kSample>(target, draft, tokens, uniforms, b, lane, gamma, V);
+      if (in.x < 0 || in.x >= V) raise_error(err, kErrIndex);
+      s_in[lane] = in;
+    }
+  }
+  pdl_wait_producer();
+  for (int i = warp; i < rows && warp < n_merge; i += n_merge) {
     const int row = i < g1 ? b * g1 + i : n_target_rows + b * gamma + (i - g1);
     const RowState st = warp_row_state<kSample>(row, n_chunks, vmax, vsum, varg, c, lane);
     if (lane == 0) { s_mx[i] = st.mx; s_sum[i] = st.sum; s_arg[i] = st.arg; }
@@ -179,22 +289,13 @@ __global__ void __launch_bounds__(512)
   if (warp != 0) return;
   // lane j < gamma: the decision at drafted position j
   bool ok = true;
-  int x = 0;
   if (lane < gamma) {
-    x = tokens[(size_t)b * gamma + lane];
-    const bool bad = (x < 0 || x >= V);
-    if (bad) raise_error(err, kErrIndex);
-    if (bad) {
-      ok = false;
-    } else if (!kSample) {
-      ok = (x == s_arg[lane]);
-    } else {
-      const float lp = target[((size_t)b * g1 + lane) * V + x];
-      const float lq = draft[((size_t)b * gamma + lane) * V + x];
-      const float px = __fdiv_rn(fast_exp2((lp - s_mx[lane]) * c), s_sum[lane]);
-      const float qx = __fdiv_rn(fast_exp2((lq - s_mx[g1 + lane]) * c), s_sum[g1 + lane]);
-      ok = uniforms[(size_t)b * g1 + lane] * qx < px;
-    }
+    if (lane == 0 && seq_ok != nullptr)
+      ok = seq_ok[b] != 0;
+    else
+      ok = position_accepts<kSample>(s_in[lane], V, c, s_mx[lane], s_sum[lane], s_arg[lane],
+                                     kSample ? s_mx[g1 + lane] : 0.f,
+                                     kSample ? s_sum[g1 + lane] : 1.f);
   }
   const unsigned fail = __ballot_sync(0xFFFFFFFFu, lane < gamma && !ok);
   const int n = fail ? __ffs(fail) - 1 : gamma;
@@ -408,8 +509,30 @@ size_t verify_ws_bytes(int B, int gamma, int V, bool sample) {
   s += align256(rows * n_chunks * sizeof(int));         // varg
   s += align256((size_t)B * sizeof(VerifyInfo));        // info
   s += align256((size_t)B * n_chunks * sizeof(float));  // rmass
+  s += align256((size_t)B * sizeof(int));               // seq_ok
   return s;
 }
+
+namespace {
+// Rows of fp32 logits above which position 0 is decided before the other
+// positions are read (below it the extra launch costs more than the rows of
+// sequences rejected at position 0).
+constexpr double kSplitBytes = 64.0 * 1024 * 1024;
+
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, int grid, int block, cudaStream_t st, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3((unsigned)block);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+}  // namespace
 
 cudaError_t launch_verify(const float* target, const float* draft, const int32_t* tokens, int B,
                           int gamma, int V, float temperature, const float* uniforms,
@@ -427,35 +550,66 @@ cudaError_t launch_verify(const float* target, const float* draft, const int32_t
   int* varg = cv.take<int>((size_t)n_rows * n_chunks);
   VerifyInfo* info = cv.take<VerifyInfo>(B);
   float* rmass = cv.take<float>((size_t)B * n_chunks);
+  int* seq_ok = cv.take<int>(B);
+  const bool split = (double)n_rows * V * 4.0 >= kSplitBytes;
 
   // one warp per unit; the grid is what fits on the GPU at once (one wave)
-  const long long units = (long long)n_rows * n_chunks;
-  {
   constexpr int kThr = 256;
-  const void* kern = sample ? reinterpret_cast<const void*>(k_verify_rows<true>)
-                            : reinterpret_cast<const void*>(k_verify_rows<false>);
-  const long long cap = (long long)resident_blocks(kern, kThr, 0) * sm_count();
-  const int grid = (int)std::max<long long>(1, std::min<long long>((units + 7) / 8, cap));
-  ProfScope ps(kKVerifyRows, st);
-  if (sample)
-    k_verify_rows<true><<<grid, kThr, 0, st>>>(target, draft, n_target_rows, n_rows, V, c,
-                                               n_chunks, vmax, vsum, varg);
-  else
-    k_verify_rows<false><<<grid, kThr, 0, st>>>(target, draft, n_target_rows, n_rows, V, c,
-                                                n_chunks, vmax, vsum, varg);
+  const void* rows_kern = sample ? reinterpret_cast<const void*>(k_verify_rows<true>)
+                                 : reinterpret_cast<const void*>(k_verify_rows<false>);
+  const long long cap = (long long)resident_blocks(rows_kern, kThr, 0) * sm_count();
+  auto rows_pass = [&](int j0, int j1, const int* ok, bool pdl) -> cudaError_t {
+    const int nt = j1 - j0 + 1;
+    const int nd = sample ? std::max(0, std::min(j1, gamma - 1) - j0 + 1) : 0;
+    const long long units = (long long)B * (nt + nd) * n_chunks;
+    const int grid = (int)std::max<long long>(1, std::min<long long>((units + 7) / 8, cap));
+    ProfScope ps(kKVerifyRows, st);
+    if (pdl)
+      return sample ? launch_pdl(k_verify_rows<true>, grid, kThr, st, target, draft, B, gamma, V,
+                                 c, n_chunks, j0, j1, ok, vmax, vsum, varg)
+                    : launch_pdl(k_verify_rows<false>, grid, kThr, st, target, draft, B, gamma,
+                                 V, c, n_chunks, j0, j1, ok, vmax, vsum, varg);
+    if (sample)
+      k_verify_rows<true><<<grid, kThr, 0, st>>>(target, draft, B, gamma, V, c, n_chunks, j0, j1,
+                                                 ok, vmax, vsum, varg);
+    else
+      k_verify_rows<false><<<grid, kThr, 0, st>>>(target, draft, B, gamma, V, c, n_chunks, j0,
+                                                  j1, ok, vmax, vsum, varg);
+    return cudaGetLastError();
+  };
+  cudaError_t e;
+  if (split) {
+    // position 0 of every sequence, its decision, then the rest of the
+    // sequences that kept their position-0 token
+    if ((e = rows_pass(0, 0, nullptr, false)) != cudaSuccess) return e;
+    {
+      ProfScope ps(kKVerifyFirst, st);
+      e = sample ? launch_pdl(k_verify_first<true>, B, 96, st, target, draft, tokens, B, gamma,
+                              V, c, n_chunks, (const float*)vmax, (const float*)vsum,
+                              (const int*)varg, uniforms, seq_ok)
+                 : launch_pdl(k_verify_first<false>, B, 96, st, target, draft, tokens, B,
+                              gamma, V, c, n_chunks, (const float*)vmax, (const float*)vsum,
+                              (const int*)varg, uniforms, seq_ok);
+      if (e != cudaSuccess) return e;
+    }
+    if ((e = rows_pass(1, gamma, seq_ok, true)) != cudaSuccess) return e;
+  } else {
+    if ((e = rows_pass(0, gamma, nullptr, false)) != cudaSuccess) return e;
   }
   {
-  const int rows = sample ? 2 * gamma + 1 : gamma + 1;
-  const int dthreads = 32 * std::min(16, rows);
-  ProfScope ps(kKVerifyDecide, st);
-  if (sample)
-    k_verify_decide<true><<<B, dthreads, 0, st>>>(target, draft, tokens, B, gamma, V, c, n_chunks,
-                                                 vmax, vsum, varg, uniforms, out_tokens, out_nacc,
-                                                 info, error_word());
-  else
-    k_verify_decide<false><<<B, dthreads, 0, st>>>(target, draft, tokens, B, gamma, V, c,
-                                                  n_chunks, vmax, vsum, varg, uniforms,
-                                                  out_tokens, out_nacc, info, error_word());
+    const int rows = sample ? 2 * gamma + 1 : gamma + 1;
+    const int dthreads = 32 * (std::min(16, rows) + 1);  // merging warps + a loading warp
+    const int* ok = split ? seq_ok : nullptr;
+    ProfScope ps(kKVerifyDecide, st);
+    e = sample ? launch_pdl(k_verify_decide<true>, B, dthreads, st, target, draft, tokens, B,
+                            gamma, V, c, n_chunks, (const float*)vmax, (const float*)vsum,
+                            (const int*)varg, uniforms, ok, out_tokens, out_nacc, info,
+                            error_word())
+               : launch_pdl(k_verify_decide<false>, B, dthreads, st, target, draft, tokens, B,
+                            gamma, V, c, n_chunks, (const float*)vmax, (const float*)vsum,
+                            (const int*)varg, uniforms, ok, out_tokens, out_nacc, info,
+                            error_word());
+    if (e != cudaSuccess) return e;
   }
   if (sample) {
     const long long ru = (long long)B * n_chunks;

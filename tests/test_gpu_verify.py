@@ -106,6 +106,39 @@ def test_verify_bad_token_reports_device_error():
     assert ss.ss_get_device_error() == ss.SS_OK      # cleared by the read
 
 
+def test_verify_split_greedy():
+    """Rows above the split size: position 0 is decided between two row
+    passes.  Half the sequences keep their position-0 token (so their later
+    rows are read), half reject it (so theirs are not)."""
+    B, g, V = 32, 4, 131072
+    assert B * (g + 1) * V * 4 >= 64 * 2 ** 20
+    v = synth.verify_logits(77, B=B, gamma=g, V=V, kind="zipf")
+    x = _drafts(v, 0.0)
+    a0 = np.argmax(v["target"][:, 0], axis=1)
+    x[::2, 0] = a0[::2]                              # kept at position 0
+    x[1::2, 0] = (a0[1::2] + 1) % V                  # rejected at position 0
+    x[::4, 1:] = np.argmax(v["target"][::4, 1:g], axis=2)  # and some keep everything
+    toks, n = run_verify(v, x, 0.0)
+    check(v, x, 0.0, toks, n)
+    assert np.all(n[1::2] == 0) and np.all(n[::4] == g)
+
+
+@pytest.mark.parametrize("T", [0.7, 1.5])
+def test_verify_split_sampling(T):
+    """Sampling above the split size, with drafts close to the target (most
+    sequences keep position 0) and far from it (most do not)."""
+    B, g, V = 16, 3, 262144
+    assert B * (2 * g + 1) * V * 4 >= 64 * 2 ** 20
+    v = synth.verify_logits(78, B=B, gamma=g, V=V, kind="zipf", draft_sigma=0.3)
+    far = synth.verify_logits(79, B=B, gamma=g, V=V, kind="zipf", draft_sigma=3.0)
+    v["draft"][B // 2:] = far["draft"][B // 2:]
+    x = _drafts(v, T)
+    toks, n = run_verify(v, x, T)
+    c = check(v, x, T, toks, n)
+    print("split sampling", T, c, n.tolist())
+    assert c["exact"] >= 0.8 * B
+
+
 # ------------------------------------------------ full workload shapes -----
 def test_verify_llama8b_shape_greedy():
     p = synth.PRESETS["llama8b"]
