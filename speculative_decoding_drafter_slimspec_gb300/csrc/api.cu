@@ -46,7 +46,7 @@ static size_t head_ws_bytes(int M, int r, int V, bool bf16) {
     const MmaPlan p = mma_plan(r, M, V);
     size_t s = align256((size_t)M * r * 2);
     s += 3 * align256((size_t)M * p.n_sub * sizeof(float));
-    s += align256(2 * sizeof(unsigned));  // tile counters of the two launches
+    s += align256(2 * kMmaCtrs * sizeof(unsigned));  // tile counters of the two launches
     return s;
   }
   const HeadPlan plan = head_plan(bf16, r, M, V);
@@ -137,15 +137,15 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
     wk.pmax = cv.take<float>((size_t)M * mp.n_sub);
     wk.psum = cv.take<float>((size_t)M * mp.n_sub);
     wk.parg = cv.take<int>((size_t)M * mp.n_sub);
-    unsigned* ctr = cv.take<unsigned>(2);
+    unsigned* ctr = cv.take<unsigned>(2 * kMmaCtrs);
     const HeadOutputs outs{uniforms, out_tokens, out_logprob, out_row_max, out_row_lse};
-    cudaError_t e = launch_down_proj(bf16, hidden, w_down, M, d, r, true, z_ws, out_z, ctr, 2,
-                                     stream);
+    cudaError_t e = launch_down_proj(bf16, hidden, w_down, M, d, r, true, z_ws, out_z, ctr,
+                                     2 * kMmaCtrs, stream);
     if (e == cudaSuccess && out_logits != nullptr)
       e = launch_head_mma(mp, z_ws, w_up, M, r, V, 0.f, wk, outs, out_logits, ctr, stream);
     if (e == cudaSuccess)
-      e = launch_head_mma(mp, z_ws, w_up, M, r, V, temperature, wk, outs, nullptr, ctr + 1,
-                          stream);
+      e = launch_head_mma(mp, z_ws, w_up, M, r, V, temperature, wk, outs, nullptr,
+                          ctr + kMmaCtrs, stream);
     return cuda_status(e);
   }
   const HeadPlan plan = head_plan(bf16, r, M, V);

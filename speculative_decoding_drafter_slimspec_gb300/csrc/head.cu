@@ -8,6 +8,9 @@
 //
 //   k_down_proj    z = bf16(h W_down^T); all loads of a thread issued before
 //                  any use (one round trip); also clears the CTA counters.
+//                  Launched as a dependent of the previous library kernel: it
+//                  reads and multiplies while that kernel finishes and waits
+//                  for it only before writing.
 //   k_head_stream  W_up tiles -> shared memory by cp.async.bulk (a 3-deep ring
 //                  per warp, no cross-warp synchronisation in the stream), dot
 //                  products with mixed-precision FMAs (bf16 x bf16 + fp32, no
@@ -223,9 +226,7 @@ __global__ void __launch_bounds__(256) k_down_proj(const uint8_t* __restrict__ h
   constexpr int E = kBF16 ? 8 : 4, EB = kBF16 ? 2 : 4, JT = 4, MT = 8;
   const int j0 = blockIdx.x * JT, m0 = blockIdx.y * MT;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  pdl_launch_dependents();  // the stream kernel may start its W_up prologue now
-  if (ctr != nullptr && blockIdx.x == 0 && blockIdx.y == 0)
-    for (int i = threadIdx.x; i < n_ctr; i += blockDim.x) ctr[i] = 0u;
+  pdl_launch_dependents();  // the up-projection may start its W_up prologue now
   const int nch = d / E;
   const size_t rowb = (size_t)d * EB;
   uint4 wr[Q][JT], hr[Q][MT];
@@ -276,6 +277,12 @@ __global__ void __launch_bounds__(256) k_down_proj(const uint8_t* __restrict__ h
   ReduceScatter<32, 16>::run(v, lane);  // lane l now holds entry l = (a, b) = (l/8, l%8)
   __shared__ float red[8][32];
   red[warp][lane] = v[0];
+  // Launched as a dependent of the previous library kernel: h and W are
+  // inputs (never library outputs), read above while it may still run; z and
+  // the counters may still be in use by it, so they wait for its completion.
+  pdl_wait_producer();
+  if (ctr != nullptr && blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < n_ctr; i += blockDim.x) ctr[i] = 0u;
   __syncthreads();
   if (warp == 0) {
     float s = red[0][lane];
@@ -684,12 +691,22 @@ cudaError_t launch_down_proj(bool bf16, const void* h, const void* w, int M, int
   uint8_t* oz = (uint8_t*)out_z;
   const int rnd = round_bf16_z ? 1 : 0;
   ProfScope ps(kKDownProj, st);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
 #define SS_DOWN(B, Q)                                                                     \
   do {                                                                                      \
     cudaError_t e0 = set_smem_once(reinterpret_cast<const void*>(k_down_proj<B, Q>), 0);    \
     if (e0 != cudaSuccess) return e0;                                                       \
-    k_down_proj<B, Q><<<grid, 256, 0, st>>>(hp, wp, M, d, r, rnd, (uint8_t*)z_ws, oz, ctr,  \
-                                            n_ctr);                                         \
+    e0 = cudaLaunchKernelEx(&cfg, k_down_proj<B, Q>, hp, wp, M, d, r, rnd, (uint8_t*)z_ws,  \
+                            oz, ctr, n_ctr);                                                \
+    if (e0 != cudaSuccess) return e0;                                                       \
   } while (0)
   if (bf16) {
     if (q <= 1) SS_DOWN(true, 1);

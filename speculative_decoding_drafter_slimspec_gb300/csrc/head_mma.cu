@@ -170,18 +170,15 @@ constexpr uint32_t idesc_bf16(int m, int n) {
          | ((uint32_t)(m >> 4) << 24); // M / 16
 }
 
-// Swizzle atoms (8 rows of z) kept per K block of M tile mt, and the byte
-// offset of block (mt, kb) of z in shared memory.
-__host__ __device__ __forceinline__ int z_atoms(int M, int mt) {
-  const int rows = M - mt * kTileM;
-  return rows >= kTileM ? kTileM / 8 : (rows + 7) / 8;
+// Swizzle atoms (8 rows of z) kept per K block for a CTA's Ml <= 128 rows of
+// z, the byte offset of K block kb of them in shared memory, and their size.
+__host__ __device__ __forceinline__ int z_atoms(int Ml) {
+  return Ml >= kTileM ? kTileM / 8 : (Ml + 7) / 8;
 }
-__host__ __device__ __forceinline__ int z_block_off(int M, int KB, int mt, int kb) {
-  return (mt * KB * (kTileM / 8) + kb * z_atoms(M, mt)) * 1024;
+__host__ __device__ __forceinline__ int z_block_off(int Ml, int kb) {
+  return kb * z_atoms(Ml) * 1024;
 }
-__host__ __device__ __forceinline__ int z_bytes(int M, int KB, int MT) {
-  return MT == 1 ? KB * z_atoms(M, 0) * 1024 : KB * (kTileM / 8 + z_atoms(M, 1)) * 1024;
-}
+__host__ __device__ __forceinline__ int z_bytes(int Ml, int KB) { return KB * z_atoms(Ml) * 1024; }
 
 }  // namespace
 
@@ -244,25 +241,35 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&v)[32], int vid0, int
 }
 
 // ------------------------------------------------------------------ kernel --
-// MT: M tiles of 128 rows of z (1 or 2).  kMode 0: softmax partials; kMode 1:
-// the fp32 scores D[m, v] are written to out_scores (M x V).  kWide false: a
+// Every CTA holds one M tile of up to 128 rows of z: CTA b takes M tile
+// b % m_tiles and streams the vocabulary tiles of that M tile with the other
+// gridDim.x / m_tiles CTAs of it (their own tile counter).  With two M tiles
+// each W_up tile is read by two CTAs; the second read mostly hits L2, and
+// each CTA keeps room for more W_up stages in flight than one holding both
+// tiles of z would.  kMode 0: softmax partials; kMode 1: the fp32 scores
+// D[m, v] are written to out_scores (M x V).  kWide false: a
 // W_up stage is one K block, a 2-D box of 128 rows x 128 bytes.  kWide true:
 // a stage is KPS K blocks -- WB full ones as one 4-D box of 128 rows x WB*128
 // contiguous bytes (every row's bytes of the stage in one request run: fewer
 // DRAM page openings per byte), then, when r is not a multiple of 64, the
 // ragged last block as a 2-D box.  tile_ctr is zeroed by the down-projection
 // that precedes this grid.
-template <bool kSample, int MT, int kMode, bool kWide>
+template <bool kSample, int kMode, bool kWide>
 __global__ void __launch_bounds__(kThreads, 1)
     k_head_mma(const uint16_t* __restrict__ z, const __grid_constant__ CUtensorMap tm_w,
-               const __grid_constant__ CUtensorMap tm_w2, int M, int R, int V, int KB, int KPS,
-               int WB, int NST, float c, int n_tiles, MmaPart part, float* __restrict__ out_scores,
-               unsigned* __restrict__ tile_ctr, unsigned* err) {
+               const __grid_constant__ CUtensorMap tm_w2, int M, int m_tiles, int R, int V, int KB,
+               int KPS, int WB, int NST, float c, int n_tiles, MmaPart part,
+               float* __restrict__ out_scores, unsigned* __restrict__ tile_ctr, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint8_t* sA = smem;                          // MT * KB compact blocks of z
-  uint8_t* sB = smem + z_bytes(M, KB, MT);     // NST stages of W_up
+  const int mtc = (int)blockIdx.x % m_tiles;   // this CTA's M tile
+  const int cb = (int)blockIdx.x / m_tiles;    // its index among that tile's CTAs
+  const int gm = (int)gridDim.x / m_tiles;     // CTAs per M tile
+  const int m0 = mtc * kTileM;                 // first row of z of this CTA
+  const int Ml = min(kTileM, M - m0);          // rows of z of this CTA
+  uint8_t* sA = smem;                          // KB compact blocks of z
+  uint8_t* sB = smem + z_bytes(Ml, KB);        // NST stages of W_up
   const int kStageBytes = (kWide ? KPS : 1) * kBlockBytes;
   const int SPT = kWide ? KB / KPS : KB;       // stages per vocabulary tile
   __shared__ uint64_t full[kMaxStages], empty[kMaxStages], a_full, acc_full[2], acc_empty[2];
@@ -271,7 +278,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_fills[kMaxStages];  // TMA fills issued per stage (drained before exit)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  constexpr uint32_t kCols = 2 * MT * kTileN;  // double-buffered accumulators
+  constexpr uint32_t kCols = 2 * kTileN;  // double-buffered accumulators
   constexpr uint32_t kIdesc = idesc_bf16(kTileM, kTileN);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -317,19 +324,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int G = kWide ? 1 : (NST >= 2 * kProdGroup ? kProdGroup : 2);
     int it = 0;
     bool ok = true;
-    // Tiles b + k * grid (k < kStaticTiles) are this CTA's own (the first is
-    // loaded while the down-projection runs); tile kStaticTiles * grid + k
-    // goes to whoever draws k from the counter.  Lane 0 draws one tile ahead:
+    // Tiles cb + k * gm (k < kStaticTiles) are this CTA's own (the first is
+    // loaded while the down-projection runs); tile kStaticTiles * gm + k goes
+    // to whichever CTA of this M tile draws k from its counter.  Lane 0 draws one tile ahead:
     // the draw gets a tile's worth of loads to come back, and a CTA holds at
     // most one tile it has not started when the counter runs out.
     unsigned q0 = 0;
     for (int i = 0; ok; ++i) {
       int t;
       if (i < kStaticTiles) {
-        t = blockIdx.x + i * gridDim.x;
+        t = cb + i * gm;
       } else {
-        t = kStaticTiles * gridDim.x + (int)__shfl_sync(0xFFFFFFFFu, q0, 0);
-        if (lane == 0 && t < n_tiles) q0 = atomicAdd(tile_ctr, 1u);  // none past the end
+        t = kStaticTiles * gm + (int)__shfl_sync(0xFFFFFFFFu, q0, 0);
+        if (lane == 0 && t < n_tiles) q0 = atomicAdd(tile_ctr + mtc, 1u);  // none past the end
       }
       if (t >= n_tiles) t = -1;
       const int slot = i % kTileRing;
@@ -373,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (i == kStaticTiles - 1 && lane == 0) {
         pdl_wait_producer();  // the counter is zeroed by the down-projection
-        q0 = atomicAdd(tile_ctr, 1u);
+        q0 = atomicAdd(tile_ctr + mtc, 1u);
       }
     }
   } else if (warp == kMmaWarp) {
@@ -403,15 +410,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 !kWide ? sw128_desc(smem_u32(stg))
                 : kbi < WB ? sw128_desc(smem_u32(stg + kbi * 1024), (uint32_t)WB * 1024u)
                            : sw128_desc(smem_u32(stg + (size_t)WB * kBlockBytes));
+            const uint64_t adesc = sw128_desc(smem_u32(sA + z_block_off(Ml, kb)));
 #pragma unroll
-            for (int k4 = 0; k4 < 4; ++k4) {
-#pragma unroll
-              for (int mt = 0; mt < MT; ++mt) {
-                const uint64_t adesc = sw128_desc(smem_u32(sA + z_block_off(M, KB, mt, kb)));
-                mma_bf16(tmem + (uint32_t)((buf * MT + mt) * kTileN), adesc + 2 * k4,
-                         bdesc + 2 * k4, kIdesc, (kb | k4) != 0 ? 1u : 0u);
-              }
-            }
+            for (int k4 = 0; k4 < 4; ++k4)
+              mma_bf16(tmem + (uint32_t)(buf * kTileN), adesc + 2 * k4, bdesc + 2 * k4, kIdesc,
+                       (kb | k4) != 0 ? 1u : 0u);
           }
           mma_commit(&empty[s]);  // the stage is free once these MMAs complete
         }
@@ -430,32 +433,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;           // the TMEM lane quadrant this warp may read
     {
       // z is written by the down-projection that precedes this grid.  Block
-      // (mt, kb) holds rows mt*128 .. +127 and columns kb*64 .. +63 of z; row
-      // i of a block is 128 bytes at i*128, its 16-byte chunk c stored at
+      // kb holds this CTA's rows m0 .. m0+Ml-1 and columns kb*64 .. +63 of z;
+      // row i of a block is 128 bytes at i*128, its 16-byte chunk c stored at
       // chunk c ^ (i % 8) (the 128-byte swizzle).  Columns past r are zero.
       // Every 16-byte piece is an asynchronous copy, all of a thread's in
       // flight at once (under a full memory queue each round trip takes
       // microseconds); pieces past r are zero-filled by the copy itself.
       pdl_wait_producer();
-      const int n_items = M * KB * 8;  // (row m, K block, 16-byte chunk), chunk fastest
+      const int n_items = Ml * KB * 8;  // (row i, K block, 16-byte chunk), chunk fastest
       for (int it = ew * 32 + lane; it < n_items; it += 32 * kEpiWarps) {
         const int c8 = it & 7, q = it >> 3;
-        const int m = q / KB, kb = q - m * KB;
-        const int i = m & (kTileM - 1), k0 = kb * 64 + c8 * 8;
+        const int i = q / KB, kb = q - i * KB;
+        const int k0 = kb * 64 + c8 * 8;
         const bool in = k0 < R;
-        cp_async16_zfill(sA + z_block_off(M, KB, m >> 7, kb) + i * 128 + ((c8 ^ (i & 7)) * 16),
-                         z + (size_t)m * R + (in ? k0 : 0), in ? 16u : 0u);
+        cp_async16_zfill(sA + z_block_off(Ml, kb) + i * 128 + ((c8 ^ (i & 7)) * 16),
+                         z + (size_t)(m0 + i) * R + (in ? k0 : 0), in ? 16u : 0u);
       }
       cp_async_wait_all();
       fence_proxy_async_smem();  // visible to the tensor cores (async proxy)
       __syncwarp();
       if (lane == 0) mbar_arrive(&a_full);
     }
-    const int mt = MT == 2 ? ew / 4 : 0;
-    const int half = MT == 2 ? 0 : ew / 4;
-    const int row = mt * kTileM + quad * 32 + lane;  // row of z owned by this thread
-    const bool live = row < M;
-    const bool warp_live = mt * kTileM + quad * 32 < M;  // any live row in this warp
+    const int half = ew / 4;                 // the 64-column half of each tile
+    const int row = m0 + quad * 32 + lane;   // row of z owned by this thread
+    const bool live = quad * 32 + lane < Ml;
+    const bool warp_live = quad * 32 < Ml;   // any live row in this warp
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const int n_sub = 2 * n_tiles;
     for (int i = 0;; ++i) {
@@ -469,16 +471,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait_bounded(&acc_full[buf], (i >> 1) & 1, err);
       if (!__all_sync(0xFFFFFFFFu, ok) || *(volatile int*)&s_abort) break;
       tc_fence_after();
-#pragma unroll
-      for (int hh = 0; hh < (MT == 2 ? 2 : 1); ++hh) {
-        const int h = MT == 2 ? hh : half;
+      {
+        const int h = half;
         RowState st = row_state_empty();
         if (warp_live) {
           // both 32-column loads of the sub-tile in flight, one wait
           uint32_t v2[2][32];
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc)
-            tmem_ld32_issue(tmem + lane_addr + (uint32_t)((buf * MT + mt) * kTileN + h * kSubW + cc * 32),
+            tmem_ld32_issue(tmem + lane_addr + (uint32_t)(buf * kTileN + h * kSubW + cc * 32),
                             v2[cc]);
           tmem_ld_wait();
 #pragma unroll
@@ -583,6 +584,8 @@ __global__ void __launch_bounds__(kFinThreads)
   __shared__ int s_i[2];    // chosen thread, chosen sub-tile
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x;
+  pdl_launch_dependents();  // the next call's down-projection may start reading
+  const float u = (kSample && m < M) ? __ldg(out.uniforms + m) : 0.f;  // an input
   pdl_wait_producer();
   if (m >= M) return;
   const int per = (n_sub + kFinThreads - 1) / kFinThreads;
@@ -636,7 +639,7 @@ __global__ void __launch_bounds__(kFinThreads)
   const float incl = __fadd_rn(woff, wincl);
   const float prev = __shfl_up_sync(0xFFFFFFFFu, wincl, 1);
   const float excl = lane > 0 ? __fadd_rn(woff, prev) : woff;
-  const float target = __ldg(out.uniforms + m) * W;
+  const float target = u * W;
   // the first thread whose inclusive mass passes the target; else the last
   // thread with any mass (the target sits at the very top after rounding).
   // Both in one reduction: the key ranks hits above misses, then by thread.
@@ -800,9 +803,9 @@ MmaPlan mma_plan(int r, int M, int V) {
   MmaPlan p{};
   p.ok = false;
   if (M <= 0 || M > 2 * kTileM || r % 8 != 0 || r > 512) return p;  // finish: <= 2 chunks per lane
-  p.mt = M <= kTileM ? 1 : 2;
+  p.mt = M <= kTileM ? 1 : 2;  // M tiles, one per CTA
   p.kb = (r + 63) / 64;
-  const int a_bytes = z_bytes(M, p.kb, p.mt);
+  const int a_bytes = z_bytes(std::min(M, kTileM), p.kb);  // the largest CTA's z
   const int room = kSmemCap - 1024 - a_bytes;
   // wide stages (several K blocks per request run of each row) when the 4-D
   // view is exact (V % 8 == 0) and z leaves room for two of them: 4 K blocks
@@ -810,7 +813,7 @@ MmaPlan mma_plan(int r, int M, int V) {
   // full ones by 4-D box, a ragged last one by 2-D box)
   p.kps = 1;
   p.wb = 0;
-  if (p.mt == 1 && V % 8 == 0) {  // (with two M tiles z leaves no room for them)
+  if (V % 8 == 0) {
     if (r % 256 == 0 && room / (4 * kBlockBytes) >= 2) {
       p.kps = 4;
       p.wb = 4;
@@ -824,19 +827,19 @@ MmaPlan mma_plan(int r, int M, int V) {
   if (p.nst < (p.kps > 1 ? 2 : 3)) return p;
   p.smem = 1024 + a_bytes + p.nst * stage;
   p.n_tiles = (V + kTileN - 1) / kTileN;
-  p.grid = std::max(1, std::min(sm_count(), p.n_tiles));
+  p.grid = p.mt * std::max(1, std::min(sm_count() / p.mt, p.n_tiles));
   p.n_sub = 2 * p.n_tiles;
   if (p.n_sub > kFinThreads * kFinPer) return p;  // V > 786432: beyond the finish's registers
   p.ok = true;
   return p;
 }
 
-template <bool kSample, int MT, int kMode, bool kWide>
+template <bool kSample, int kMode, bool kWide>
 static cudaError_t launch_mma_kps(const MmaPlan& p, const void* z, const CUtensorMap& tw,
                                   const CUtensorMap& tw2, int M, int r, int V, float c,
                                   const MmaPart& part, float* scores, unsigned* ctr,
                                   cudaStream_t st) {
-  auto kern = k_head_mma<kSample, MT, kMode, kWide>;
+  auto kern = k_head_mma<kSample, kMode, kWide>;
   // the limit is set once per kernel: make it the largest size any plan asks for
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), kSmemCap);
   if (e != cudaSuccess) return e;
@@ -851,21 +854,18 @@ static cudaError_t launch_mma_kps(const MmaPlan& p, const void* z, const CUtenso
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   ProfScope ps(kKHeadMma, st);
-  return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint16_t*>(z), tw, tw2, M, r, V,
-                            p.kb, p.kps, p.wb, p.nst, c, p.n_tiles, part, scores, ctr,
+  return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint16_t*>(z), tw, tw2, M, p.mt, r,
+                            V, p.kb, p.kps, p.wb, p.nst, c, p.n_tiles, part, scores, ctr,
                             error_word());
 }
-// Wide stages only with one M tile (z of up to 128 rows leaves room for them).
-template <bool kSample, int MT, int kMode>
+template <bool kSample, int kMode>
 static cudaError_t launch_mma_one(const MmaPlan& p, const void* z, const CUtensorMap& tw,
                                   const CUtensorMap& tw2, int M, int r, int V, float c,
                                   const MmaPart& part, float* scores, unsigned* ctr,
                                   cudaStream_t st) {
-  if (MT == 1 && p.kps > 1)  // the plan picks wide stages only with one M tile
-    return launch_mma_kps<kSample, 1, kMode, true>(p, z, tw, tw2, M, r, V, c, part, scores, ctr,
-                                                    st);
-  return launch_mma_kps<kSample, MT, kMode, false>(p, z, tw, tw2, M, r, V, c, part, scores, ctr,
-                                                    st);
+  if (p.kps > 1)
+    return launch_mma_kps<kSample, kMode, true>(p, z, tw, tw2, M, r, V, c, part, scores, ctr, st);
+  return launch_mma_kps<kSample, kMode, false>(p, z, tw, tw2, M, r, V, c, part, scores, ctr, st);
 }
 
 cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up, int M, int r,
@@ -887,16 +887,13 @@ cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up
   const MmaPart part{w.pmax, w.psum, w.parg};
   cudaError_t e;
   if (scores != nullptr) {
-    e = p.mt == 1 ? launch_mma_one<false, 1, 1>(p, z_ws, tw, tw2, M, r, V, c, part, scores, ctr, st)
-                  : launch_mma_one<false, 2, 1>(p, z_ws, tw, tw2, M, r, V, c, part, scores, ctr, st);
+    e = launch_mma_one<false, 1>(p, z_ws, tw, tw2, M, r, V, c, part, scores, ctr, st);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   if (sample)
-    e = p.mt == 1 ? launch_mma_one<true, 1, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st)
-                  : launch_mma_one<true, 2, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st);
+    e = launch_mma_one<true, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st);
   else
-    e = p.mt == 1 ? launch_mma_one<false, 1, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st)
-                  : launch_mma_one<false, 2, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st);
+    e = launch_mma_one<false, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st);
   if (e != cudaSuccess) return e;
   // the per-row finish, launched to overlap the tail of the MMA grid
   cudaLaunchConfig_t cfg = {};

@@ -481,7 +481,7 @@ size_t specvocab_ws_bytes(int M, int d, int d_prime, int V, int k) {
     size_t s = 0;
     s += align256((size_t)M * d_prime * 2);          // h' (bf16)
     s += align256((size_t)M * V * sizeof(float));    // scores
-    s += align256(sizeof(unsigned));                 // the router's tile counter
+    s += align256(kMmaCtrs * sizeof(unsigned));      // the router's tile counters
     s += align256((size_t)M * k * sizeof(int32_t));  // candidates
     s += align256((size_t)M * k * sizeof(float));    // candidate logits
     return s;
@@ -514,11 +514,11 @@ cudaError_t launch_specvocab(const void* h, const void* w_down, const void* w_vo
   cudaError_t e;
   if (router_mma(M, d_prime, V)) {
     // s = W_vocab h' as the tcgen05 kernel's fp32 scores
-    unsigned* ctr = cv.take<unsigned>(1);
+    unsigned* ctr = cv.take<unsigned>(kMmaCtrs);
     cand = cv.take<int32_t>((size_t)M * k);
     zc = cv.take<float>((size_t)M * k);
     if (out_scores) scores = out_scores;
-    e = launch_down_proj(true, h, w_down, M, d, d_prime, true, hp, nullptr, ctr, 1, st);
+    e = launch_down_proj(true, h, w_down, M, d, d_prime, true, hp, nullptr, ctr, kMmaCtrs, st);
     if (e != cudaSuccess) return e;
     const MmaPlan mp = mma_plan(d_prime, M, V);
     const MmaWork none{nullptr, nullptr, nullptr};

@@ -100,14 +100,14 @@ cudaError_t launch_head_stream(const HeadPlan& plan, bool bf16, const void* w_up
 
 // Tensor-core up-projection (head_mma.cu) for bf16 heads.
 struct MmaPlan {
-  int mt;       // 128-row tiles of z (1 or 2)
+  int mt;       // 128-row tiles of z (1 or 2), each taken by its own CTAs
   int kb;       // 64-wide K blocks of r
   int kps;      // K blocks per W_up stage (1 for 2-D boxes; more for wide stages)
   int wb;       // of those, full K blocks loaded by one 4-D box (wide stages)
   int nst;      // W_up stages in shared memory
   int smem;     // dynamic shared memory bytes
   int n_tiles;  // 128-row vocabulary tiles
-  int grid;     // CTAs (one per SM)
+  int grid;     // CTAs (one per SM; a multiple of mt)
   int n_sub;    // 64-row partials per row of z (2 per tile)
   bool ok;
 };
@@ -118,8 +118,10 @@ struct MmaWork {
   int* parg;
 };
 // z_ws: M x r bf16.  With `scores` non-null the fp32 products z W_up^T are
-// written there (M x V) instead of being reduced.  ctr: the launch's tile
-// counter, zeroed by the down-projection that precedes it in the stream.
+// written there (M x V) instead of being reduced.  ctr: the launch's kMmaCtrs
+// tile counters (one per M tile), zeroed by the down-projection that precedes
+// it in the stream.
+constexpr int kMmaCtrs = 2;
 cudaError_t launch_head_mma(const MmaPlan& plan, const void* z_ws, const void* w_up, int M, int r,
                             int V, float temperature, const MmaWork& work,
                             const HeadOutputs& out, float* scores, unsigned* ctr,
