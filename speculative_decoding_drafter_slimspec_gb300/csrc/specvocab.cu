@@ -4,8 +4,10 @@
 //   h' = bf16(W_down h)        (k_down_proj, shared with the low-rank head)
 //   s  = W_vocab h'            (the head's tcgen05 up-projection in its scores
 //                              mode, or the CUDA-core stream when it does not fit)
-//   K  = topk(s, k)            k_topk: radix select on order-preserving keys,
-//                              ties to the lowest id, ordered compaction
+//   K  = topk(s, k)            k_topk: a cluster of CTAs per row filters the
+//                              row against a sampled threshold; radix select
+//                              on order-preserving keys, ties to the lowest
+//                              id, ordered compaction
 //   z' = U[K] h                k_gather_logits: a warp per candidate row of U
 //                              (8 KB at d = 4096) with h held in registers;
 //                              CTAs of one candidate range across all rows of
@@ -152,50 +154,8 @@ __device__ void block_compact(const Keys& key_at, const Ids& id_at, int n, uint3
     eq_seen += __popc(eqb);
   }
 }
-// The candidate buffer as 32 per-warp regions of kTopkRegion entries, region w
-// holding cnt[w] entries in id order.  Entry i of the buffer is live when
-// (i % kTopkRegion) < cnt[i / kTopkRegion].
+// The region buffer: 32 per-warp regions of kTopkRegion entries each.
 constexpr int kTopkRegion = kTopkCap / 32;
-struct KeysInRegions {
-  const uint32_t* k;
-  const int* cnt;
-  __device__ bool live(int i) const { return (i % kTopkRegion) < cnt[i / kTopkRegion]; }
-  __device__ uint32_t operator()(int i) const { return k[i]; }
-};
-
-// block_compact over the regions: warp w walks region w (its cnt[w] entries).
-template <class Ids>
-__device__ void region_compact(const uint32_t* keys, const Ids& id_at, const int* cnt, uint32_t thr,
-                               int need, int k, int* s_cnt, int32_t* out) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int lo = warp * kTopkRegion, hi = lo + cnt[warp];
-  const unsigned lt = (1u << lane) - 1u;
-  int gt = 0, eq = 0;
-  for (int v0 = lo; v0 < hi; v0 += 32) {
-    const int v = v0 + lane;
-    const uint32_t key = v < hi ? keys[v] : 0u;
-    gt += __popc(__ballot_sync(0xFFFFFFFFu, v < hi && key > thr));
-    eq += __popc(__ballot_sync(0xFFFFFFFFu, v < hi && key == thr));
-  }
-  if (lane == 0) { s_cnt[warp] = gt; s_cnt[32 + warp] = eq; }
-  __syncthreads();
-  int gt_pre = 0, eq_pre = 0;
-  for (int w = 0; w < warp; ++w) { gt_pre += s_cnt[w]; eq_pre += s_cnt[32 + w]; }
-  __syncthreads();
-  int pos = gt_pre + min(eq_pre, need), eq_seen = eq_pre;
-  for (int v0 = lo; v0 < hi; v0 += 32) {
-    const int v = v0 + lane;
-    const uint32_t key = v < hi ? keys[v] : 0u;
-    const bool is_gt = v < hi && key > thr, is_eq = v < hi && key == thr;
-    const unsigned eqb = __ballot_sync(0xFFFFFFFFu, is_eq);
-    const bool keep = is_gt || (is_eq && eq_seen + __popc(eqb & lt) < need);
-    const unsigned kb = __ballot_sync(0xFFFFFFFFu, keep);
-    const int my = pos + __popc(kb & lt);
-    if (keep && my < k) out[my] = id_at(v);
-    pos += __popc(kb);
-    eq_seen += __popc(eqb);
-  }
-}
 
 struct IdSelf {
   __device__ int32_t operator()(int i) const { return i; }
@@ -205,28 +165,74 @@ struct IdInShared {
   __device__ int32_t operator()(int i) const { return id[i]; }
 };
 
-// One CTA of 1024 threads per row.
+// Clusters: rank and size of this CTA in its cluster, the cluster-wide
+// barrier (release / acquire: shared-memory writes before it, local or
+// remote, are visible after it), and loads / stores to another CTA's shared
+// memory at the address of a local object.
+__device__ __forceinline__ int cluster_rank() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return (int)r;
+}
+__device__ __forceinline__ int cluster_size() {
+  unsigned r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return (int)r;
+}
+__device__ __forceinline__ void cluster_barrier() {
+  asm volatile(
+      "barrier.cluster.arrive.release.aligned;\n\t"
+      "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ __forceinline__ uint32_t cluster_addr(const void* local, int rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_cluster(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+
+// One cluster of C CTAs (1024 threads each) per row; CTA rank j takes the
+// j-th of C equal id ranges of the row.
 //   1. A threshold t: the key of rank ~1.25 k V / S in a strided sample of S
-//      scores (exact rank k when the sample is the whole row).
-//   2. One ordered pass keeps every score with key >= t, in id order, in a
-//      shared buffer of kTopkCap entries.
-//   3. Exact selection among those: they hold the k largest whenever there are
-//      at least k of them, so the result is the full row's; otherwise (or on
-//      overflow) the selection runs over the whole row instead.
+//      scores (exact rank k when the sample is the whole row); every CTA of
+//      the cluster computes the same one.
+//   2. One ordered pass over the CTA's range keeps every score with key >= t,
+//      in id order, in per-warp regions of a shared buffer.
+//   3. After a cluster barrier every CTA writes its candidates, in id order,
+//      into the first CTA's compact buffer (CTAs in rank order, warps in
+//      order), through distributed shared memory.
+//   4. The first CTA selects exactly among them: they hold the k largest
+//      whenever there are at least k of them, so the result is the full
+//      row's; otherwise (or when a region or the compact buffer would
+//      overflow) it selects over the whole row instead.
 __global__ void __launch_bounds__(kTopkThreads) k_topk(const float* __restrict__ scores, int V,
                                                        int k, int32_t* __restrict__ out_idx) {
   extern __shared__ uint32_t s_dyn[];
-  uint32_t* c_key = s_dyn;                                     // kTopkCap keys
-  int32_t* c_id = reinterpret_cast<int32_t*>(s_dyn + kTopkCap);  // kTopkCap ids
+  uint32_t* c_key = s_dyn;                                         // kTopkCap keys (regions)
+  int32_t* c_id = reinterpret_cast<int32_t*>(s_dyn + kTopkCap);    // kTopkCap ids (regions)
+  uint32_t* a_key = s_dyn + 2 * kTopkCap;                          // compact keys (first CTA)
+  int32_t* a_id = reinterpret_cast<int32_t*>(s_dyn + 3 * kTopkCap);  // compact ids
   __shared__ int hist[2048];
   __shared__ int s_warp[32];
   __shared__ int s_sel[2];
-  const int row = blockIdx.x, tid = threadIdx.x;
+  __shared__ int s_reg[32];     // candidates kept per warp region
+  __shared__ int s_over;        // a region of this CTA overflowed
+  __shared__ int s_all[8 * 32]; // every CTA's region counts, CTAs in rank order
+  __shared__ int s_any;         // an overflow anywhere in the cluster
+  const int C = cluster_size(), rank = cluster_rank();
+  const int row = blockIdx.x / C, tid = threadIdx.x;
   const float* s = scores + (size_t)row * V;
   int32_t* out = out_idx + (size_t)row * k;
   const KeysFromScores row_keys{s};
 
-  // 1. the threshold from the sample (held in the candidate buffer for now):
+  // 1. the threshold from the sample (held in the region buffer for now):
   //    S scores in blocks of 32 consecutive ones spread evenly over the row
   const int S = min(V, kTopkSample);
   const int lane = tid & 31, warp = tid >> 5;
@@ -253,18 +259,16 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float* __restrict__
   block_select_desc(KeysInShared{c_key}, S, q, hist, s_warp, s_sel, t_low, unused);
 
   // 2. (the sample's keys are no longer read: block_select_desc ended on a
-  //    barrier) one pass over the row: warp w walks a contiguous segment, 16 loads in
-  //    flight per lane, and appends the scores with key >= t, in id order, to
-  //    region w of the buffer (s_reg[w] entries; an overflow sends the row to
-  //    the full selection)
-  __shared__ int s_reg[32];
-  __shared__ int s_over;
+  //    barrier) one pass over this CTA's ids: warp w walks a contiguous
+  //    segment, 16 loads in flight per lane, and appends the scores with
+  //    key >= t, in id order, to region w of the buffer
   if (tid == 0) s_over = 0;
-  const int segw = ((V + 1023) / 1024) * 32;
-  const int lo = min(V, warp * segw), hi = min(V, lo + segw);
+  const int part = (V + C - 1) / C;
+  const int p_lo = min(V, rank * part), p_hi = min(V, p_lo + part);
+  const int segw = ((p_hi - p_lo + 1023) / 1024) * 32;
+  const int lo = min(p_hi, p_lo + warp * segw), hi = min(p_hi, lo + segw);
   const unsigned lt = (1u << lane) - 1u;
   int cnt = 0;
-  bool over = false;
   constexpr int kDepth = 16;
   for (int b0 = lo; b0 < hi; b0 += 32 * kDepth) {
     float x[kDepth];
@@ -287,24 +291,42 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float* __restrict__
       cnt += __popc(kb);
     }
   }
-  over = cnt > kTopkRegion;
   __syncthreads();
   if (lane == 0) {
     s_reg[warp] = min(cnt, kTopkRegion);
-    if (over) s_over = 1;
-    hist[warp] = cnt;
+    if (cnt > kTopkRegion) s_over = 1;
   }
+  cluster_barrier();  // every CTA's regions and counts are final
+
+  // 3. every CTA's counts (CTAs in rank order), then this CTA's candidates into
+  //    the first CTA's compact buffer
+  if (tid == 0) s_any = 0;
   __syncthreads();
-  int n_c = 0;
-  for (int w = 0; w < kTopkThreads / 32; ++w) n_c += hist[w];
-  const bool ok = !s_over && n_c >= k;
+  if (tid < C * 32) s_all[tid] = (int)ld_cluster(cluster_addr(&s_reg[tid & 31], tid >> 5));
+  if (tid < C && ld_cluster(cluster_addr(&s_over, tid)) != 0u) atomicOr(&s_any, 1);
   __syncthreads();
+  int base = 0, n_c = 0;
+  for (int i = 0; i < C * 32; ++i) {
+    if (i < rank * 32 + warp) base += s_all[i];
+    n_c += s_all[i];
+  }
+  const bool ok = s_any == 0 && n_c >= k && n_c <= kTopkCap;
+  if (ok) {
+    const uint32_t dk = cluster_addr(a_key, 0), di = cluster_addr(a_id, 0);
+    for (int i = lane; i < s_reg[warp]; i += 32) {
+      st_cluster(dk + 4u * (uint32_t)(base + i), c_key[warp * kTopkRegion + i]);
+      st_cluster(di + 4u * (uint32_t)(base + i), (uint32_t)c_id[warp * kTopkRegion + i]);
+    }
+  }
+  cluster_barrier();  // the first CTA's compact buffer is complete
+  if (rank != 0) return;
+
+  // 4. exact selection
   uint32_t thr;
   int need;
   if (ok) {
-    // 3. exact selection among the candidates
-    block_select_desc(KeysInRegions{c_key, s_reg}, kTopkCap, k, hist, s_warp, s_sel, thr, need);
-    region_compact(c_key, IdInShared{c_id}, s_reg, thr, need, k, hist, out);
+    block_select_desc(KeysInShared{a_key}, n_c, k, hist, s_warp, s_sel, thr, need);
+    block_compact(KeysInShared{a_key}, IdInShared{a_id}, n_c, thr, need, k, hist, out);
   } else {
     block_select_desc(row_keys, V, k, hist, s_warp, s_sel, thr, need);
     block_compact(row_keys, IdSelf{}, V, thr, need, k, hist, out);
@@ -462,15 +484,60 @@ __global__ void __launch_bounds__(256)
 // -------------------------------------------------------------- host side --
 size_t topk_ws_bytes(int M, int V, int k) { return 0; }
 
+namespace {
+// CTAs per row: the largest power of two <= 8 with M * C <= the SM count that
+// the occupancy calculator accepts as a cluster (C >= 1).
+int topk_cluster(int M) {
+  static int fits[4] = {-1, -1, -1, -1};  // C = 1, 2, 4, 8
+  int C = 1;
+  while (C < 8 && (long long)M * C * 2 <= sm_count()) C *= 2;
+  for (; C > 1; C >>= 1) {
+    int& f = fits[C == 2 ? 1 : C == 4 ? 2 : 3];
+    if (f < 0) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3((unsigned)C);
+      cfg.blockDim = dim3(kTopkThreads);
+      cfg.dynamicSmemBytes = kTopkCap * 16;
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = (unsigned)C;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int n = 0;
+      const cudaError_t e = cudaOccupancyMaxActiveClusters(&n, k_topk, &cfg);
+      if (e != cudaSuccess) (void)cudaGetLastError();
+      f = (e == cudaSuccess && n > 0) ? 1 : 0;
+    }
+    if (f == 1) break;
+  }
+  return C;
+}
+}  // namespace
+
 cudaError_t launch_topk(const float* scores, int M, int V, int k, int32_t* out_idx, void* ws,
                         cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
-  const int smem = kTopkCap * 8;
+  const int smem = kTopkCap * 16;  // region keys and ids, compact keys and ids
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(k_topk), smem);
   if (e != cudaSuccess) return e;
+  const int C = topk_cluster(M);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(M * C));
+  cfg.blockDim = dim3(kTopkThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)C;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   ProfScope ps(kKTopk, st);
-  k_topk<<<M, kTopkThreads, smem, st>>>(scores, V, k, out_idx);
-  return cudaGetLastError();
+  e = cudaLaunchKernelEx(&cfg, k_topk, scores, V, k, out_idx);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // The router runs on the tensor cores when the shape fits the tcgen05 kernel.

@@ -37,6 +37,34 @@ def test_topk_continuous_scores():
         np.testing.assert_array_equal(g[m], oracle.topk_lowest_index(s[m], k))
 
 
+@pytest.mark.parametrize("M", [1, 32, 40])
+def test_topk_cluster_shapes(M):
+    """Rows split over clusters of 8, 4 and 2 CTAs (the cluster size follows
+    the row count); candidates of every CTA meet in one ordered buffer."""
+    rng = np.random.default_rng(100 + M)
+    V, k = 151936, 2048
+    s = rng.standard_normal((M, V)).astype(np.float32)
+    s[:, ::1000] += 3.0   # a spread of large scores across every CTA's range
+    g = ss.ss_topk_rows(to_dev(s, "f32"), k).cpu().numpy()
+    for m in range(M):
+        np.testing.assert_array_equal(g[m], oracle.topk_lowest_index(s[m], k))
+
+
+def test_topk_skewed_rows_fall_back():
+    """The largest scores packed into the first ids of a row (one warp's
+    region overflows), at the end of a row, and a row of exact ties: the
+    whole-row selection gives the same ids."""
+    rng = np.random.default_rng(7)
+    M, V, k = 3, 151936, 2048
+    s = rng.standard_normal((M, V)).astype(np.float32)
+    s[0, :3000] += 10.0
+    s[1, -2500:] += 10.0
+    s[2] = 1.0
+    g = ss.ss_topk_rows(to_dev(s, "f32"), k).cpu().numpy()
+    for m in range(M):
+        np.testing.assert_array_equal(g[m], oracle.topk_lowest_index(s[m], k))
+
+
 def _run(seed, M, d, dp, V, k, T):
     inp = synth.specvocab_inputs(seed, M=M, d=d, d_prime=dp, V=V)
     u = synth.uniforms(np.random.default_rng(seed + 1), (M,))
