@@ -334,7 +334,11 @@ def profiled_traffic(kernel: str, workload: str):
         if ":" in line:
             k, v = line.split(":", 1)
             fields[k.strip()] = v.strip()
-    src_file = {"k_head_mma": "head_mma.cu", "k_head_stream": "head.cu"}.get(kernel, "head.cu")
+    src_file = {"k_head_mma": "head_mma.cu", "k_head_stream": "head.cu", "k_down_proj": "head.cu",
+                "k_verify_rows": "verify.cu", "k_topk": "specvocab.cu",
+                "k_gather_logits": "specvocab.cu"}.get(kernel)
+    if src_file is None:
+        return None
     src = os.path.join(ROOT, "speculative_decoding_drafter_slimspec_gb300", "csrc", src_file)
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     if fields.get("source_sha256") != sha:
