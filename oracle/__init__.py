@@ -45,12 +45,13 @@ from .bf16 import round_to_bf16
 from .head import down_projection, up_projection, dense_logits, row_reduce, \
     inverse_cdf, slimspec_head, dense_head
 from .specvocab import approx_scores, topk_lowest_index, specvocab_head
-from .verify import softmax_t, verify_greedy, verify_decide, verify_sampling, verify_batch
+from .verify import softmax_t, verify_greedy, verify_decide, verify_sampling, verify_batch, \
+    verify_lowrank_batch
 from . import theory
 
 __all__ = [
     "round_to_bf16", "down_projection", "up_projection", "dense_logits",
     "row_reduce", "inverse_cdf", "slimspec_head", "dense_head", "approx_scores",
     "topk_lowest_index", "specvocab_head", "softmax_t", "verify_greedy",
-    "verify_decide", "verify_sampling", "verify_batch", "theory",
+    "verify_decide", "verify_sampling", "verify_batch", "verify_lowrank_batch", "theory",
 ]

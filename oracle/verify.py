@@ -16,7 +16,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .head import inverse_cdf
+from .head import inverse_cdf, up_projection
 
 
 def softmax_t(logits_row, temperature: float) -> np.ndarray:
@@ -100,3 +100,17 @@ def verify_batch(target, draft, draft_tokens, u, temperature: float):
         out[b, :len(toks)] = toks
         nacc[b] = n
     return out, nacc
+
+
+def verify_lowrank_batch(target, z, w_up, draft_tokens, u, temperature: float):
+    """Sampling verification when the draft distributions come from the
+    low-rank drafter head itself (SlimSpec article, section 三: the drafter's
+    scores are z W_up^T over the full vocabulary; explainer, section
+    "为什么答案不会变": the accept test and the residual need q at each
+    position).  z (B, gamma, r) holds the drafter's intermediate rows (the
+    bf16-rounded values the head multiplied), w_up (V, r).  The draft rows are
+    q_j = softmax(z_j W_up^T / T); everything else is verify_batch.
+    """
+    B, g, _ = z.shape
+    draft = np.stack([up_projection(z[b], w_up) for b in range(B)])
+    return verify_batch(target, draft, draft_tokens, u, temperature)

@@ -162,3 +162,52 @@ def test_batch_padding_and_counts():
     for b in range(4):
         assert np.all(out[b, : n[b] + 1] >= 0)
         assert np.all(out[b, n[b] + 1:] == -1)
+
+
+# ----------------------------------------------- draft side from the head
+def test_lowrank_verify_reads_draft_rows_through_w_up():
+    """z rows that are unit vectors pick columns of W_up: the draft rows the
+    low-rank form sees are exactly those columns, so it must agree with the
+    plain verifier on those rows (a transposed or mis-indexed W_up fails)."""
+    rng = np.random.default_rng(21)
+    B, g, V, r, T = 5, 3, 40, 8, 0.8
+    target = rng.standard_normal((B, g + 1, V))
+    w_up = rng.standard_normal((V, r))
+    cols = rng.integers(0, r, (B, g))
+    z = np.zeros((B, g, r))
+    for b in range(B):
+        for j in range(g):
+            z[b, j, cols[b, j]] = 1.0
+    draft = np.stack([[w_up[:, cols[b, j]] for j in range(g)] for b in range(B)])
+    x = rng.integers(0, V, (B, g))
+    u = synth.uniforms(rng, (B, g + 1))
+    got = oracle.verify_lowrank_batch(target, z, w_up, x, u, T)
+    want = oracle.verify_batch(target, draft, x, u, T)
+    np.testing.assert_array_equal(got[0], want[0])
+    np.testing.assert_array_equal(got[1], want[1])
+    # scaling z scales the draft logits: at T the same as z / 2 at T / 2
+    got2 = oracle.verify_lowrank_batch(target * 0.5, z * 0.5, w_up, x, u, T * 0.5)
+    np.testing.assert_array_equal(got2[0], want[0])
+
+
+def test_lowrank_verify_draft_distribution_from_z():
+    """With W_up = I (r = V) and z = log q, the draft distributions the
+    low-rank form builds are q itself, at any temperature T applied to
+    z = T log q; its outcomes then match the plain verifier on log q rows."""
+    rng = np.random.default_rng(5)
+    B, g, V = 4, 2, 6
+    q = rng.dirichlet(np.ones(V), size=(B, g))
+    target = rng.standard_normal((B, g + 1, V))
+    x = rng.integers(0, V, (B, g))
+    u = synth.uniforms(rng, (B, g + 1))
+    w_up = np.eye(V)
+    for T in (0.5, 1.0, 2.0):
+        z = T * np.log(q)
+        for b in range(B):
+            for j in range(g):
+                qb = oracle.softmax_t(oracle.up_projection(z[b, j][None, :], w_up)[0], T)
+                np.testing.assert_allclose(qb, q[b, j], rtol=1e-12)
+        got = oracle.verify_lowrank_batch(target, z, w_up, x, u, T)
+        want = oracle.verify_batch(target, z, x, u, T)
+        np.testing.assert_array_equal(got[0], want[0])
+        np.testing.assert_array_equal(got[1], want[1])
