@@ -195,6 +195,40 @@ int spec_verify(const float* target_logits, const float* draft_logits,
                 cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * Sampling verification with the draft side taken from the low-rank head.
+ *
+ * [SlimSpec] section 三 (the drafter's scores are z W_up^T over the whole
+ * vocabulary) with [Explainer] "为什么答案不会变" (the accept test needs q(x),
+ * the residual draw needs the whole q row at the first rejection).  The
+ * same outcome as spec_verify with draft_logits = z W_up^T, but no draft row
+ * is read or needed: position j uses log q_j(x_j) and the row's log-sum-exp
+ * as the head reported them (slimspec_head_forward's out_logprob and
+ * out_row_lse, same T), and the one draft row a rejection needs is
+ * recomputed from its z row on the tensor cores.
+ *  target_logits B x (gamma+1) x V float32
+ *  z             the drafter's z rows, bf16, r wide (slimspec_head_forward's
+ *                out_z): the row of sequence b, position j starts at row
+ *                b * seq_stride + j * pos_stride (gamma x B head outputs:
+ *                seq_stride 1, pos_stride B; B x gamma: gamma, 1)
+ *  w_up          V x r bf16, the head's up-projection
+ *  draft_logprob, draft_lse   float32, indexed like the rows of z
+ *  draft_tokens  B x gamma int32 (checked on the device); uniforms B x (gamma+1)
+ *  temperature > 0; 1 <= gamma <= 32; r % 8 == 0, r <= 512; B <= 256;
+ *  V <= 524288; z, w_up and target_logits 16-byte aligned
+ *  out_tokens, out_num_accepted as for spec_verify.
+ * Returns SS_ERR_INVALID_ARG / SS_ERR_UNSUPPORTED / SS_ERR_WORKSPACE as
+ * spec_verify does; nothing is launched then.
+ * ------------------------------------------------------------------------ */
+size_t spec_verify_lowrank_workspace_size(int B, int gamma, int V, int r);
+
+int spec_verify_lowrank(const float* target_logits, const void* z, const void* w_up,
+                        const float* draft_logprob, const float* draft_lse, int seq_stride,
+                        int pos_stride, int r, const int32_t* draft_tokens, int B, int gamma,
+                        int V, float temperature, const float* uniforms, int32_t* out_tokens,
+                        int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * Instrumentation (no counterpart in the articles; used by the benchmark).
  *
  * ss_launch_count: kernels this library has launched in this process.

@@ -11,6 +11,7 @@ Public calls (same names as the C ABI):
     specvocab_head_forward  SpecVocab-style dynamic-vocabulary head
     ss_topk_rows            the top-k stage on its own
     spec_verify             greedy / sampling verification
+    spec_verify_lowrank     sampling verification with the draft side from the head
     ss_get_device_error     device error word (synchronises the stream)
 """
 from __future__ import annotations
@@ -25,9 +26,9 @@ __all__ = [
     "SS_OK", "SS_ERR_INVALID_ARG", "SS_ERR_UNSUPPORTED", "SS_ERR_WORKSPACE",
     "SS_ERR_CUDA", "SS_ERR_TIMEOUT", "SS_ERR_DEVICE_INDEX", "SlimspecError",
     "lib", "lib_path", "header_functions", "slimspec_head_forward",
-    "specvocab_head_forward", "ss_topk_rows", "spec_verify", "ss_get_device_error",
-    "slimspec_head_workspace_size", "specvocab_head_workspace_size",
-    "spec_verify_workspace_size", "ss_topk_workspace_size",
+    "specvocab_head_forward", "ss_topk_rows", "spec_verify", "spec_verify_lowrank",
+    "ss_get_device_error", "slimspec_head_workspace_size", "specvocab_head_workspace_size",
+    "spec_verify_workspace_size", "spec_verify_lowrank_workspace_size", "ss_topk_workspace_size",
 ]
 
 SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE = 0, 1, 2, 3
@@ -55,6 +56,9 @@ _SIGS = {
     "ss_topk_rows": (_i, [_vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "spec_verify_workspace_size": (_sz, [_i, _i, _i, _f]),
     "spec_verify": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "spec_verify_lowrank_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "spec_verify_lowrank": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _f, _vp,
+                                 _vp, _vp, _vp, _sz, _vp]),
     "ss_launch_count": (ctypes.c_longlong, []),
     "ss_profile_start": (_i, []),
     "ss_profile_stop": (_i, []),
@@ -147,6 +151,10 @@ def specvocab_head_workspace_size(M, d, d_prime, V, k) -> int:
 
 def spec_verify_workspace_size(B, gamma, V, temperature) -> int:
     return int(lib().spec_verify_workspace_size(B, gamma, V, float(temperature)))
+
+
+def spec_verify_lowrank_workspace_size(B, gamma, V, r) -> int:
+    return int(lib().spec_verify_lowrank_workspace_size(B, gamma, V, r))
 
 
 def ss_topk_workspace_size(M, V, k) -> int:
@@ -261,7 +269,35 @@ def spec_verify(target_logits, draft_logits, draft_tokens, temperature=0.0, unif
     return o
 
 
-N_KERNEL_KINDS = 12
+def spec_verify_lowrank(target_logits, z, w_up, draft_logprob, draft_lse, draft_tokens,
+                        temperature, uniforms, *, position_major=True, workspace=None, out=None,
+                        stream=None) -> dict:
+    """Sampling verification of B sequences with the draft side from the
+    low-rank head: target (B, g+1, V) fp32; z (g*B, r) bf16 in position-major
+    order (row j*B + b: g head calls of B rows), or (B*g, r) sequence-major
+    with position_major=False; draft_logprob, draft_lse fp32 in the same
+    order; w_up (V, r) bf16; draft_tokens (B, g) int32; uniforms (B, g+1)."""
+    B, g1, V = target_logits.shape
+    gamma = g1 - 1
+    r = z.shape[-1]
+    dev = target_logits.device
+    ss, sp = (1, B) if position_major else (gamma, 1)
+    o = dict(out or {})
+    if "tokens" not in o:
+        o["tokens"] = torch.empty(B, g1, dtype=torch.int32, device=dev)
+    if "num_accepted" not in o:
+        o["num_accepted"] = torch.empty(B, dtype=torch.int32, device=dev)
+    nbytes = spec_verify_lowrank_workspace_size(B, gamma, V, r)
+    ws = _workspace(nbytes, dev, workspace)
+    st = lib().spec_verify_lowrank(
+        _ptr(target_logits), _ptr(z), _ptr(w_up), _ptr(draft_logprob), _ptr(draft_lse), ss, sp,
+        r, _ptr(draft_tokens), B, gamma, V, float(temperature), _ptr(uniforms),
+        _ptr(o["tokens"]), _ptr(o["num_accepted"]), _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "spec_verify_lowrank")
+    return o
+
+
+N_KERNEL_KINDS = 13
 
 
 def launch_count() -> int:

@@ -228,6 +228,40 @@ size_t spec_verify_workspace_size(int B, int gamma, int V, float temperature) {
   return verify_ws_bytes(B, gamma, V, temperature > 0.f);
 }
 
+size_t spec_verify_lowrank_workspace_size(int B, int gamma, int V, int r) {
+  if (B < 0 || gamma < 1 || gamma > 32 || V <= 0 || r <= 0) return 0;
+  return verify_lowrank_ws_bytes(B, gamma, V, r);
+}
+
+int spec_verify_lowrank(const float* target_logits, const void* z, const void* w_up,
+                        const float* draft_logprob, const float* draft_lse, int seq_stride,
+                        int pos_stride, int r, const int32_t* draft_tokens, int B, int gamma,
+                        int V, float temperature, const float* uniforms, int32_t* out_tokens,
+                        int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream) {
+  if (B < 0 || gamma < 1 || gamma > 32 || V <= 0 || r <= 0 || seq_stride < 0 || pos_stride < 0 ||
+      !(temperature > 0.f) || !temp_ok(temperature))
+    return SS_ERR_INVALID_ARG;
+  if ((long long)B * (gamma + 1) * V >= (1LL << 40)) return SS_ERR_UNSUPPORTED;
+  if (V > 524288) return SS_ERR_UNSUPPORTED;  // the final draw scans at most 256 chunks
+  if ((long long)B * (gamma + 1) * ((V + 2047) / 2048) >= (1LL << 31)) return SS_ERR_UNSUPPORTED;
+  if (B == 0) return SS_OK;
+  if (!mma_plan(r, B, V).ok) return SS_ERR_UNSUPPORTED;  // the recompute: B <= 256, r <= 512
+  if (!target_logits || !z || !w_up || !draft_logprob || !draft_lse || !draft_tokens ||
+      !uniforms || !out_tokens || !out_num_accepted)
+    return SS_ERR_INVALID_ARG;
+  if (!aligned(target_logits, 16) || !aligned(z, 16) || !aligned(w_up, 16) ||
+      !aligned(draft_logprob, 4) || !aligned(draft_lse, 4) || !aligned(draft_tokens, 4) ||
+      !aligned(uniforms, 4) || !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4))
+    return SS_ERR_INVALID_ARG;
+  const size_t need = verify_lowrank_ws_bytes(B, gamma, V, r);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return SS_ERR_WORKSPACE;
+  return cuda_status(launch_verify_lowrank(target_logits, z, w_up, draft_logprob, draft_lse,
+                                           seq_stride, pos_stride, r, draft_tokens, B, gamma, V,
+                                           temperature, uniforms, out_tokens, out_num_accepted,
+                                           workspace, stream));
+}
+
 int spec_verify(const float* target_logits, const float* draft_logits, const int32_t* draft_tokens,
                 int B, int gamma, int V, float temperature, const float* uniforms,
                 int32_t* out_tokens, int32_t* out_num_accepted, void* workspace,

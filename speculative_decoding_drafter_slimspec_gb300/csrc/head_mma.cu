@@ -838,7 +838,7 @@ template <bool kSample, int kMode, bool kWide>
 static cudaError_t launch_mma_kps(const MmaPlan& p, const void* z, const CUtensorMap& tw,
                                   const CUtensorMap& tw2, int M, int r, int V, float c,
                                   const MmaPart& part, float* scores, unsigned* ctr,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, KernelKind kind) {
   auto kern = k_head_mma<kSample, kMode, kWide>;
   // the limit is set once per kernel: make it the largest size any plan asks for
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), kSmemCap);
@@ -853,7 +853,7 @@ static cudaError_t launch_mma_kps(const MmaPlan& p, const void* z, const CUtenso
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  ProfScope ps(kKHeadMma, st);
+  ProfScope ps(kind, st);
   return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint16_t*>(z), tw, tw2, M, p.mt, r,
                             V, p.kb, p.kps, p.wb, p.nst, c, p.n_tiles, part, scores, ctr,
                             error_word());
@@ -862,15 +862,17 @@ template <bool kSample, int kMode>
 static cudaError_t launch_mma_one(const MmaPlan& p, const void* z, const CUtensorMap& tw,
                                   const CUtensorMap& tw2, int M, int r, int V, float c,
                                   const MmaPart& part, float* scores, unsigned* ctr,
-                                  cudaStream_t st) {
+                                  cudaStream_t st, KernelKind kind) {
   if (p.kps > 1)
-    return launch_mma_kps<kSample, kMode, true>(p, z, tw, tw2, M, r, V, c, part, scores, ctr, st);
-  return launch_mma_kps<kSample, kMode, false>(p, z, tw, tw2, M, r, V, c, part, scores, ctr, st);
+    return launch_mma_kps<kSample, kMode, true>(p, z, tw, tw2, M, r, V, c, part, scores, ctr, st,
+                                                 kind);
+  return launch_mma_kps<kSample, kMode, false>(p, z, tw, tw2, M, r, V, c, part, scores, ctr, st,
+                                                kind);
 }
 
 cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up, int M, int r,
                             int V, float temperature, const MmaWork& w, const HeadOutputs& out,
-                            float* scores, unsigned* ctr, cudaStream_t st) {
+                            float* scores, unsigned* ctr, cudaStream_t st, KernelKind kind) {
   if (M <= 0) return cudaSuccess;
   // tw: the stages' map (2-D, or 4-D for wide stages); tw2: the 2-D map, for
   // a wide stage's ragged last K block
@@ -887,13 +889,13 @@ cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up
   const MmaPart part{w.pmax, w.psum, w.parg};
   cudaError_t e;
   if (scores != nullptr) {
-    e = launch_mma_one<false, 1>(p, z_ws, tw, tw2, M, r, V, c, part, scores, ctr, st);
+    e = launch_mma_one<false, 1>(p, z_ws, tw, tw2, M, r, V, c, part, scores, ctr, st, kind);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
   if (sample)
-    e = launch_mma_one<true, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st);
+    e = launch_mma_one<true, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st, kind);
   else
-    e = launch_mma_one<false, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st);
+    e = launch_mma_one<false, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st, kind);
   if (e != cudaSuccess) return e;
   // the per-row finish, launched to overlap the tail of the MMA grid
   cudaLaunchConfig_t cfg = {};

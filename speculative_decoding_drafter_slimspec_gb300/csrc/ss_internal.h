@@ -17,7 +17,8 @@ unsigned* error_word();
 // Kernel kinds known to the optional profiler (profile.cu).
 enum KernelKind {
   kKDownProj = 0, kKHeadStream, kKHeadFinish, kKVerifyRows, kKVerifyDecide, kKVerifyResid,
-  kKVerifyFinish, kKTopk, kKGather, kKCandFinish, kKHeadMma, kKVerifyFirst, kKindCount
+  kKVerifyFinish, kKTopk, kKGather, kKCandFinish, kKHeadMma, kKVerifyFirst, kKVerifyQRow,
+  kKindCount
 };
 
 // Counts one launch and, while profiling is on, brackets it with two events
@@ -125,10 +126,18 @@ constexpr int kMmaCtrs = 2;
 cudaError_t launch_head_mma(const MmaPlan& plan, const void* z_ws, const void* w_up, int M, int r,
                             int V, float temperature, const MmaWork& work,
                             const HeadOutputs& out, float* scores, unsigned* ctr,
-                            cudaStream_t st);
+                            cudaStream_t st, KernelKind kind = kKHeadMma);
 
 // ---------------------------------------------------------------- verify --
 size_t verify_ws_bytes(int B, int gamma, int V, bool sample);
+// Sampling verification with the low-rank draft side (see spec_verify_lowrank).
+size_t verify_lowrank_ws_bytes(int B, int gamma, int V, int r);
+cudaError_t launch_verify_lowrank(const float* target, const void* z, const void* w_up,
+                                  const float* logprob, const float* lse, int seq_stride,
+                                  int pos_stride, int r, const int32_t* tokens, int B, int gamma,
+                                  int V, float temperature, const float* uniforms,
+                                  int32_t* out_tokens, int32_t* out_nacc, void* ws,
+                                  cudaStream_t st);
 cudaError_t launch_verify(const float* target, const float* draft, const int32_t* tokens, int B,
                           int gamma, int V, float temperature, const float* uniforms,
                           int32_t* out_tokens, int32_t* out_nacc, void* ws, cudaStream_t st);

@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(256)
   const bool vec = (V & 3) == 0;
   const int g1 = gamma + 1;
   const int nt = j1 - j0 + 1;                                    // target rows per sequence
-  const int nd = kSample ? max(0, min(j1, gamma - 1) - j0 + 1) : 0;  // draft rows
+  const int nd = (kSample && draft != nullptr) ? max(0, min(j1, gamma - 1) - j0 + 1) : 0;
   const unsigned seq_units = (unsigned)(nt + nd) * (unsigned)n_chunks;
   const unsigned units = (unsigned)B * seq_units;  // < 2^31: checked by the host
   for (unsigned u = gw; u < units; u += nw) {
@@ -175,11 +175,25 @@ __device__ __forceinline__ RowState warp_row_state(int row, int n_chunks, const 
 // uniform (loaded apart from, and in parallel with, the partial merges).
 struct PosInputs {
   int x;
-  float lp, lq, u;
+  float lp, lq, u;  // lq: the draft logit at x, or (low-rank form) log q(x)
+};
+
+// Where the draft distribution of a drafted position comes from: its logits
+// (B x gamma x V rows), or -- the low-rank form -- the drafter head's own
+// outputs: log q(x), the row's log-sum-exp at T and its z row, with the
+// final draw's draft row recomputed as z W_up^T.
+struct DraftSide {
+  const float* rows;       // B x gamma x V draft logits, or nullptr (low-rank form)
+  const float* logprob;    // low-rank: log q_j(x_j) at T, entry b * ss + j * sp
+  const float* lse;        // low-rank: log sum_v exp(l_v / T), same indexing
+  const uint16_t* z;       // low-rank: z rows (bf16, r wide), same indexing
+  int ss, sp, r;           // low-rank: strides in rows (sequence, position) and rank
+  uint16_t* z_sel;         // low-rank workspace: the z row of each sequence's draw
+  unsigned* mma_ctr;       // low-rank workspace: tile counters of the recompute
 };
 template <bool kSample>
 __device__ __forceinline__ PosInputs load_position(const float* __restrict__ target,
-                                                   const float* __restrict__ draft,
+                                                   const DraftSide& ds,
                                                    const int32_t* __restrict__ tokens,
                                                    const float* __restrict__ uniforms, int b,
                                                    int j, int gamma, int V) {
@@ -187,9 +201,10 @@ __device__ __forceinline__ PosInputs load_position(const float* __restrict__ tar
   PosInputs in{tokens[(size_t)b * gamma + j], 0.f, 0.f, 0.f};
   if (kSample) {
     in.u = uniforms[(size_t)b * g1 + j];
+    if (ds.rows == nullptr) in.lq = ds.logprob[(size_t)b * ds.ss + (size_t)j * ds.sp];
     if (in.x >= 0 && in.x < V) {
       in.lp = target[((size_t)b * g1 + j) * V + in.x];
-      in.lq = draft[((size_t)b * gamma + j) * V + in.x];
+      if (ds.rows != nullptr) in.lq = ds.rows[((size_t)b * gamma + j) * V + in.x];
     }
   }
   return in;
@@ -199,13 +214,16 @@ __device__ __forceinline__ PosInputs load_position(const float* __restrict__ tar
 // (pmx, psum, parg) and, when sampling, draft row state (qmx, qsum): greedy
 // keeps the token iff it is the target argmax; sampling keeps it iff
 // u * q(x) < p(x).  An out-of-range token rejects.
+// (low-rank form: q(x) = exp(log q(x)) directly.)
 template <bool kSample>
 __device__ __forceinline__ bool position_accepts(const PosInputs& in, int V, float c, float pmx,
-                                                 float psum, int parg, float qmx, float qsum) {
+                                                 float psum, int parg, float qmx, float qsum,
+                                                 bool lowrank) {
   if (in.x < 0 || in.x >= V) return false;
   if (!kSample) return in.x == parg;
   const float px = __fdiv_rn(fast_exp2((in.lp - pmx) * c), psum);
-  const float qx = __fdiv_rn(fast_exp2((in.lq - qmx) * c), qsum);
+  const float qx = lowrank ? fast_exp2(in.lq * 1.4426950408889634f)
+                           : __fdiv_rn(fast_exp2((in.lq - qmx) * c), qsum);
   return in.u * qx < px;
 }
 
@@ -217,7 +235,7 @@ __device__ __forceinline__ bool position_accepts(const PosInputs& in, int V, flo
 // only for those sequences).
 template <bool kSample>
 __global__ void __launch_bounds__(96)
-    k_verify_first(const float* __restrict__ target, const float* __restrict__ draft,
+    k_verify_first(const float* __restrict__ target, DraftSide ds,
                    const int32_t* __restrict__ tokens, int B, int gamma, int V, float c,
                    int n_chunks, const float* __restrict__ vmax, const float* __restrict__ vsum,
                    const int* __restrict__ varg, const float* __restrict__ uniforms,
@@ -228,10 +246,10 @@ __global__ void __launch_bounds__(96)
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.x;
   if (warp == 2) {  // inputs that do not depend on the row pass
-    if (lane == 0) s_in = load_position<kSample>(target, draft, tokens, uniforms, b, 0, gamma, V);
+    if (lane == 0) s_in = load_position<kSample>(target, ds, tokens, uniforms, b, 0, gamma, V);
   }
   pdl_wait_producer();
-  if (warp == 0 || (kSample && warp == 1)) {
+  if (warp == 0 || (kSample && warp == 1 && ds.rows != nullptr)) {
     const int row = warp == 0 ? b * (gamma + 1) : B * (gamma + 1) + b * gamma;
     const RowState st = warp_row_state<kSample>(row, n_chunks, vmax, vsum, varg, c, lane);
     if (lane == 0) s_st[warp] = st;
@@ -239,9 +257,9 @@ __global__ void __launch_bounds__(96)
   __syncthreads();
   if (threadIdx.x == 0) {
     const RowState pt = s_st[0];
-    const RowState pq = kSample ? s_st[1] : row_state_empty();
-    seq_ok[b] = position_accepts<kSample>(s_in, V, c, pt.mx, pt.sum, pt.arg, pq.mx, pq.sum) ? 1
-                                                                                            : 0;
+    const RowState pq = (kSample && ds.rows != nullptr) ? s_st[1] : row_state_empty();
+    seq_ok[b] = position_accepts<kSample>(s_in, V, c, pt.mx, pt.sum, pt.arg, pq.mx, pq.sum,
+                                          ds.rows == nullptr) ? 1 : 0;
   }
 }
 
@@ -256,7 +274,7 @@ __global__ void __launch_bounds__(96)
 constexpr int kMaxGamma = 32;
 template <bool kSample>
 __global__ void __launch_bounds__(544)
-    k_verify_decide(const float* __restrict__ target, const float* __restrict__ draft,
+    k_verify_decide(const float* __restrict__ target, DraftSide ds,
                     const int32_t* __restrict__ tokens, int B, int gamma, int V, float c,
                     int n_chunks, const float* __restrict__ vmax, const float* __restrict__ vsum,
                     const int* __restrict__ varg, const float* __restrict__ uniforms,
@@ -271,10 +289,12 @@ __global__ void __launch_bounds__(544)
   const int b = blockIdx.x;
   const int g1 = gamma + 1;
   const int n_target_rows = B * g1;
-  const int rows = kSample ? g1 + gamma : g1;
+  const bool lowrank = kSample && ds.rows == nullptr;
+  const int rows = (kSample && !lowrank) ? g1 + gamma : g1;
+  if (lowrank && b == 0 && threadIdx.x < kMmaCtrs) ds.mma_ctr[threadIdx.x] = 0u;  // recompute's
   if (warp == n_merge) {
     if (lane < gamma) {
-      const PosInputs in = load_position<kSample>(target, draft, tokens, uniforms, b, lane, gamma, V);
+      const PosInputs in = load_position<kSample>(target, ds, tokens, uniforms, b, lane, gamma, V);
       if (in.x < 0 || in.x >= V) raise_error(err, kErrIndex);
       s_in[lane] = in;
     }
@@ -294,8 +314,8 @@ __global__ void __launch_bounds__(544)
       ok = seq_ok[b] != 0;
     else
       ok = position_accepts<kSample>(s_in[lane], V, c, s_mx[lane], s_sum[lane], s_arg[lane],
-                                     kSample ? s_mx[g1 + lane] : 0.f,
-                                     kSample ? s_sum[g1 + lane] : 1.f);
+                                     (kSample && !lowrank) ? s_mx[g1 + lane] : 0.f,
+                                     (kSample && !lowrank) ? s_sum[g1 + lane] : 1.f, lowrank);
   }
   const unsigned fail = __ballot_sync(0xFFFFFFFFu, lane < gamma && !ok);
   const int n = fail ? __ffs(fail) - 1 : gamma;
@@ -305,6 +325,14 @@ __global__ void __launch_bounds__(544)
     else if (i == n) t = kSample ? -1 : s_arg[n];
     out_tokens[(size_t)b * g1 + i] = t;
   }
+  if (lowrank) {
+    // the z row of the final draw's draft row (position n; any row when the
+    // draw is the bonus, whose weights do not use q), for the recompute
+    const size_t src = (size_t)b * ds.ss + (size_t)min(n, gamma - 1) * ds.sp;
+    const uint4* zs = reinterpret_cast<const uint4*>(ds.z + src * ds.r);
+    uint4* zd = reinterpret_cast<uint4*>(ds.z_sel + (size_t)b * ds.r);
+    for (int i = lane; i < ds.r / 8; i += 32) zd[i] = zs[i];
+  }
   if (lane == 0) {
     out_nacc[b] = n;
     if (kSample) {
@@ -313,8 +341,17 @@ __global__ void __launch_bounds__(544)
       in.mode = (n == gamma) ? 1 : 0;
       in.pmx = s_mx[n];
       in.pinv = __frcp_rn(s_sum[n]);
-      in.qmx = (n == gamma) ? 0.f : s_mx[g1 + n];
-      in.qinv = (n == gamma) ? 0.f : __frcp_rn(s_sum[g1 + n]);
+      if (n == gamma) {
+        in.qmx = 0.f;
+        in.qinv = 0.f;
+      } else if (lowrank) {
+        // q(v) = exp(l_v / T - lse) = 2^((l_v - lse T) c)
+        in.qmx = ds.lse[(size_t)b * ds.ss + (size_t)n * ds.sp] * (1.4426950408889634f / c);
+        in.qinv = 1.f;
+      } else {
+        in.qmx = s_mx[g1 + n];
+        in.qinv = __frcp_rn(s_sum[g1 + n]);
+      }
       info[b] = in;
     }
   }
@@ -334,8 +371,9 @@ __device__ __forceinline__ float final_weight(const VerifyInfo& in, int mode, fl
 // the chunk.  Residual rows are read with 16 x 16-byte loads of each of the
 // two rows in flight per lane; bonus rows come straight from the partials.
 __global__ void __launch_bounds__(256)
-    k_verify_resid(const float* __restrict__ target, const float* __restrict__ draft, int B,
-                   int gamma, int V, float c, int n_chunks, const float* __restrict__ vmax,
+    k_verify_resid(const float* __restrict__ target, const float* __restrict__ draft, int qs,
+                   int qp, int B, int gamma, int V, float c, int n_chunks,
+                   const float* __restrict__ vmax,
                    const float* __restrict__ vsum, const VerifyInfo* __restrict__ info,
                    float* __restrict__ rmass) {
   const int lane = threadIdx.x & 31;
@@ -356,7 +394,7 @@ __global__ void __launch_bounds__(256)
       }
     } else {
       const float* t = target + (size_t)trow * V;
-      const float* q = draft + ((size_t)b * gamma + in.n) * V;
+      const float* q = draft + ((size_t)b * qs + (size_t)in.n * qp) * V;
       const int lo = ch * kVChunk, hi = min(V, lo + kVChunk);
       if (vec) {
         const float4* t4 = reinterpret_cast<const float4*>(t);
@@ -392,8 +430,9 @@ __global__ void __launch_bounds__(256)
 constexpr int kMaxChunkRegs = 8;  // up to 256 chunks of 2048 floats: V <= 524288
 
 __global__ void __launch_bounds__(256)
-    k_verify_finish(const float* __restrict__ target, const float* __restrict__ draft, int B,
-                    int gamma, int V, float c, int n_chunks, const float* __restrict__ vmax,
+    k_verify_finish(const float* __restrict__ target, const float* __restrict__ draft, int qs,
+                    int qp, int B, int gamma, int V, float c, int n_chunks,
+                    const float* __restrict__ vmax,
                     const float* __restrict__ vsum, const VerifyInfo* __restrict__ info,
                     const float* __restrict__ rmass, const float* __restrict__ uniforms,
                     int32_t* __restrict__ out_tokens) {
@@ -444,7 +483,7 @@ __global__ void __launch_bounds__(256)
   const int ch = s_ch, mode = s_mode;
   const float resid = s_resid;
   const float* t = target + (size_t)trow * V;
-  const float* q = draft + ((size_t)b * gamma + in.n) * V;
+  const float* q = draft + ((size_t)b * qs + (size_t)in.n * qp) * V;
   const int lo = ch * kVChunk + tid * PER, hi = min(V, ch * kVChunk + kVChunk);
   float wv[PER];
   float my = 0.f;
@@ -500,9 +539,12 @@ __global__ void __launch_bounds__(256)
 }
 
 // -------------------------------------------------------------- host side --
-size_t verify_ws_bytes(int B, int gamma, int V, bool sample) {
+// Workspace of the verifier; `lowrank` adds the draw's z rows, their
+// recomputed draft rows and the recompute's tile counters, and drops the
+// draft rows' partials.
+static size_t ws_bytes(int B, int gamma, int V, bool sample, bool lowrank, int r) {
   const int n_chunks = (V + kVChunk - 1) / kVChunk;
-  const size_t rows = (size_t)B * (gamma + 1) + (sample ? (size_t)B * gamma : 0);
+  const size_t rows = (size_t)B * (gamma + 1) + ((sample && !lowrank) ? (size_t)B * gamma : 0);
   size_t s = 0;
   s += align256(rows * n_chunks * sizeof(float));       // vmax
   s += align256(rows * n_chunks * sizeof(float));       // vsum
@@ -510,7 +552,18 @@ size_t verify_ws_bytes(int B, int gamma, int V, bool sample) {
   s += align256((size_t)B * sizeof(VerifyInfo));        // info
   s += align256((size_t)B * n_chunks * sizeof(float));  // rmass
   s += align256((size_t)B * sizeof(int));               // seq_ok
+  if (lowrank) {
+    s += align256((size_t)B * r * 2);                   // z rows of the draws
+    s += align256((size_t)B * V * sizeof(float));       // their draft rows
+    s += align256(kMmaCtrs * sizeof(unsigned));         // recompute tile counters
+  }
   return s;
+}
+size_t verify_ws_bytes(int B, int gamma, int V, bool sample) {
+  return ws_bytes(B, gamma, V, sample, false, 0);
+}
+size_t verify_lowrank_ws_bytes(int B, int gamma, int V, int r) {
+  return ws_bytes(B, gamma, V, true, true, r);
 }
 
 namespace {
@@ -532,18 +585,21 @@ cudaError_t launch_pdl(Kern kern, int grid, int block, cudaStream_t st, Args... 
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, args...);
 }
-}  // namespace
 
-cudaError_t launch_verify(const float* target, const float* draft, const int32_t* tokens, int B,
-                          int gamma, int V, float temperature, const float* uniforms,
-                          int32_t* out_tokens, int32_t* out_nacc, void* ws, cudaStream_t st) {
+// Both forms: `ds.rows` (draft logits) or the low-rank draft side (with
+// `w_up`, the drafter's V x r up-projection, for the recompute).
+cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
+                        const int32_t* tokens, int B, int gamma, int V, float temperature,
+                        const float* uniforms, int32_t* out_tokens, int32_t* out_nacc, void* ws,
+                        cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
   const bool sample = temperature > 0.f;
+  const bool lowrank = sample && ds.rows == nullptr;
   const float c = sample ? (float)(1.4426950408889634 / (double)temperature) : 0.f;
   const int n_chunks = (V + kVChunk - 1) / kVChunk;
   const int g1 = gamma + 1;
   const int n_target_rows = B * g1;
-  const int n_rows = n_target_rows + (sample ? B * gamma : 0);
+  const int n_rows = n_target_rows + ((sample && !lowrank) ? B * gamma : 0);
   Carver cv(ws);
   float* vmax = cv.take<float>((size_t)n_rows * n_chunks);
   float* vsum = cv.take<float>((size_t)n_rows * n_chunks);
@@ -551,6 +607,12 @@ cudaError_t launch_verify(const float* target, const float* draft, const int32_t
   VerifyInfo* info = cv.take<VerifyInfo>(B);
   float* rmass = cv.take<float>((size_t)B * n_chunks);
   int* seq_ok = cv.take<int>(B);
+  float* q_rows = nullptr;
+  if (lowrank) {
+    ds.z_sel = cv.take<uint16_t>((size_t)B * ds.r);
+    q_rows = cv.take<float>((size_t)B * V);
+    ds.mma_ctr = cv.take<unsigned>(kMmaCtrs);
+  }
   const bool split = (double)n_rows * V * 4.0 >= kSplitBytes;
 
   // one warp per unit; the grid is what fits on the GPU at once (one wave)
@@ -558,9 +620,10 @@ cudaError_t launch_verify(const float* target, const float* draft, const int32_t
   const void* rows_kern = sample ? reinterpret_cast<const void*>(k_verify_rows<true>)
                                  : reinterpret_cast<const void*>(k_verify_rows<false>);
   const long long cap = (long long)resident_blocks(rows_kern, kThr, 0) * sm_count();
+  const float* draft = ds.rows;
   auto rows_pass = [&](int j0, int j1, const int* ok, bool pdl) -> cudaError_t {
     const int nt = j1 - j0 + 1;
-    const int nd = sample ? std::max(0, std::min(j1, gamma - 1) - j0 + 1) : 0;
+    const int nd = (sample && draft) ? std::max(0, std::min(j1, gamma - 1) - j0 + 1) : 0;
     const long long units = (long long)B * (nt + nd) * n_chunks;
     const int grid = (int)std::max<long long>(1, std::min<long long>((units + 7) / 8, cap));
     ProfScope ps(kKVerifyRows, st);
@@ -584,10 +647,10 @@ cudaError_t launch_verify(const float* target, const float* draft, const int32_t
     if ((e = rows_pass(0, 0, nullptr, false)) != cudaSuccess) return e;
     {
       ProfScope ps(kKVerifyFirst, st);
-      e = sample ? launch_pdl(k_verify_first<true>, B, 96, st, target, draft, tokens, B, gamma,
+      e = sample ? launch_pdl(k_verify_first<true>, B, 96, st, target, ds, tokens, B, gamma,
                               V, c, n_chunks, (const float*)vmax, (const float*)vsum,
                               (const int*)varg, uniforms, seq_ok)
-                 : launch_pdl(k_verify_first<false>, B, 96, st, target, draft, tokens, B,
+                 : launch_pdl(k_verify_first<false>, B, 96, st, target, ds, tokens, B,
                               gamma, V, c, n_chunks, (const float*)vmax, (const float*)vsum,
                               (const int*)varg, uniforms, seq_ok);
       if (e != cudaSuccess) return e;
@@ -597,35 +660,77 @@ cudaError_t launch_verify(const float* target, const float* draft, const int32_t
     if ((e = rows_pass(0, gamma, nullptr, false)) != cudaSuccess) return e;
   }
   {
-    const int rows = sample ? 2 * gamma + 1 : gamma + 1;
+    const int rows = (sample && !lowrank) ? 2 * gamma + 1 : gamma + 1;
     const int dthreads = 32 * (std::min(16, rows) + 1);  // merging warps + a loading warp
     const int* ok = split ? seq_ok : nullptr;
     ProfScope ps(kKVerifyDecide, st);
-    e = sample ? launch_pdl(k_verify_decide<true>, B, dthreads, st, target, draft, tokens, B,
+    e = sample ? launch_pdl(k_verify_decide<true>, B, dthreads, st, target, ds, tokens, B,
                             gamma, V, c, n_chunks, (const float*)vmax, (const float*)vsum,
                             (const int*)varg, uniforms, ok, out_tokens, out_nacc, info,
                             error_word())
-               : launch_pdl(k_verify_decide<false>, B, dthreads, st, target, draft, tokens, B,
+               : launch_pdl(k_verify_decide<false>, B, dthreads, st, target, ds, tokens, B,
                             gamma, V, c, n_chunks, (const float*)vmax, (const float*)vsum,
                             (const int*)varg, uniforms, ok, out_tokens, out_nacc, info,
                             error_word());
     if (e != cudaSuccess) return e;
   }
   if (sample) {
+    int qs = gamma, qp = 1;
+    const float* qbase = draft;
+    if (lowrank) {
+      // the draft rows of the final draws, z W_up^T on the tensor cores
+      const MmaPlan mp = mma_plan(ds.r, B, V);
+      const MmaWork none{nullptr, nullptr, nullptr};
+      const HeadOutputs no_out{nullptr, nullptr, nullptr, nullptr, nullptr};
+      e = launch_head_mma(mp, ds.z_sel, w_up, B, ds.r, V, 0.f, none, no_out, q_rows, ds.mma_ctr,
+                          st, kKVerifyQRow);
+      if (e != cudaSuccess) return e;
+      qbase = q_rows;
+      qs = 1;
+      qp = 0;
+    }
     const long long ru = (long long)B * n_chunks;
     const long long rcap = (long long)resident_blocks(reinterpret_cast<const void*>(k_verify_resid),
                                                       256, 0) * sm_count();
     const int rgrid = (int)std::max<long long>(1, std::min<long long>((ru + 7) / 8, rcap));
     {
       ProfScope ps(kKVerifyResid, st);
-      k_verify_resid<<<rgrid, 256, 0, st>>>(target, draft, B, gamma, V, c, n_chunks, vmax, vsum,
-                                          info, rmass);
+      k_verify_resid<<<rgrid, 256, 0, st>>>(target, qbase, qs, qp, B, gamma, V, c, n_chunks,
+                                            vmax, vsum, info, rmass);
     }
     ProfScope ps(kKVerifyFinish, st);
-    k_verify_finish<<<B, 256, 0, st>>>(target, draft, B, gamma, V, c, n_chunks, vmax, vsum, info,
-                                       rmass, uniforms, out_tokens);
+    k_verify_finish<<<B, 256, 0, st>>>(target, qbase, qs, qp, B, gamma, V, c, n_chunks, vmax,
+                                       vsum, info, rmass, uniforms, out_tokens);
   }
   return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_verify(const float* target, const float* draft, const int32_t* tokens, int B,
+                          int gamma, int V, float temperature, const float* uniforms,
+                          int32_t* out_tokens, int32_t* out_nacc, void* ws, cudaStream_t st) {
+  DraftSide ds{};
+  ds.rows = draft;
+  return verify_impl(target, ds, nullptr, tokens, B, gamma, V, temperature, uniforms, out_tokens,
+                     out_nacc, ws, st);
+}
+
+cudaError_t launch_verify_lowrank(const float* target, const void* z, const void* w_up,
+                                  const float* logprob, const float* lse, int seq_stride,
+                                  int pos_stride, int r, const int32_t* tokens, int B, int gamma,
+                                  int V, float temperature, const float* uniforms,
+                                  int32_t* out_tokens, int32_t* out_nacc, void* ws,
+                                  cudaStream_t st) {
+  DraftSide ds{};
+  ds.rows = nullptr;
+  ds.logprob = logprob;
+  ds.lse = lse;
+  ds.z = reinterpret_cast<const uint16_t*>(z);
+  ds.ss = seq_stride;
+  ds.sp = pos_stride;
+  ds.r = r;
+  return verify_impl(target, ds, w_up, tokens, B, gamma, V, temperature, uniforms, out_tokens,
+                     out_nacc, ws, st);
 }
 
 }  // namespace ss

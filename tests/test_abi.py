@@ -98,6 +98,33 @@ def test_verify_argument_errors(lib):
     assert call(B=0) == ss.SS_OK
 
 
+def test_verify_lowrank_argument_errors(lib):
+    def call(B=2, g=3, V=104, r=64, T=1.0, ss_=1, sp=2, tgt=FAKE, z=FAKE, w=FAKE, lp=FAKE,
+             lse=FAKE, tok=FAKE, u=FAKE, ws=FAKE, wsb=1 << 24):
+        return lib.spec_verify_lowrank(tgt, z, w, lp, lse, ss_, sp, r, tok, B, g, V, T, u, FAKE,
+                                       FAKE, ws, wsb, NULL)
+    E = ss.SS_ERR_INVALID_ARG
+    assert call(T=0.0) == E                          # sampling only
+    assert call(T=float("inf")) == E
+    assert call(B=-1) == E
+    assert call(g=0) == E
+    assert call(g=33) == E
+    assert call(r=0) == E
+    assert call(ss_=-1) == E
+    assert call(z=NULL) == E
+    assert call(lse=NULL) == E
+    assert call(u=NULL) == E
+    assert call(z=MISAL) == E
+    assert call(w=MISAL) == E
+    assert call(r=12) == ss.SS_ERR_UNSUPPORTED        # r % 8 != 0: no recompute kernel
+    assert call(r=520) == ss.SS_ERR_UNSUPPORTED       # r > 512
+    assert call(B=300) == ss.SS_ERR_UNSUPPORTED       # B > 256
+    assert call(wsb=8) == ss.SS_ERR_WORKSPACE
+    assert call(B=0) == ss.SS_OK
+    assert lib.spec_verify_lowrank_workspace_size(16, 6, 201088, 360) > \
+        lib.spec_verify_lowrank_workspace_size(16, 6, 201088, 8)
+
+
 def test_specvocab_and_topk_argument_errors(lib):
     def sv(M=2, d=64, dp=16, V=100, k=10, T=0.0, ws=FAKE, wsb=1 << 24):
         return lib.specvocab_head_forward(FAKE, FAKE, FAKE, FAKE, M, d, dp, V, k, T, NULL, FAKE,

@@ -172,3 +172,140 @@ def test_verify_qwen30b_shape_sampling(sigma):
     # where neighbouring ids hold ~1e-7 of the mass each, may legitimately sit
     # on the other side of an fp32-vs-fp64 rounding boundary
     assert c["exact"] >= 0.8 * p.B
+
+
+# ------------------------------------------ draft side from the low-rank head
+def _lowrank_case(seed, B, g, V, r, T, sigma):
+    """z rows (position-major, g x B) and W_up with bf16 values, draft logits
+    z W_up^T, target = draft + N(0, sigma^2) at the drafted positions, tokens
+    drawn from q, and the head-side log q(x) and LSE (oracle values in fp32)."""
+    rng = np.random.default_rng(seed)
+    z = synth.normal(rng, (g, B, r), 1.0, "bf16")
+    w_up = synth.normal(rng, (V, r), 1.0 / np.sqrt(r), "bf16")
+    draft_pm = np.einsum("jbr,vr->jbv", z.astype(np.float64), w_up.astype(np.float64))
+    draft = np.ascontiguousarray(draft_pm.transpose(1, 0, 2))           # (B, g, V)
+    target = np.empty((B, g + 1, V), np.float32)
+    target[:, :g] = draft + sigma * rng.standard_normal((B, g, V))
+    target[:, g] = 2.0 * rng.standard_normal((B, V))
+    u_draft = synth.uniforms(rng, (B, g))
+    x = np.zeros((B, g), np.int32)
+    logprob = np.zeros((g, B), np.float32)
+    lse = np.zeros((g, B), np.float32)
+    for b in range(B):
+        for j in range(g):
+            rr = oracle.row_reduce(draft[b, j], T, u_draft[b, j])
+            x[b, j] = rr["token"]
+            logprob[j, b] = rr["logprob"]
+            lse[j, b] = rr["lse"]
+    u = synth.uniforms(rng, (B, g + 1))
+    z_seq = np.ascontiguousarray(z.transpose(1, 0, 2))                  # (B, g, r)
+    return dict(z=z, z_seq=z_seq, w_up=w_up, draft=draft, target=target, x=x, logprob=logprob,
+                lse=lse, u=u)
+
+
+def _run_lowrank(c, T, position_major=True):
+    g, B, r = c["z"].shape
+    if position_major:
+        z, lp, ls = c["z"].reshape(g * B, r), c["logprob"].reshape(-1), c["lse"].reshape(-1)
+    else:
+        z = c["z_seq"].reshape(B * g, r)
+        lp = np.ascontiguousarray(c["logprob"].T).reshape(-1)
+        ls = np.ascontiguousarray(c["lse"].T).reshape(-1)
+    o = ss.spec_verify_lowrank(to_dev(c["target"], "f32"), to_dev(z, "bf16"),
+                               to_dev(c["w_up"], "bf16"), to_dev(lp, "f32"), to_dev(ls, "f32"),
+                               to_dev(c["x"], "i32"), T, to_dev(c["u"], "f32"),
+                               position_major=position_major)
+    torch.cuda.synchronize()
+    assert ss.ss_get_device_error() == ss.SS_OK
+    return o["tokens"].cpu().numpy(), o["num_accepted"].cpu().numpy()
+
+
+def _check_lowrank(c, T, toks, nacc):
+    ref_t, ref_n = oracle.verify_lowrank_batch(c["target"], c["z_seq"], c["w_up"], c["x"], c["u"], T)
+    B = c["x"].shape[0]
+    counts = {"exact": 0, "boundary": 0}
+    for b in range(B):
+        n = int(nacc[b])
+        assert 0 <= n <= c["x"].shape[1]
+        assert np.all(toks[b, n + 1:] == -1)
+        verdict = check_verify_sampling(toks[b], n, c["target"][b], c["draft"][b], c["x"][b],
+                                        c["u"][b], T)
+        counts[verdict] += 1
+    same = int(np.sum(np.all(toks == ref_t, axis=1)))
+    return counts, same
+
+
+@pytest.mark.parametrize("V,r,T,sigma", [(1000, 64, 1.0, 0.3), (1001, 40, 0.7, 1.0),
+                                         (50000, 256, 1.0, 0.5), (20000, 360, 0.7, 2.0)])
+def test_verify_lowrank_matches_oracle(V, r, T, sigma):
+    """Draft side from z rows and W_up (ragged vocabularies, r not a multiple
+    of 64, close and far drafts): every outcome is one the oracle's decision
+    procedure allows, and almost all are the oracle's own."""
+    B, g = 16, 4
+    c = _lowrank_case(V + r, B, g, V, r, T, sigma)
+    toks, n = _run_lowrank(c, T)
+    counts, same = _check_lowrank(c, T, toks, n)
+    print("lowrank", V, r, T, sigma, counts, "identical rows", same, "accepted", n.tolist())
+    assert counts["exact"] >= B - 2 and same >= B - 2
+
+
+def test_verify_lowrank_sequence_major_rows():
+    """z, log q and LSE given sequence-major (B x gamma rows) give the same
+    outcome as position-major."""
+    c = _lowrank_case(9, 8, 3, 5000, 128, 1.0, 0.5)
+    a = _run_lowrank(c, 1.0, position_major=True)
+    b = _run_lowrank(c, 1.0, position_major=False)
+    np.testing.assert_array_equal(a[0], b[0])
+    np.testing.assert_array_equal(a[1], b[1])
+
+
+def test_verify_lowrank_split_path():
+    """Target rows above the split size (position 0 decided between two row
+    passes) with the low-rank draft side."""
+    B, g, V, r, T = 32, 4, 131072, 128, 1.0
+    assert B * (g + 1) * V * 4 >= 64 * 2 ** 20
+    c = _lowrank_case(31, B, g, V, r, T, 0.3)
+    toks, n = _run_lowrank(c, T)
+    counts, same = _check_lowrank(c, T, toks, n)
+    print("lowrank split", counts, "identical rows", same, "accepted", n.tolist())
+    assert counts["exact"] >= B - 2
+
+
+def test_verify_lowrank_after_head_calls():
+    """A whole sampling round on the GPU: gamma low-rank head calls produce
+    tokens, log q(x), LSE and z; the verifier consumes them as they are.
+    Outcomes are checked against the oracle fed the head's own z rows."""
+    B, g, d, r, V, T = 8, 3, 512, 128, 20000, 1.0
+    rng = np.random.default_rng(44)
+    inp = synth.head_inputs(44, M=B, d=d, r=r, V=V, dtype="bf16")
+    w_down, w_up = inp["w_down"], inp["w_up"]
+    hs = [synth.normal(rng, (B, d), 1.0, "bf16") for _ in range(g)]
+    u_head = synth.uniforms(rng, (g, B))
+    zs, lps, lses, toks = [], [], [], []
+    for j in range(g):
+        o = ss.slimspec_head_forward(to_dev(hs[j], "bf16"), to_dev(w_down, "bf16"),
+                                     to_dev(w_up, "bf16"), T, to_dev(u_head[j], "f32"),
+                                     want_stats=True, want_z=True)
+        zs.append(o["z"]); lps.append(o["logprob"]); lses.append(o["lse"]); toks.append(o["tokens"])
+    torch.cuda.synchronize()
+    z = torch.cat(zs).contiguous()                       # (g*B, r) position-major
+    lp = torch.cat(lps).contiguous()
+    ls = torch.cat(lses).contiguous()
+    x = torch.stack(toks, dim=1).contiguous()            # (B, g)
+    z_seq = z.float().cpu().numpy().reshape(g, B, r).transpose(1, 0, 2).copy()
+    draft = np.einsum("bjr,vr->bjv", z_seq.astype(np.float64), w_up.astype(np.float64))
+    target = np.empty((B, g + 1, V), np.float32)
+    target[:, :g] = draft + 0.5 * rng.standard_normal((B, g, V))
+    target[:, g] = rng.standard_normal((B, V))
+    u = synth.uniforms(rng, (B, g + 1))
+    o = ss.spec_verify_lowrank(to_dev(target, "f32"), z, to_dev(w_up, "bf16"), lp, ls, x, T,
+                               to_dev(u, "f32"))
+    torch.cuda.synchronize()
+    assert ss.ss_get_device_error() == ss.SS_OK
+    got_t, got_n = o["tokens"].cpu().numpy(), o["num_accepted"].cpu().numpy()
+    xn = x.cpu().numpy()
+    for b in range(B):
+        n = int(got_n[b])
+        assert np.all(got_t[b, :n] == xn[b, :n])
+        verdict = check_verify_sampling(got_t[b], n, target[b], draft[b], xn[b], u[b], T)
+        assert verdict is not None
