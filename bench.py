@@ -153,10 +153,15 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ workload -----
-def make_inputs(name: str, seed: int, dev):
+def make_inputs(name: str, seed: int, dev, lowrank: bool = False):
     """Seeded synthetic tensors on the device: bf16 weights N(0, 1/fan_in),
     hidden states N(0, 1), Zipf-like target logits (-1.1 ln rank over a random
-    permutation + N(0, 0.25)), draft logits = target + N(0, 1)."""
+    permutation + N(0, 0.25)), draft logits = target + N(0, 1).
+
+    lowrank (sampling workloads): the draft side is the head's own; the
+    target rows of the drafted positions are its draft logits z W_up^T
+    (computed here with torch, before timing) + N(0, 1), the bonus rows
+    Zipf-like, and every head call uses the same W_up (one drafter)."""
     import torch
     d, r, V, M, gamma, T = WORKLOADS[name]
     g = torch.Generator(device=dev)
@@ -187,9 +192,18 @@ def make_inputs(name: str, seed: int, dev):
     else:
         tokens = torch.argmax(draft, dim=2).to(torch.int32)
     u_verify = torch.rand(B, gamma + 1, generator=g, device=dev)
+    if lowrank:
+        # position-major rows j*B + b: gamma calls of B rows, or one call of gamma*B
+        del draft, tokens
+        z = torch.cat([(h.float() @ w_down.float().t()).to(torch.bfloat16) for h in hidden])
+        dl = (z.float() @ w_ups[0].float().t()).reshape(gamma, B, V)
+        target = target.clone()
+        target[:, :gamma] = dl.transpose(0, 1) + torch.randn(B, gamma, V, generator=g, device=dev)
+        del z, dl
+        draft, tokens = None, None
     return dict(name=name, d=d, r=r, V=V, M=M, B=B, gamma=gamma, T=T, n_calls=n_calls,
                 w_down=w_down, w_ups=w_ups, u_full=u_full, hidden=hidden, u_head=u_head,
-                target=target,
+                target=target, lowrank=lowrank,
                 draft=draft if T > 0 else None, tokens=tokens, u_verify=u_verify)
 
 
@@ -212,6 +226,19 @@ class Round:
                          for _ in range(x["n_calls"])]
         self.ver_out = {"tokens": torch.empty(B, gamma + 1, dtype=torch.int32, device=dev),
                         "num_accepted": torch.empty(B, dtype=torch.int32, device=dev)}
+        self.lowrank = x.get("lowrank", False)
+        if self.lowrank:
+            # the head calls' outputs, position-major, as the verifier reads them
+            n = gamma * B
+            self.lr = {"z": torch.empty(n, r, dtype=torch.bfloat16, device=dev),
+                       "logprob": torch.empty(n, dtype=torch.float32, device=dev),
+                       "lse": torch.empty(n, dtype=torch.float32, device=dev),
+                       "row_max": torch.empty(n, dtype=torch.float32, device=dev),
+                       "tokens": torch.empty(n, dtype=torch.int32, device=dev)}
+            self.head_out = [{k: v[j * M:(j + 1) * M] for k, v in self.lr.items()}
+                             for j in range(x["n_calls"])]
+            self.ver_ws = torch.empty(ss.spec_verify_lowrank_workspace_size(B, gamma, V, r),
+                                      dtype=torch.uint8, device=dev)
 
     def head_call(self, j, hidden, u):
         """Head call j of the round (the low-rank head or the SpecVocab head)."""
@@ -222,6 +249,10 @@ class Round:
                                              x["u_full"], SPECVOCAB_K, T, u if T > 0 else None,
                                              want_topk=False, workspace=self.head_ws,
                                              out=self.head_out[j])
+        if self.lowrank:
+            return ss.slimspec_head_forward(hidden, x["w_down"], x["w_ups"][0], T, u,
+                                            want_stats=True, want_z=True,
+                                            workspace=self.head_ws, out=self.head_out[j])
         return ss.slimspec_head_forward(hidden, x["w_down"], x["w_ups"][j % len(x["w_ups"])], T,
                                         u if T > 0 else None, want_stats=False,
                                         workspace=self.head_ws, out=self.head_out[j])
@@ -231,6 +262,12 @@ class Round:
         T = x["T"]
         for j in range(x["n_calls"]):
             self.head_call(j, x["hidden"][j], x["u_head"][j])
+        if self.lowrank:
+            lr = self.lr
+            ss.spec_verify_lowrank(x["target"], lr["z"], x["w_ups"][0], lr["logprob"], lr["lse"],
+                                   lr["tokens"], T, x["u_verify"], position_major=True,
+                                   workspace=self.ver_ws, out=self.ver_out)
+            return
         ss.spec_verify(x["target"], x["draft"], x["tokens"], T,
                        x["u_verify"] if T > 0 else None, workspace=self.ver_ws,
                        out=self.ver_out)
@@ -251,7 +288,7 @@ def verify_rows_read(x, num_accepted) -> int:
     least these; its roofline is taken against them."""
     n = num_accepted.to("cpu").long()
     rows = int((n + 1).sum())
-    if x["T"] > 0:
+    if x["T"] > 0 and not x.get("lowrank", False):
         rows += int((n + 1).clamp(max=x["gamma"]).sum())
     return rows
 
@@ -482,7 +519,10 @@ def run_ours(args, world, rank, local):
     __graft_entry__.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    x = make_inputs(args.workload, 1234 + rank, dev)
+    lowrank = args.verify == "lowrank"
+    if lowrank and (WORKLOADS[args.workload][5] <= 0 or args.workload == "specvocab8b"):
+        raise SystemExit("--verify lowrank needs a sampling low-rank workload (gptoss20b, qwen30b)")
+    x = make_inputs(args.workload, 1234 + rank, dev, lowrank=lowrank)
     rnd = Round(x, ss)
     stream = torch.cuda.Stream(device=dev)
     units_per_step = x["n_calls"] * x["M"]
@@ -551,7 +591,7 @@ def run_ours(args, world, rank, local):
     prof = {k: tuple(v) for k, v in prof.items()}
 
     # end to end through the public API with host buffers
-    e2e = run_e2e(args, x, ss, stream, world) if not args.no_e2e else None
+    e2e = run_e2e(args, x, ss, stream, world) if not (args.no_e2e or lowrank) else None
 
     if rank != 0:
         return
@@ -591,14 +631,16 @@ def run_ours(args, world, rank, local):
         ver_roof["launches_per_step"] = prof["k_verify_rows"][0] / n_prof
         ver_roof["rows_needed"] = ver_rows
         ver_roof["rows_total"] = x["B"] * (x["gamma"] + 1) + (
-            x["B"] * x["gamma"] if x["T"] > 0 else 0)
+            x["B"] * x["gamma"] if x["T"] > 0 and not x.get("lowrank", False) else 0)
     ver_ms = sum(ms for name, (n, ms) in prof.items() if name.startswith("k_verify")) / n_prof
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1000.0 / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic: seeded N(0,1/fan_in) bf16 weights, N(0,1) hidden states, "
                     "Zipf-like target logits",
-            "config": config_dict(args.workload), "roofline": roof,
+            "config": dict(config_dict(args.workload), **(
+                {"verify": "draft side from the head calls (z, log q, lse; spec_verify_lowrank), "
+                           "one W_up for all calls"} if lowrank else {})), "roofline": roof,
             "head_roofline": head_roof, "verify_roofline": ver_roof,
             "specvocab_union_rows": union_rows if x["u_full"] is not None else None,
             "gpu_launches": int(launches_per_step * args.steps),
@@ -701,6 +743,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama8b")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--verify", choices=["logits", "lowrank"], default="logits",
+                    help="lowrank: the verifier takes the draft side from the head calls "
+                         "(spec_verify_lowrank) instead of draft logits (sampling workloads)")
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -212,7 +212,8 @@ int spec_verify(const float* target_logits, const float* draft_logits,
  *                seq_stride 1, pos_stride B; B x gamma: gamma, 1)
  *  w_up          V x r bf16, the head's up-projection
  *  draft_logprob, draft_lse   float32, indexed like the rows of z
- *  draft_tokens  B x gamma int32 (checked on the device); uniforms B x (gamma+1)
+ *  draft_tokens  int32, indexed like the rows of z (checked on the device)
+ *  uniforms      B x (gamma+1) float32
  *  temperature > 0; 1 <= gamma <= 32; r % 8 == 0, r <= 512; B <= 256;
  *  V <= 524288; z, w_up and target_logits 16-byte aligned
  *  out_tokens, out_num_accepted as for spec_verify.

@@ -276,7 +276,8 @@ def spec_verify_lowrank(target_logits, z, w_up, draft_logprob, draft_lse, draft_
     low-rank head: target (B, g+1, V) fp32; z (g*B, r) bf16 in position-major
     order (row j*B + b: g head calls of B rows), or (B*g, r) sequence-major
     with position_major=False; draft_logprob, draft_lse fp32 in the same
-    order; w_up (V, r) bf16; draft_tokens (B, g) int32; uniforms (B, g+1)."""
+    order; w_up (V, r) bf16; draft_tokens int32 in the same order;
+    uniforms (B, g+1)."""
     B, g1, V = target_logits.shape
     gamma = g1 - 1
     r = z.shape[-1]

@@ -184,6 +184,7 @@ struct PosInputs {
 // final draw's draft row recomputed as z W_up^T.
 struct DraftSide {
   const float* rows;       // B x gamma x V draft logits, or nullptr (low-rank form)
+  int ts, tp;              // drafted token of (b, j) at tokens[b * ts + j * tp]
   const float* logprob;    // low-rank: log q_j(x_j) at T, entry b * ss + j * sp
   const float* lse;        // low-rank: log sum_v exp(l_v / T), same indexing
   const uint16_t* z;       // low-rank: z rows (bf16, r wide), same indexing
@@ -198,7 +199,7 @@ __device__ __forceinline__ PosInputs load_position(const float* __restrict__ tar
                                                    const float* __restrict__ uniforms, int b,
                                                    int j, int gamma, int V) {
   const int g1 = gamma + 1;
-  PosInputs in{tokens[(size_t)b * gamma + j], 0.f, 0.f, 0.f};
+  PosInputs in{tokens[(size_t)b * ds.ts + (size_t)j * ds.tp], 0.f, 0.f, 0.f};
   if (kSample) {
     in.u = uniforms[(size_t)b * g1 + j];
     if (ds.rows == nullptr) in.lq = ds.logprob[(size_t)b * ds.ss + (size_t)j * ds.sp];
@@ -321,7 +322,7 @@ __global__ void __launch_bounds__(544)
   const int n = fail ? __ffs(fail) - 1 : gamma;
   for (int i = lane; i < g1; i += 32) {
     int32_t t = -1;
-    if (i < n) t = tokens[(size_t)b * gamma + i];
+    if (i < n) t = tokens[(size_t)b * ds.ts + (size_t)i * ds.tp];
     else if (i == n) t = kSample ? -1 : s_arg[n];
     out_tokens[(size_t)b * g1 + i] = t;
   }
@@ -711,6 +712,8 @@ cudaError_t launch_verify(const float* target, const float* draft, const int32_t
                           int32_t* out_tokens, int32_t* out_nacc, void* ws, cudaStream_t st) {
   DraftSide ds{};
   ds.rows = draft;
+  ds.ts = gamma;
+  ds.tp = 1;
   return verify_impl(target, ds, nullptr, tokens, B, gamma, V, temperature, uniforms, out_tokens,
                      out_nacc, ws, st);
 }
@@ -728,6 +731,8 @@ cudaError_t launch_verify_lowrank(const float* target, const void* z, const void
   ds.z = reinterpret_cast<const uint16_t*>(z);
   ds.ss = seq_stride;
   ds.sp = pos_stride;
+  ds.ts = seq_stride;
+  ds.tp = pos_stride;
   ds.r = r;
   return verify_impl(target, ds, w_up, tokens, B, gamma, V, temperature, uniforms, out_tokens,
                      out_nacc, ws, st);

@@ -207,13 +207,15 @@ def _run_lowrank(c, T, position_major=True):
     g, B, r = c["z"].shape
     if position_major:
         z, lp, ls = c["z"].reshape(g * B, r), c["logprob"].reshape(-1), c["lse"].reshape(-1)
+        x = np.ascontiguousarray(c["x"].T).reshape(-1)
     else:
         z = c["z_seq"].reshape(B * g, r)
         lp = np.ascontiguousarray(c["logprob"].T).reshape(-1)
         ls = np.ascontiguousarray(c["lse"].T).reshape(-1)
+        x = c["x"].reshape(-1)
     o = ss.spec_verify_lowrank(to_dev(c["target"], "f32"), to_dev(z, "bf16"),
                                to_dev(c["w_up"], "bf16"), to_dev(lp, "f32"), to_dev(ls, "f32"),
-                               to_dev(c["x"], "i32"), T, to_dev(c["u"], "f32"),
+                               to_dev(x, "i32"), T, to_dev(c["u"], "f32"),
                                position_major=position_major)
     torch.cuda.synchronize()
     assert ss.ss_get_device_error() == ss.SS_OK
@@ -291,7 +293,7 @@ def test_verify_lowrank_after_head_calls():
     z = torch.cat(zs).contiguous()                       # (g*B, r) position-major
     lp = torch.cat(lps).contiguous()
     ls = torch.cat(lses).contiguous()
-    x = torch.stack(toks, dim=1).contiguous()            # (B, g)
+    x = torch.cat(toks).contiguous()                     # (g*B,) position-major
     z_seq = z.float().cpu().numpy().reshape(g, B, r).transpose(1, 0, 2).copy()
     draft = np.einsum("bjr,vr->bjv", z_seq.astype(np.float64), w_up.astype(np.float64))
     target = np.empty((B, g + 1, V), np.float32)
@@ -303,7 +305,7 @@ def test_verify_lowrank_after_head_calls():
     torch.cuda.synchronize()
     assert ss.ss_get_device_error() == ss.SS_OK
     got_t, got_n = o["tokens"].cpu().numpy(), o["num_accepted"].cpu().numpy()
-    xn = x.cpu().numpy()
+    xn = x.cpu().numpy().reshape(g, B).T.copy()
     for b in range(B):
         n = int(got_n[b])
         assert np.all(got_t[b, :n] == xn[b, :n])
