@@ -247,7 +247,10 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&v)[32], int vid0, int
 // each W_up tile is read by two CTAs; the second read mostly hits L2, and
 // each CTA keeps room for more W_up stages in flight than one holding both
 // tiles of z would.  kMode 0: softmax partials; kMode 1: the fp32 scores
-// D[m, v] are written to out_scores (M x V).  kWide false: a
+// D[m, v] are written to out_scores (M x V); kMode 2: the residual masses of
+// a verified sequence's final draw (ResidRow), the target values of each
+// tile loaded ahead of its accumulator, into part.pmax (residual) and
+// part.psum (p).  kWide false: a
 // W_up stage is one K block, a 2-D box of 128 rows x 128 bytes.  kWide true:
 // a stage is KPS K blocks -- WB full ones as one 4-D box of 128 rows x WB*128
 // contiguous bytes (every row's bytes of the stage in one request run: fewer
@@ -259,7 +262,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_head_mma(const uint16_t* __restrict__ z, const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ CUtensorMap tm_w2, int M, int m_tiles, int R, int V, int KB,
                int KPS, int WB, int NST, float c, int n_tiles, MmaPart part,
-               float* __restrict__ out_scores, unsigned* __restrict__ tile_ctr, unsigned* err) {
+               float* __restrict__ out_scores, const ResidRow* __restrict__ rrows,
+               unsigned* __restrict__ tile_ctr, unsigned* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -460,6 +464,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool warp_live = quad * 32 < Ml;   // any live row in this warp
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const int n_sub = 2 * n_tiles;
+    ResidRow rr{nullptr, 0.f, 0.f, 0.f, 1};
+    if (kMode == 2 && live) rr = rrows[row];
     for (int i = 0;; ++i) {
       const int slot = i % kTileRing;
       bool ok = mbar_wait_bounded(&tile_full[slot], (i / kTileRing) & 1, err);
@@ -468,6 +474,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0 && ok) mbar_arrive(&tile_empty[slot]);
       if (!__all_sync(0xFFFFFFFFu, ok) || t < 0) break;
       const int buf = i & 1;
+      // residual mode: this row's 64 target values of the tile, in flight
+      // while the accumulator is computed
+      float tv[kMode == 2 ? kSubW : 1];
+      if (kMode == 2 && live) {
+        const int v0 = t * kTileN + half * kSubW;
+        if ((V & 3) == 0 && v0 + kSubW <= V) {
+          const float4* tp = reinterpret_cast<const float4*>(rr.trow + v0);
+#pragma unroll
+          for (int j = 0; j < kSubW / 4; ++j) {
+            const float4 a = __ldcs(tp + j);
+            tv[4 * j] = a.x; tv[4 * j + 1] = a.y; tv[4 * j + 2] = a.z; tv[4 * j + 3] = a.w;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < kSubW; ++j) tv[j] = v0 + j < V ? __ldcs(rr.trow + v0 + j) : 0.f;
+        }
+      }
       ok = mbar_wait_bounded(&acc_full[buf], (i >> 1) & 1, err);
       if (!__all_sync(0xFFFFFFFFu, ok) || *(volatile int*)&s_abort) break;
       tc_fence_after();
@@ -482,8 +505,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32_issue(tmem + lane_addr + (uint32_t)(buf * kTileN + h * kSubW + cc * 32),
                             v2[cc]);
           tmem_ld_wait();
+          if (kMode == 2) {
+            // weights max(0, p - q) (mode 0) or p, and p alone, in four
+            // fixed-order partial sums each
+            const int vb = t * kTileN + h * kSubW;
+            float r4[4] = {0.f, 0.f, 0.f, 0.f}, p4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
+            for (int j = 0; j < kSubW; ++j) {
+              const float l = __uint_as_float(v2[j >> 5][j & 31]);
+              const float pv = fast_exp2((tv[j] - rr.pmx) * c) * rr.pinv;
+              const float w = rr.mode == 0 ? fmaxf(pv - fast_exp2((l - rr.qoff) * c), 0.f) : pv;
+              const bool in = vb + j < V;
+              r4[j & 3] = __fadd_rn(r4[j & 3], in ? w : 0.f);
+              p4[j & 3] = __fadd_rn(p4[j & 3], in ? pv : 0.f);
+            }
+            st.mx = __fadd_rn(__fadd_rn(r4[0], r4[1]), __fadd_rn(r4[2], r4[3]));
+            st.sum = __fadd_rn(__fadd_rn(p4[0], p4[1]), __fadd_rn(p4[2], p4[3]));
+          }
+#pragma unroll
+          for (int cc = 0; cc < (kMode == 2 ? 0 : 2); ++cc) {
             const int col = h * kSubW + cc * 32;
             const uint32_t (&v)[32] = v2[cc];
             const int vid0 = t * kTileN + col;
@@ -511,6 +551,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           part.pmax[o] = st.mx;
           part.parg[o] = st.arg;
           if (kSample) part.psum[o] = st.sum;
+        }
+        if (kMode == 2 && live) {
+          const size_t o = (size_t)row * n_sub + 2 * t + h;
+          part.pmax[o] = st.mx;   // residual mass of the sub-tile
+          part.psum[o] = st.sum;  // p mass of the sub-tile
         }
       }
       tc_fence_before();
@@ -838,7 +883,8 @@ template <bool kSample, int kMode, bool kWide>
 static cudaError_t launch_mma_kps(const MmaPlan& p, const void* z, const CUtensorMap& tw,
                                   const CUtensorMap& tw2, int M, int r, int V, float c,
                                   const MmaPart& part, float* scores, unsigned* ctr,
-                                  cudaStream_t st, KernelKind kind) {
+                                  cudaStream_t st, KernelKind kind,
+                                  const ResidRow* rrows = nullptr) {
   auto kern = k_head_mma<kSample, kMode, kWide>;
   // the limit is set once per kernel: make it the largest size any plan asks for
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), kSmemCap);
@@ -855,19 +901,43 @@ static cudaError_t launch_mma_kps(const MmaPlan& p, const void* z, const CUtenso
   cfg.numAttrs = 1;
   ProfScope ps(kind, st);
   return cudaLaunchKernelEx(&cfg, kern, reinterpret_cast<const uint16_t*>(z), tw, tw2, M, p.mt, r,
-                            V, p.kb, p.kps, p.wb, p.nst, c, p.n_tiles, part, scores, ctr,
+                            V, p.kb, p.kps, p.wb, p.nst, c, p.n_tiles, part, scores, rrows, ctr,
                             error_word());
 }
 template <bool kSample, int kMode>
 static cudaError_t launch_mma_one(const MmaPlan& p, const void* z, const CUtensorMap& tw,
                                   const CUtensorMap& tw2, int M, int r, int V, float c,
                                   const MmaPart& part, float* scores, unsigned* ctr,
-                                  cudaStream_t st, KernelKind kind) {
+                                  cudaStream_t st, KernelKind kind,
+                                  const ResidRow* rrows = nullptr) {
   if (p.kps > 1)
     return launch_mma_kps<kSample, kMode, true>(p, z, tw, tw2, M, r, V, c, part, scores, ctr, st,
-                                                 kind);
+                                                 kind, rrows);
   return launch_mma_kps<kSample, kMode, false>(p, z, tw, tw2, M, r, V, c, part, scores, ctr, st,
-                                                kind);
+                                                kind, rrows);
+}
+
+// The two tensor maps of W_up a plan needs: tw for the stages (2-D, or 4-D for
+// wide stages), tw2 the 2-D map for a wide stage's ragged last K block.
+static bool make_maps(const MmaPlan& p, const void* w_up, int V, int r, CUtensorMap* tw,
+                      CUtensorMap* tw2) {
+  if (!make_map(tw2, w_up, V, r)) return false;
+  if (p.kps > 1 && p.wb > 0) return make_map_wide(tw, w_up, V, r, p.wb);
+  *tw = *tw2;
+  return true;
+}
+
+cudaError_t launch_head_mma_resid(const MmaPlan& p, const void* z, const void* w_up, int B,
+                                  int r, int V, float temperature, const ResidRow* rows,
+                                  float* rmass, float* pmass, unsigned* ctr, cudaStream_t st) {
+  if (B <= 0) return cudaSuccess;
+  CUtensorMap tw, tw2;
+  if (!make_maps(p, w_up, V, r, &tw, &tw2)) return cudaErrorInvalidValue;
+  const float c = (float)(1.4426950408889634 / (double)temperature);
+  const MmaPart part{rmass, pmass, nullptr};
+  const cudaError_t e = launch_mma_one<false, 2>(p, z, tw, tw2, B, r, V, c, part, nullptr, ctr,
+                                                 st, kKVerifyQRow, rows);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up, int M, int r,

@@ -113,6 +113,21 @@ struct MmaPlan {
   bool ok;
 };
 MmaPlan mma_plan(int r, int M, int V);
+// A row of the tcgen05 up-projection's residual mode: the final draw of a
+// verified sequence whose draft row is z W_up^T.  For vocabulary row v with
+// target logit t_v and recomputed draft logit l_v: p(v) = 2^((t_v - pmx) c)
+// * pinv and q(v) = 2^((l_v - qoff) c); the row's weights are max(0, p - q)
+// (mode 0) or p (mode 1).
+struct ResidRow {
+  const float* trow;  // the target row of the final-draw position (V floats)
+  float pmx, pinv, qoff;
+  int mode;
+};
+// The residual mode's launch: per (row, 64-row sub-tile) the residual mass
+// (rmass) and the p mass (pmass), B x n_sub each.
+cudaError_t launch_head_mma_resid(const MmaPlan& plan, const void* z, const void* w_up, int B,
+                                  int r, int V, float temperature, const ResidRow* rows,
+                                  float* rmass, float* pmass, unsigned* ctr, cudaStream_t st);
 struct MmaWork {
   float* pmax;  // [M][n_sub]
   float* psum;

@@ -191,6 +191,7 @@ struct DraftSide {
   int ss, sp, r;           // low-rank: strides in rows (sequence, position) and rank
   uint16_t* z_sel;         // low-rank workspace: the z row of each sequence's draw
   unsigned* mma_ctr;       // low-rank workspace: tile counters of the recompute
+  ResidRow* rrows;         // low-rank workspace: each sequence's final draw for it
 };
 template <bool kSample>
 __device__ __forceinline__ PosInputs load_position(const float* __restrict__ target,
@@ -354,6 +355,9 @@ __global__ void __launch_bounds__(544)
         in.qinv = __frcp_rn(s_sum[g1 + n]);
       }
       info[b] = in;
+      if (lowrank)
+        ds.rrows[b] = ResidRow{target + ((size_t)b * g1 + n) * V, in.pmx, in.pinv, in.qmx,
+                               in.mode};
     }
   }
 }
@@ -539,10 +543,183 @@ __global__ void __launch_bounds__(256)
   }
 }
 
+// ------------------------------------------------------------------ K12 ----
+// The final draw of the low-rank draft side: one CTA of 256 threads per
+// sequence.  The tcgen05 residual mode left, per 64-row sub-tile, the mass of
+// max(0, p - q) and of p.  Thread j owns a contiguous run of sub-tiles; the
+// draw uses the residual masses (p's when the draw is the bonus or the
+// residual vanished), an ordered block scan finds the thread and then the
+// sub-tile holding u * W, whose 64 draft logits are recomputed on CUDA cores
+// from the sequence's z row (fp32 sums of the bf16 products) and walked in
+// order with its target values.
+constexpr int kLrPer = 24;  // sub-tile masses per thread: n_sub <= 6144
+__global__ void __launch_bounds__(256)
+    k_verify_lr_finish(const ResidRow* __restrict__ rows, const VerifyInfo* __restrict__ info,
+                       const uint8_t* __restrict__ w_up, const uint16_t* __restrict__ z_sel, int r,
+                       int V, float c, int n_sub, const float* __restrict__ rmass,
+                       const float* __restrict__ pmass, const float* __restrict__ uniforms,
+                       int gamma, int32_t* __restrict__ out_tokens) {
+  constexpr int NT = 256, kW = 64;
+  __shared__ float s_wsum[NT / 32], s_rsum[NT / 32];
+  __shared__ float s_w[kW];
+  __shared__ int s_first, s_last, s_sid;
+  __shared__ float s_resid;
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g1 = gamma + 1;
+  const ResidRow rr = rows[b];
+  const int n = info[b].n;
+  const float u = uniforms[(size_t)b * g1 + gamma];
+  const int per = (n_sub + NT - 1) / NT;
+  const int j0 = min(n_sub, tid * per), nj = min(n_sub, j0 + per) - j0;
+  float rm[kLrPer], pm[kLrPer];
+#pragma unroll
+  for (int k = 0; k < kLrPer; ++k) {
+    rm[k] = k < nj ? __ldcg(rmass + (size_t)b * n_sub + j0 + k) : 0.f;
+    pm[k] = k < nj ? __ldcg(pmass + (size_t)b * n_sub + j0 + k) : 0.f;
+  }
+  float mr = 0.f, mp = 0.f;
+#pragma unroll
+  for (int k = 0; k < kLrPer; ++k) {
+    mr = __fadd_rn(mr, rm[k]);
+    mp = __fadd_rn(mp, pm[k]);
+  }
+  // the residual's total decides which masses the draw uses
+  const float wr = warp_incl_scan(mr, lane);
+  if (lane == 31) s_rsum[warp] = wr;
+  if (tid == 0) { s_first = NT; s_last = -1; }
+  __syncthreads();
+  float R = 0.f;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) R = __fadd_rn(R, s_rsum[w]);
+  const bool use_p = rr.mode == 1 || !(R > 0.f);
+  const float mass = use_p ? mp : mr;
+  // ordered block scan of the thread masses
+  const float wincl = warp_incl_scan(mass, lane);
+  if (lane == 31) s_wsum[warp] = wincl;
+  __syncthreads();
+  float woff = 0.f, W = 0.f;
+#pragma unroll
+  for (int w = 0; w < NT / 32; ++w) {
+    if (w < warp) woff = __fadd_rn(woff, s_wsum[w]);
+    W = __fadd_rn(W, s_wsum[w]);
+  }
+  const float incl = __fadd_rn(woff, wincl);
+  const float prev = __shfl_up_sync(0xFFFFFFFFu, wincl, 1);
+  const float excl = lane > 0 ? __fadd_rn(woff, prev) : woff;
+  const float target = u * W;
+  // the first thread whose inclusive mass passes the target, else (rounding)
+  // the last thread with any mass
+  if (mass > 0.f) {
+    atomicMax(&s_last, tid);
+    if (incl > target) atomicMin(&s_first, tid);
+  }
+  __syncthreads();
+  const int sel = s_first < NT ? s_first : max(0, s_last);
+  if (tid == sel) {
+    float cum = excl, before_sid = excl, before_last = excl;
+    int sid = -1, lastpos = -1;
+#pragma unroll
+    for (int k = 0; k < kLrPer; ++k) {
+      const float mk = use_p ? pm[k] : rm[k];
+      if (k < nj && sid < 0) {
+        const float nxt = __fadd_rn(cum, mk);
+        if (mk > 0.f) {
+          if (nxt > target) {
+            sid = j0 + k;
+            before_sid = cum;
+          } else {
+            lastpos = j0 + k;
+            before_last = cum;
+          }
+        }
+        cum = nxt;
+      }
+    }
+    if (sid < 0) {
+      sid = lastpos >= 0 ? lastpos : j0;
+      before_sid = before_last;
+    }
+    s_sid = sid;
+    s_resid = target - before_sid;
+  }
+  __syncthreads();
+  const int v0 = s_sid * kW;
+  const int nv = max(0, min(kW, V - v0));
+  // recompute: warp w takes rows 8w .. 8w+7 of the sub-tile, lanes over K
+  const int nch = r / 8;  // <= 64: two 16-byte chunks per lane
+  uint4 zc[2], wv[8][2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int ch = lane + 32 * q;
+    zc[q] = ch < nch ? __ldg(reinterpret_cast<const uint4*>(z_sel + (size_t)b * r) + ch)
+                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int ii = 0; ii < 8; ++ii) {
+    const int i = warp * 8 + ii;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int ch = lane + 32 * q;
+      wv[ii][q] = (i < nv && ch < nch)
+                      ? __ldg(reinterpret_cast<const uint4*>(w_up + ((size_t)(v0 + i) * r) * 2) + ch)
+                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+  const float tv = (lane < 8 && warp * 8 + lane < nv) ? rr.trow[v0 + warp * 8 + lane] : 0.f;
+#pragma unroll
+  for (int ii = 0; ii < 8; ++ii) {
+    float a = 0.f;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t ww[4] = {wv[ii][q].x, wv[ii][q].y, wv[ii][q].z, wv[ii][q].w};
+      const uint32_t zz[4] = {zc[q].x, zc[q].y, zc[q].z, zc[q].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        a = fma_bf16_lo(ww[e], zz[e], a);
+        a = fma_bf16_hi(ww[e], zz[e], a);
+      }
+    }
+    a = warp_sum_fixed(a);
+    const float t = __shfl_sync(0xFFFFFFFFu, tv, ii);
+    if (lane == 0) {
+      const int i = warp * 8 + ii;
+      float w = 0.f;
+      if (i < nv) {
+        const float pv = fast_exp2((t - rr.pmx) * c) * rr.pinv;
+        w = use_p ? pv : fmaxf(pv - fast_exp2((a - rr.qoff) * c), 0.f);
+      }
+      s_w[i] = w;
+    }
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  const float resid = s_resid;
+  float cum = 0.f;
+  int tok = -1, lastp = -1;
+#pragma unroll
+  for (int h = 0; h < kW; h += 32) {
+    const float w1 = s_w[h + lane];
+    const float csum = __fadd_rn(cum, warp_incl_scan(w1, lane));
+    const unsigned pos = __ballot_sync(0xFFFFFFFFu, w1 > 0.f);
+    const unsigned hit = __ballot_sync(0xFFFFFFFFu, w1 > 0.f && csum > resid);
+    if (tok < 0 && hit) tok = h + __ffs(hit) - 1;
+    if (pos) lastp = h + 31 - __clz(pos);
+    cum = __shfl_sync(0xFFFFFFFFu, csum, 31);
+  }
+  if (tok < 0) tok = lastp < 0 ? 0 : lastp;
+  if (lane == 0) out_tokens[(size_t)b * g1 + n] = v0 + tok;
+}
+
 // -------------------------------------------------------------- host side --
-// Workspace of the verifier; `lowrank` adds the draw's z rows, their
-// recomputed draft rows and the recompute's tile counters, and drops the
-// draft rows' partials.
+// The low-rank draft side recomputes the final draws' draft rows either
+// reduced on the fly to sub-tile masses against the target rows (the
+// residual mode, from this many sequences on: with fewer rows per tile the
+// epilogue's target loads are not hidden), or written out for the residual
+// and finish kernels.
+constexpr int kFusedResidMinB = 32;
+
+// Workspace of the verifier; `lowrank` adds the draws' z rows, the
+// recompute's outputs and tile counters, and drops the draft rows' partials.
 static size_t ws_bytes(int B, int gamma, int V, bool sample, bool lowrank, int r) {
   const int n_chunks = (V + kVChunk - 1) / kVChunk;
   const size_t rows = (size_t)B * (gamma + 1) + ((sample && !lowrank) ? (size_t)B * gamma : 0);
@@ -554,9 +731,14 @@ static size_t ws_bytes(int B, int gamma, int V, bool sample, bool lowrank, int r
   s += align256((size_t)B * n_chunks * sizeof(float));  // rmass
   s += align256((size_t)B * sizeof(int));               // seq_ok
   if (lowrank) {
-    s += align256((size_t)B * r * 2);                   // z rows of the draws
-    s += align256((size_t)B * V * sizeof(float));       // their draft rows
-    s += align256(kMmaCtrs * sizeof(unsigned));         // recompute tile counters
+    const size_t n_sub = 2 * (size_t)((V + 127) / 128);  // 64-row sub-tiles of the recompute
+    s += align256((size_t)B * r * 2);                    // z rows of the draws
+    s += align256((size_t)B * sizeof(ResidRow));         // the draws
+    if (B >= kFusedResidMinB)
+      s += 2 * align256((size_t)B * n_sub * sizeof(float));  // residual and p masses
+    else
+      s += align256((size_t)B * V * sizeof(float));          // the recomputed draft rows
+    s += align256(kMmaCtrs * sizeof(unsigned));          // recompute tile counters
   }
   return s;
 }
@@ -608,10 +790,20 @@ cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
   VerifyInfo* info = cv.take<VerifyInfo>(B);
   float* rmass = cv.take<float>((size_t)B * n_chunks);
   int* seq_ok = cv.take<int>(B);
+  const int n_sub = 2 * ((V + 127) / 128);
+  const bool fused = lowrank && B >= kFusedResidMinB;
+  float* rm = nullptr;
+  float* pm = nullptr;
   float* q_rows = nullptr;
   if (lowrank) {
     ds.z_sel = cv.take<uint16_t>((size_t)B * ds.r);
-    q_rows = cv.take<float>((size_t)B * V);
+    ds.rrows = cv.take<ResidRow>(B);
+    if (fused) {
+      rm = cv.take<float>((size_t)B * n_sub);
+      pm = cv.take<float>((size_t)B * n_sub);
+    } else {
+      q_rows = cv.take<float>((size_t)B * V);
+    }
     ds.mma_ctr = cv.take<unsigned>(kMmaCtrs);
   }
   const bool split = (double)n_rows * V * 4.0 >= kSplitBytes;
@@ -675,11 +867,23 @@ cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
                             error_word());
     if (e != cudaSuccess) return e;
   }
+  if (fused) {
+    // the final draws' draft rows z W_up^T on the tensor cores, reduced on the
+    // fly to per-sub-tile residual and p masses against the target rows
+    const MmaPlan mp = mma_plan(ds.r, B, V);
+    e = launch_head_mma_resid(mp, ds.z_sel, w_up, B, ds.r, V, temperature, ds.rrows, rm, pm,
+                              ds.mma_ctr, st);
+    if (e != cudaSuccess) return e;
+    ProfScope ps(kKVerifyFinish, st);
+    k_verify_lr_finish<<<B, 256, 0, st>>>(ds.rrows, info, (const uint8_t*)w_up, ds.z_sel, ds.r,
+                                          V, c, n_sub, rm, pm, uniforms, gamma, out_tokens);
+    return cudaGetLastError();
+  }
   if (sample) {
     int qs = gamma, qp = 1;
     const float* qbase = draft;
     if (lowrank) {
-      // the draft rows of the final draws, z W_up^T on the tensor cores
+      // the final draws' draft rows z W_up^T on the tensor cores, written out
       const MmaPlan mp = mma_plan(ds.r, B, V);
       const MmaWork none{nullptr, nullptr, nullptr};
       const HeadOutputs no_out{nullptr, nullptr, nullptr, nullptr, nullptr};
