@@ -10,7 +10,8 @@ Sources (each function names the one it follows):
 
 * "SlimSpec article" -- 荷兰Nebius团队：给AI“起草员“瘦身，大模型推理速度提升5倍
   (mhpn.cn).  Section 三 defines the low-rank head (W_down: d -> r, W_up: r -> V,
-  cost O(r*d + V*r), r = d/8); section 四 the acceptance rate sum_x min(p, q).
+  cost O(r*d + V*r), r = d/8); section 四 the acceptance rate sum_x min(p, q);
+  section 二 static vocabulary trimming (FR-Spec, VocabTrim).
 * "SpecVocab write-up" -- 动态词汇推测加速大语言模型推理 (2kiu.com).  Sections
   2.2.1-2.2.3: h' = W_down h at d' = d/16, s = W_vocab h', k_t = topk(s, 2048),
   z' = U[k_t] h, q = softmax(z').  Section 3.3: verification still uses the full
@@ -43,7 +44,7 @@ and exact enumeration.  No function is "parity unpinned".
 """
 from .bf16 import round_to_bf16
 from .head import down_projection, up_projection, dense_logits, row_reduce, \
-    inverse_cdf, slimspec_head, dense_head
+    inverse_cdf, slimspec_head, dense_head, trimmed_head
 from .specvocab import approx_scores, topk_lowest_index, specvocab_head
 from .verify import softmax_t, verify_greedy, verify_decide, verify_sampling, verify_batch, \
     verify_lowrank_batch
@@ -51,7 +52,7 @@ from . import theory
 
 __all__ = [
     "round_to_bf16", "down_projection", "up_projection", "dense_logits",
-    "row_reduce", "inverse_cdf", "slimspec_head", "dense_head", "approx_scores",
+    "row_reduce", "inverse_cdf", "slimspec_head", "dense_head", "trimmed_head", "approx_scores",
     "topk_lowest_index", "specvocab_head", "softmax_t", "verify_greedy",
     "verify_decide", "verify_sampling", "verify_batch", "verify_lowrank_batch", "theory",
 ]

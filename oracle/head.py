@@ -109,3 +109,19 @@ def slimspec_head(hidden, w_down, w_up, dtype: str, temperature: float,
 def dense_head(hidden, w, temperature: float, u=None) -> dict:
     """The dense V x d head followed by the same reduction (comparison path)."""
     return _reduce_rows(dense_logits(hidden, w), temperature, u)
+
+
+def trimmed_head(hidden, w_kept, kept_ids, temperature: float, u=None) -> dict:
+    """Static vocabulary trimming (SlimSpec article, section 二: FR-Spec and
+    VocabTrim keep a fixed subset of the vocabulary and score only it): the
+    dense head over the kept rows w_kept (V' x d, the head rows of the kept
+    ids, in the kept order), the row reduction over those V' scores, and the
+    chosen kept row mapped back to its vocabulary id through kept_ids.  Ties
+    and the inverse-CDF order follow the kept order (ascending kept_ids make
+    that ascending vocabulary id).  Tokens outside the kept set are never
+    drafted.
+    """
+    out = _reduce_rows(dense_logits(hidden, w_kept), temperature, u)
+    out["kept_index"] = out["tokens"].copy()
+    out["tokens"] = np.asarray(kept_ids, np.int64)[out["tokens"]]
+    return out

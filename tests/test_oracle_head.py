@@ -144,3 +144,65 @@ def test_sampling_tends_to_argmax_as_t_to_zero():
     l = np.array([0.1, 3.0, 1.0, 2.9, -2.0])
     for u in np.linspace(0, 0.999, 50):
         assert oracle.row_reduce(l, 1e-3, u)["token"] == 1
+
+
+# ----------------------------------------------------- static trimmed head ---
+def test_trimmed_head_keeping_everything_is_the_dense_head():
+    """Every row kept in vocabulary order: the dense head itself."""
+    rng = np.random.default_rng(3)
+    M, d, V = 4, 16, 50
+    h = rng.standard_normal((M, d))
+    W = rng.standard_normal((V, d))
+    u = rng.random(M)
+    for T in (0.0, 0.7):
+        got = oracle.trimmed_head(h, W, np.arange(V), T, u if T > 0 else None)
+        want = oracle.dense_head(h, W, T, u if T > 0 else None)
+        np.testing.assert_array_equal(got["tokens"], want["tokens"])
+        np.testing.assert_allclose(got["lse"], want["lse"], rtol=1e-14)
+
+
+def test_trimmed_head_brute_force_over_the_kept_set():
+    """Small integer heads: the greedy token is, by exhaustive search over the
+    kept ids in kept order, the first kept id with the largest score; the
+    sampled token's cumulative weights straddle u (exact fractions); tokens
+    outside the kept set never appear, even when they hold the full head's
+    maximum."""
+    rng = np.random.default_rng(8)
+    M, d, V = 6, 5, 30
+    h = rng.integers(-3, 4, (M, d)).astype(np.float64)
+    W = rng.integers(-3, 4, (V, d)).astype(np.float64)
+    full = h @ W.T
+    kept = np.array(sorted(rng.choice(V, 12, replace=False)))
+    # for some rows the full head's best id is a dropped one
+    assert any(int(np.argmax(full[m])) not in set(kept.tolist()) for m in range(M))
+    got = oracle.trimmed_head(h, W[kept], kept, 0.0)
+    for m in range(M):
+        best_v, best_s = None, None
+        for i, v in enumerate(kept):
+            s = sum(int(h[m, k]) * int(W[v, k]) for k in range(d))
+            if best_s is None or s > best_s:
+                best_v, best_s = int(v), s
+        assert got["tokens"][m] == best_v
+        assert got["tokens"][m] in set(kept.tolist())
+    # sampling at T = 1 with rational weights 2^(score) on the kept set
+    u = np.array([Fraction(k, 7) for k in range(M)], dtype=object)
+    got = oracle.trimmed_head(h, W[kept], kept, 1.0, [float(x) for x in u])
+    for m in range(M):
+        s = [sum(int(h[m, k]) * int(W[v, k]) for k in range(d)) for v in kept]
+        mx = max(s)
+        w = [np.exp(si - mx) for si in s]
+        cum = np.cumsum(w) / np.sum(w)
+        i = int(np.nonzero(kept == got["tokens"][m])[0][0])
+        lo = cum[i - 1] if i > 0 else 0.0
+        assert lo - 1e-12 <= float(u[m]) < cum[i] + 1e-12
+
+
+def test_trimmed_head_kept_order_decides_ties():
+    """Two kept rows with equal scores: the one earlier in the kept order wins,
+    whatever their vocabulary ids."""
+    h = np.array([[1.0, 0.0]])
+    W = np.array([[2.0, 0.0], [2.0, 0.0], [1.0, 0.0]])   # kept rows, in kept order
+    got = oracle.trimmed_head(h, W, np.array([40, 7, 3]), 0.0)
+    assert got["tokens"][0] == 40
+    got = oracle.trimmed_head(h, W[[1, 0, 2]], np.array([7, 40, 3]), 0.0)
+    assert got["tokens"][0] == 7
