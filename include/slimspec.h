@@ -126,6 +126,30 @@ int slimspec_head_forward_noalloc(const void* hidden, const void* w_down, const 
                                   void* out_z, float* out_logits, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
+ * Static trimmed head: the dense head over a fixed subset of the vocabulary.
+ *
+ * [SlimSpec] section 二 (FR-Spec, VocabTrim: the drafter scores only a kept
+ * subset of the vocabulary).  logits = h W_kept^T over the V_kept kept rows,
+ * then the per-row reduction of slimspec_head_forward over those scores; the
+ * chosen kept row i is reported as the vocabulary id kept_ids[i].  Ties and
+ * the inverse-CDF order follow the kept rows' order (ascending kept_ids make
+ * that ascending vocabulary id); ids outside the kept set are never drafted.
+ *  hidden    M x d bf16;  w_kept  V_kept x d bf16 (the kept rows of the head)
+ *  kept_ids  V_kept int32 vocabulary ids (not checked)
+ *  d % 8 == 0; d <= 4096; h must fit in shared memory beside the W stages
+ *  (M <= 16 at d = 4096), else SS_ERR_UNSUPPORTED
+ *  outputs and uniforms as for slimspec_head_forward (logprob and lse over
+ *  the kept set).
+ * ------------------------------------------------------------------------ */
+size_t trimmed_head_workspace_size(int M, int d, int V_kept);
+
+int trimmed_head_forward(const void* hidden, const void* w_kept, const int32_t* kept_ids, int M,
+                         int d, int V_kept, float temperature, const float* uniforms,
+                         int32_t* out_tokens, float* out_logprob, float* out_row_max,
+                         float* out_row_lse, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
  * SpecVocab-style dynamic-vocabulary drafter head (bf16 only).
  *
  * [SpecVocab] sections 2.2.1-2.2.3:

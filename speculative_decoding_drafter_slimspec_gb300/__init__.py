@@ -12,6 +12,7 @@ Public calls (same names as the C ABI):
     ss_topk_rows            the top-k stage on its own
     spec_verify             greedy / sampling verification
     spec_verify_lowrank     sampling verification with the draft side from the head
+    trimmed_head_forward    dense head over a kept subset of the vocabulary
     ss_get_device_error     device error word (synchronises the stream)
 """
 from __future__ import annotations
@@ -29,6 +30,7 @@ __all__ = [
     "specvocab_head_forward", "ss_topk_rows", "spec_verify", "spec_verify_lowrank",
     "ss_get_device_error", "slimspec_head_workspace_size", "specvocab_head_workspace_size",
     "spec_verify_workspace_size", "spec_verify_lowrank_workspace_size", "ss_topk_workspace_size",
+    "trimmed_head_forward", "trimmed_head_workspace_size",
 ]
 
 SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE = 0, 1, 2, 3
@@ -57,6 +59,9 @@ _SIGS = {
     "spec_verify_workspace_size": (_sz, [_i, _i, _i, _f]),
     "spec_verify": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _sz, _vp]),
     "spec_verify_lowrank_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "trimmed_head_workspace_size": (_sz, [_i, _i, _i]),
+    "trimmed_head_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp,
+                                  _sz, _vp]),
     "spec_verify_lowrank": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _f, _vp,
                                  _vp, _vp, _vp, _sz, _vp]),
     "ss_launch_count": (ctypes.c_longlong, []),
@@ -155,6 +160,10 @@ def spec_verify_workspace_size(B, gamma, V, temperature) -> int:
 
 def spec_verify_lowrank_workspace_size(B, gamma, V, r) -> int:
     return int(lib().spec_verify_lowrank_workspace_size(B, gamma, V, r))
+
+
+def trimmed_head_workspace_size(M, d, V_kept) -> int:
+    return int(lib().trimmed_head_workspace_size(M, d, V_kept))
 
 
 def ss_topk_workspace_size(M, V, k) -> int:
@@ -295,6 +304,32 @@ def spec_verify_lowrank(target_logits, z, w_up, draft_logprob, draft_lse, draft_
         r, _ptr(draft_tokens), B, gamma, V, float(temperature), _ptr(uniforms),
         _ptr(o["tokens"]), _ptr(o["num_accepted"]), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "spec_verify_lowrank")
+    return o
+
+
+def trimmed_head_forward(hidden, w_kept, kept_ids, temperature=0.0, uniforms=None, *,
+                         want_stats=True, workspace=None, out=None, stream=None) -> dict:
+    """Dense head over the kept vocabulary rows w_kept (V_kept, d) bf16 with
+    their ids kept_ids (V_kept,) int32; hidden (M, d) bf16.  Returns 'tokens'
+    (vocabulary ids) and, with want_stats, 'logprob', 'row_max', 'lse' over
+    the kept set."""
+    M, d = hidden.shape
+    Vk = w_kept.shape[0]
+    dev = hidden.device
+    o = dict(out or {})
+    if "tokens" not in o:
+        o["tokens"] = torch.empty(M, dtype=torch.int32, device=dev)
+    if want_stats:
+        for k in ("logprob", "row_max", "lse"):
+            if k not in o:
+                o[k] = torch.empty(M, dtype=torch.float32, device=dev)
+    nbytes = trimmed_head_workspace_size(M, d, Vk)
+    ws = _workspace(nbytes, dev, workspace)
+    st = lib().trimmed_head_forward(
+        _ptr(hidden), _ptr(w_kept), _ptr(kept_ids), M, d, Vk, float(temperature), _ptr(uniforms),
+        _ptr(o["tokens"]), _ptr(o.get("logprob")), _ptr(o.get("row_max")), _ptr(o.get("lse")),
+        _ptr(ws), ws.numel(), _stream(stream))
+    _check(st, "trimmed_head_forward")
     return o
 
 

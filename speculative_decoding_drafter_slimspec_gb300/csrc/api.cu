@@ -104,6 +104,54 @@ static int head_check(int M, int d, int r, int V, int dtype) {
   return SS_OK;
 }
 
+// ----------------------------------------------------- static trimmed head --
+static size_t trimmed_ws_bytes(int M, int d, int Vk) {
+  const MmaPlan p = mma_plan(d, M, Vk);
+  if (!p.ok) return 0;
+  size_t s = 3 * align256((size_t)M * p.n_sub * sizeof(float));  // sub-tile partials
+  s += align256(kMmaCtrs * sizeof(unsigned));                     // tile counters
+  return s;
+}
+
+size_t trimmed_head_workspace_size(int M, int d, int V_kept) {
+  if (M <= 0 || d <= 0 || d % 8 != 0 || V_kept <= 0) return 0;
+  return trimmed_ws_bytes(M, d, V_kept);
+}
+
+int trimmed_head_forward(const void* hidden, const void* w_kept, const int32_t* kept_ids, int M,
+                         int d, int V_kept, float temperature, const float* uniforms,
+                         int32_t* out_tokens, float* out_logprob, float* out_row_max,
+                         float* out_row_lse, void* workspace, size_t workspace_bytes,
+                         cudaStream_t stream) {
+  if (M < 0 || d <= 0 || d % 8 != 0 || V_kept <= 0 || !temp_ok(temperature))
+    return SS_ERR_INVALID_ARG;
+  if ((long long)V_kept * d * 2 >= (1LL << 40)) return SS_ERR_UNSUPPORTED;
+  if (M == 0) return SS_OK;
+  if (!hidden || !w_kept || !kept_ids || !out_tokens) return SS_ERR_INVALID_ARG;
+  if (temperature > 0.f && (!uniforms || !aligned(uniforms, 4))) return SS_ERR_INVALID_ARG;
+  if (!aligned(hidden, 16) || !aligned(w_kept, 16) || !aligned(kept_ids, 4) ||
+      !aligned(out_tokens, 4) || (out_logprob && !aligned(out_logprob, 4)) ||
+      (out_row_max && !aligned(out_row_max, 4)) || (out_row_lse && !aligned(out_row_lse, 4)))
+    return SS_ERR_INVALID_ARG;
+  const MmaPlan mp = mma_plan(d, M, V_kept);
+  if (!mp.ok) return SS_ERR_UNSUPPORTED;  // h must fit in shared memory beside the W stages
+  const size_t need = trimmed_ws_bytes(M, d, V_kept);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return SS_ERR_WORKSPACE;
+  Carver cv(workspace);
+  MmaWork wk;
+  wk.pmax = cv.take<float>((size_t)M * mp.n_sub);
+  wk.psum = cv.take<float>((size_t)M * mp.n_sub);
+  wk.parg = cv.take<int>((size_t)M * mp.n_sub);
+  unsigned* ctr = cv.take<unsigned>(kMmaCtrs);
+  // the rows of h are the tensor-core kernel's z; its tile counters start at 0
+  cudaError_t e = cudaMemsetAsync(ctr, 0, kMmaCtrs * sizeof(unsigned), stream);
+  if (e != cudaSuccess) return cuda_status(e);
+  const HeadOutputs outs{uniforms, out_tokens, out_logprob, out_row_max, out_row_lse, kept_ids};
+  e = launch_head_mma(mp, hidden, w_kept, M, d, V_kept, temperature, wk, outs, nullptr, ctr,
+                      stream);
+  return cuda_status(e);
+}
+
 size_t slimspec_head_workspace_size(int M, int d, int r, int V, int dtype) {
   if (head_check(M, d, r, V, dtype) != SS_OK) return 0;
   return head_ws_bytes(M, r, V, dtype == SS_BF16);
@@ -246,7 +294,8 @@ int spec_verify_lowrank(const float* target_logits, const void* z, const void* w
   if (V > 524288) return SS_ERR_UNSUPPORTED;  // the final draw scans at most 256 chunks
   if ((long long)B * (gamma + 1) * ((V + 2047) / 2048) >= (1LL << 31)) return SS_ERR_UNSUPPORTED;
   if (B == 0) return SS_OK;
-  if (!mma_plan(r, B, V).ok) return SS_ERR_UNSUPPORTED;  // the recompute: B <= 256, r <= 512
+  // the recompute: B <= 256 rows; its finish holds a z row in two chunks per lane
+  if (r > 512 || !mma_plan(r, B, V).ok) return SS_ERR_UNSUPPORTED;
   if (!target_logits || !z || !w_up || !draft_logprob || !draft_lse || !draft_tokens ||
       !uniforms || !out_tokens || !out_num_accepted)
     return SS_ERR_INVALID_ARG;

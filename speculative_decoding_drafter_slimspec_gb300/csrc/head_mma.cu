@@ -657,7 +657,7 @@ __global__ void __launch_bounds__(kFinThreads)
   const float gmax = best.v;
   if (!kSample) {
     if (threadIdx.x == 0) {
-      out.tokens[m] = best.i;
+      out.tokens[m] = out.id_map != nullptr ? out.id_map[best.i] : best.i;
       if (out.logprob) out.logprob[m] = 0.f;
       if (out.row_max) out.row_max[m] = gmax;
       if (out.row_lse) out.row_lse[m] = gmax;
@@ -729,40 +729,48 @@ __global__ void __launch_bounds__(kFinThreads)
   const float resid = s_f[1];
   const int v0 = s_i[1] * kSubW;
   const int n = max(0, min(kSubW, V - v0));
-  // recompute: warp w takes rows 8w .. 8w+7 of the sub-tile, lanes over K
+  // recompute: warp w takes rows 8w .. 8w+7 of the sub-tile, lanes over K in
+  // groups of 64 16-byte chunks (every load of a group issued up front)
   const int nch = r / 8;
-  uint4 zc[2], wv[8][2];
+  float acc[8];
 #pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    const int ch = lane + 32 * q;
-    zc[q] = ch < nch ? __ldg(reinterpret_cast<const uint4*>(z + ((size_t)m * r + ch * 8) * 2))
-                     : make_uint4(0u, 0u, 0u, 0u);
-  }
-#pragma unroll
-  for (int ii = 0; ii < 8; ++ii) {
-    const int i = warp * 8 + ii;
+  for (int ii = 0; ii < 8; ++ii) acc[ii] = 0.f;
+  for (int c0 = 0; c0 < nch; c0 += 64) {
+    uint4 zc[2], wv[8][2];
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
-      const int ch = lane + 32 * q;
-      wv[ii][q] = (i < n && ch < nch) ? __ldg(reinterpret_cast<const uint4*>(
-                                            w_up + ((size_t)(v0 + i) * r + ch * 8) * 2))
-                                      : make_uint4(0u, 0u, 0u, 0u);
+      const int ch = c0 + lane + 32 * q;
+      zc[q] = ch < nch ? __ldg(reinterpret_cast<const uint4*>(z + ((size_t)m * r + ch * 8) * 2))
+                       : make_uint4(0u, 0u, 0u, 0u);
     }
-  }
 #pragma unroll
-  for (int ii = 0; ii < 8; ++ii) {
-    float a = 0.f;
+    for (int ii = 0; ii < 8; ++ii) {
+      const int i = warp * 8 + ii;
 #pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const uint32_t ww[4] = {wv[ii][q].x, wv[ii][q].y, wv[ii][q].z, wv[ii][q].w};
-      const uint32_t zz[4] = {zc[q].x, zc[q].y, zc[q].z, zc[q].w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        a = fma_bf16_lo(ww[e], zz[e], a);
-        a = fma_bf16_hi(ww[e], zz[e], a);
+      for (int q = 0; q < 2; ++q) {
+        const int ch = c0 + lane + 32 * q;
+        wv[ii][q] = (i < n && ch < nch) ? __ldg(reinterpret_cast<const uint4*>(
+                                              w_up + ((size_t)(v0 + i) * r + ch * 8) * 2))
+                                        : make_uint4(0u, 0u, 0u, 0u);
       }
     }
-    a = warp_sum_fixed(a);
+#pragma unroll
+    for (int ii = 0; ii < 8; ++ii) {
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t ww[4] = {wv[ii][q].x, wv[ii][q].y, wv[ii][q].z, wv[ii][q].w};
+        const uint32_t zz[4] = {zc[q].x, zc[q].y, zc[q].z, zc[q].w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          acc[ii] = fma_bf16_lo(ww[e], zz[e], acc[ii]);
+          acc[ii] = fma_bf16_hi(ww[e], zz[e], acc[ii]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int ii = 0; ii < 8; ++ii) {
+    const float a = warp_sum_fixed(acc[ii]);
     if (lane == 0) s_logit[warp * 8 + ii] = a;
   }
   __syncthreads();
@@ -783,7 +791,7 @@ __global__ void __launch_bounds__(kFinThreads)
   if (tok < 0) tok = lastp2 < 0 ? 0 : lastp2;
   if (lane == 0) {
     const float lW = logf(s_f[0]);
-    out.tokens[m] = v0 + tok;
+    out.tokens[m] = out.id_map != nullptr ? out.id_map[v0 + tok] : v0 + tok;
     if (out.logprob) out.logprob[m] = (s_logit[tok] - gmax) * inv_t - lW;
     if (out.row_max) out.row_max[m] = gmax;
     if (out.row_lse) out.row_lse[m] = gmax * inv_t + lW;
@@ -847,7 +855,7 @@ bool make_map_wide(CUtensorMap* map, const void* base, int rows, int cols, int w
 MmaPlan mma_plan(int r, int M, int V) {
   MmaPlan p{};
   p.ok = false;
-  if (M <= 0 || M > 2 * kTileM || r % 8 != 0 || r > 512) return p;  // finish: <= 2 chunks per lane
+  if (M <= 0 || M > 2 * kTileM || r % 8 != 0 || r > 4096) return p;
   p.mt = M <= kTileM ? 1 : 2;  // M tiles, one per CTA
   p.kb = (r + 63) / 64;
   const int a_bytes = z_bytes(std::min(M, kTileM), p.kb);  // the largest CTA's z

@@ -93,6 +93,7 @@ struct HeadOutputs {
   float* logprob;
   float* row_max;
   float* row_lse;
+  const int32_t* id_map;  // nullable: tokens are id_map[row of W_up] (a trimmed head)
 };
 cudaError_t launch_head_stream(const HeadPlan& plan, bool bf16, const void* w_up,
                                const void* z_ws, int M, int r, int V, float temperature,

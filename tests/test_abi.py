@@ -42,7 +42,8 @@ def test_workspace_sizes(lib):
     # (one partial per 64-row vocabulary sub-tile or finer)
     assert w >= 8 * 512 * 2 + 3 * 8 * 2004 * 4
     assert lib.slimspec_head_workspace_size(-1, 4096, 512, 128256, ss.SS_BF16) == 0
-    assert lib.slimspec_head_workspace_size(8, 4096, 2048, 128256, ss.SS_BF16) == 0  # r too wide
+    assert lib.slimspec_head_workspace_size(8, 4096, 2048, 128256, ss.SS_BF16) > 0   # tensor cores
+    assert lib.slimspec_head_workspace_size(8, 8192, 8192, 128256, ss.SS_BF16) == 0  # r too wide
     assert lib.spec_verify_workspace_size(16, 6, 201088, ctypes.c_float(0.7)) > 0
     assert lib.spec_verify_workspace_size(16, 0, 201088, ctypes.c_float(0.7)) == 0
     assert lib.specvocab_head_workspace_size(32, 4096, 256, 151936, 2048) >= 32 * 151936 * 4
@@ -73,7 +74,7 @@ def test_head_argument_errors(lib):
     assert _head(lib, tok=NULL) == E
     assert _head(lib, w_up=MISAL) == E
     assert _head(lib, T=1.0, u=NULL) == E           # sampling needs uniforms
-    assert _head(lib, r=4096) == ss.SS_ERR_UNSUPPORTED
+    assert _head(lib, r=8192) == ss.SS_ERR_UNSUPPORTED
     assert _head(lib, ws=NULL) == ss.SS_ERR_WORKSPACE
     assert _head(lib, wsb=16) == ss.SS_ERR_WORKSPACE
     assert _head(lib, ws=MISAL) == ss.SS_ERR_WORKSPACE
@@ -123,6 +124,24 @@ def test_verify_lowrank_argument_errors(lib):
     assert call(B=0) == ss.SS_OK
     assert lib.spec_verify_lowrank_workspace_size(16, 6, 201088, 360) > \
         lib.spec_verify_lowrank_workspace_size(16, 6, 201088, 8)
+
+
+def test_trimmed_head_argument_errors(lib):
+    def call(M=2, d=64, Vk=100, T=0.0, h=FAKE, w=FAKE, ids=FAKE, u=NULL, ws=FAKE, wsb=1 << 24):
+        return lib.trimmed_head_forward(h, w, ids, M, d, Vk, T, u, FAKE, NULL, NULL, NULL, ws,
+                                        wsb, NULL)
+    E = ss.SS_ERR_INVALID_ARG
+    assert call(M=-1) == E
+    assert call(d=12) == E
+    assert call(Vk=0) == E
+    assert call(ids=NULL) == E
+    assert call(T=1.0) == E                          # sampling needs uniforms
+    assert call(h=MISAL) == E
+    assert call(d=8192) == ss.SS_ERR_UNSUPPORTED     # beyond the tensor-core plan
+    assert call(M=64, d=4096) == ss.SS_ERR_UNSUPPORTED  # h does not fit beside the stages
+    assert call(wsb=8) == ss.SS_ERR_WORKSPACE
+    assert call(M=0) == ss.SS_OK
+    assert lib.trimmed_head_workspace_size(8, 4096, 32768) > 0
 
 
 def test_specvocab_and_topk_argument_errors(lib):

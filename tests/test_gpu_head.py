@@ -13,7 +13,7 @@ import torch
 import oracle
 import synth
 import speculative_decoding_drafter_slimspec_gb300 as ss
-from parity import check_head_tokens
+from parity import cdf_verdict, check_head_tokens, greedy_verdict
 from gpu_util import device, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -169,3 +169,43 @@ def test_head_qwen30b_shape_sampled_rows():
     toks = out["tokens"].cpu().numpy()[rows]
     check_head_tokens(toks, ref["logits"], p.temperature, u[rows], EPS_GREEDY["bf16"])
     np.testing.assert_allclose(out["lse"].cpu().numpy()[rows], ref["lse"], atol=2e-2, rtol=0)
+
+
+# ----------------------------------------------------- static trimmed head ---
+def _trimmed_case(seed, M, d, V, Vk, sorted_ids=True):
+    rng = np.random.default_rng(seed)
+    h = synth.normal(rng, (M, d), 1.0, "bf16")
+    W = synth.normal(rng, (V, d), 1.0 / np.sqrt(d), "bf16")
+    kept = rng.choice(V, Vk, replace=False)
+    if sorted_ids:
+        kept = np.sort(kept)
+    return h, W[kept], kept.astype(np.int32)
+
+
+@pytest.mark.parametrize("M,d,V,Vk,T,sorted_ids", [
+    (1, 4096, 128256, 32768, 0.0, True),      # FR-Spec-sized: 32K of Llama's 128K ids
+    (8, 4096, 128256, 32768, 1.0, True),
+    (16, 4096, 50000, 20000, 0.7, True),      # h at the shared-memory limit
+    (3, 512, 20000, 1001, 1.0, False),        # ragged kept count, unsorted ids
+    (5, 2880, 201088, 16384, 0.0, False),     # d not a multiple of 64
+])
+def test_trimmed_head_matches_oracle(M, d, V, Vk, T, sorted_ids):
+    h, Wk, kept = _trimmed_case(M + d + Vk, M, d, V, Vk, sorted_ids)
+    u = synth.uniforms(np.random.default_rng(5), (M,))
+    o = ss.trimmed_head_forward(to_dev(h, "bf16"), to_dev(Wk, "bf16"), to_dev(kept, "i32"), T,
+                                to_dev(u, "f32") if T > 0 else None)
+    torch.cuda.synchronize()
+    assert ss.ss_get_device_error() == ss.SS_OK
+    ref = oracle.trimmed_head(h, Wk, kept, T, u if T > 0 else None)
+    got = o["tokens"].cpu().numpy()
+    assert set(got.tolist()) <= set(kept.tolist())
+    pos = {int(v): i for i, v in enumerate(kept)}
+    for m in range(M):
+        j = pos[int(got[m])]
+        if T == 0:
+            assert greedy_verdict(j, ref["logits"][m], 2e-3) is not None
+        else:
+            w = np.exp((ref["logits"][m] - ref["logits"][m].max()) / T)
+            assert cdf_verdict(j, w, float(u[m])) is not None
+            assert abs(o["lse"].cpu().numpy()[m] - ref["lse"][m]) < 2e-3 * (1 + abs(ref["lse"][m]))
+    assert np.sum(got == ref["tokens"]) >= M - 1
