@@ -512,6 +512,51 @@ def config_dict(workload):
                   ">750 MB between re-reads; inputs larger than L2"}
 
 
+def trimmed_head_comparison(x, head_us, kept=32768):
+    """The static trimmed head (FR-Spec / VocabTrim form) on the same GPU: the
+    dense head over `kept` of the V vocabulary rows (d = 4096, bf16, the same
+    M rows, greedy), through this library's tensor-core kernel, two copies of
+    W_kept alternating so every call reads HBM."""
+    import torch
+    import speculative_decoding_drafter_slimspec_gb300 as ss
+    dev = x["w_down"].device
+    M, d, V = x["M"], x["d"], x["V"]
+    g = torch.Generator(device=dev)
+    g.manual_seed(98)
+    ws = [(torch.randn(kept, d, generator=g, device=dev) / d ** 0.5).to(torch.bfloat16)
+          for _ in range(2)]
+    ids = torch.sort(torch.randperm(V, generator=g, device=dev)[:kept]).values.to(torch.int32)
+    h = x["hidden"][0]
+    wsp = torch.empty(ss.trimmed_head_workspace_size(M, d, kept), dtype=torch.uint8, device=dev)
+    out = {"tokens": torch.empty(M, dtype=torch.int32, device=dev)}
+    stream = torch.cuda.Stream(device=dev)
+    with torch.cuda.stream(stream):
+        for j in range(4):
+            ss.trimmed_head_forward(h, ws[j % 2], ids, 0.0, want_stats=False, workspace=wsp,
+                                    out=out)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
+            for j in range(10):
+                ss.trimmed_head_forward(h, ws[j % 2], ids, 0.0, want_stats=False, workspace=wsp,
+                                        out=out)
+        for _ in range(3):
+            graph.replay()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(20):
+            graph.replay()
+        e1.record(stream)
+    stream.synchronize()
+    us = e0.elapsed_time(e1) * 1000.0 / 200
+    nbytes = kept * d * 2 + M * d * 2
+    return {"kernel": "k_head_mma over the kept rows (z = h, K = d) + k_head_mma_finish",
+            "kept_rows": kept, "us_per_call": us, "bytes": nbytes, "GB/s": nbytes / us / 1e3,
+            "low_rank_up_projection_us": head_us,
+            "note": "the low-rank head scores all V rows; the trimmed head never drafts the "
+                    f"{V - kept} dropped ids"}
+
+
 def run_ours(args, world, rank, local):
     import torch
     import speculative_decoding_drafter_slimspec_gb300 as ss
@@ -653,6 +698,8 @@ def run_ours(args, world, rank, local):
     if args.workload == "llama8b" and not args.no_dense:
         # the Llama-shaped configuration also names the dense 128256 x 4096 head
         line["dense_head"] = dense_head_comparison(
+            x, head_roof["us_per_launch"] if head_roof else None)
+        line["trimmed_head"] = trimmed_head_comparison(
             x, head_roof["us_per_launch"] if head_roof else None)
     if world == 1 and not args.no_cpu_baseline:
         x_np = numpy_inputs(x)
