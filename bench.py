@@ -153,7 +153,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------ workload -----
-def make_inputs(name: str, seed: int, dev, lowrank: bool = False):
+def make_inputs(name: str, seed: int, dev, lowrank: bool = False, head_ranks=None):
     """Seeded synthetic tensors on the device: bf16 weights N(0, 1/fan_in),
     hidden states N(0, 1), Zipf-like target logits (-1.1 ln rank over a random
     permutation + N(0, 0.25)), draft logits = target + N(0, 1).
@@ -161,7 +161,10 @@ def make_inputs(name: str, seed: int, dev, lowrank: bool = False):
     lowrank (sampling workloads): the draft side is the head's own; the
     target rows of the drafted positions are its draft logits z W_up^T
     (computed here with torch, before timing) + N(0, 1), the bonus rows
-    Zipf-like, and every head call uses the same W_up (one drafter)."""
+    Zipf-like, and every head call uses the same W_up (one drafter).
+
+    head_ranks (low-rank workloads): head call j uses its own pair W_down_j
+    (r_j x d) and W_up_j (V x r_j), a rank per drafted position."""
     import torch
     d, r, V, M, gamma, T = WORKLOADS[name]
     g = torch.Generator(device=dev)
@@ -172,6 +175,13 @@ def make_inputs(name: str, seed: int, dev, lowrank: bool = False):
     # the low-rank head's W_up, or SpecVocab's router matrix W_vocab (V x d')
     w_ups = [(torch.randn(V, r, generator=g, device=dev) / r ** 0.5).to(torch.bfloat16)
              for _ in range(n_copies)]
+    w_downs = None
+    if head_ranks:
+        w_downs = [(torch.randn(rj, d, generator=g, device=dev) / d ** 0.5).to(torch.bfloat16)
+                   for rj in head_ranks]
+        w_ups = [(torch.randn(V, rj, generator=g, device=dev) / rj ** 0.5).to(torch.bfloat16)
+                 for rj in head_ranks]
+        r = int(round(sum(head_ranks) / len(head_ranks)))  # mean rank: bytes per call on average
     # SpecVocab's full head U (V x d, 1.2 GB: one copy, each call gathers its own rows)
     u_full = ((torch.randn(V, d, generator=g, device=dev) / d ** 0.5).to(torch.bfloat16)
               if name == "specvocab8b" else None)
@@ -203,7 +213,7 @@ def make_inputs(name: str, seed: int, dev, lowrank: bool = False):
         draft, tokens = None, None
     return dict(name=name, d=d, r=r, V=V, M=M, B=B, gamma=gamma, T=T, n_calls=n_calls,
                 w_down=w_down, w_ups=w_ups, u_full=u_full, hidden=hidden, u_head=u_head,
-                target=target, lowrank=lowrank,
+                target=target, lowrank=lowrank, w_downs=w_downs, ranks=head_ranks,
                 draft=draft if T > 0 else None, tokens=tokens, u_verify=u_verify)
 
 
@@ -217,8 +227,9 @@ class Round:
         dev = x["w_down"].device
         M, d, r, V, B, gamma = x["M"], x["d"], x["r"], x["V"], x["B"], x["gamma"]
         self.specvocab = x["u_full"] is not None
+        r_max = max(x["ranks"]) if x.get("ranks") else r
         hw = (ss.specvocab_head_workspace_size(M, d, r, V, SPECVOCAB_K) if self.specvocab
-              else ss.slimspec_head_workspace_size(M, d, r, V, ss.SS_BF16))
+              else ss.slimspec_head_workspace_size(M, d, r_max, V, ss.SS_BF16))
         self.head_ws = torch.empty(hw, dtype=torch.uint8, device=dev)
         self.ver_ws = torch.empty(max(256, ss.spec_verify_workspace_size(B, gamma, V, x["T"])),
                                   dtype=torch.uint8, device=dev)
@@ -253,7 +264,8 @@ class Round:
             return ss.slimspec_head_forward(hidden, x["w_down"], x["w_ups"][0], T, u,
                                             want_stats=True, want_z=True,
                                             workspace=self.head_ws, out=self.head_out[j])
-        return ss.slimspec_head_forward(hidden, x["w_down"], x["w_ups"][j % len(x["w_ups"])], T,
+        w_down = x["w_downs"][j] if x.get("w_downs") else x["w_down"]
+        return ss.slimspec_head_forward(hidden, w_down, x["w_ups"][j % len(x["w_ups"])], T,
                                         u if T > 0 else None, want_stats=False,
                                         workspace=self.head_ws, out=self.head_out[j])
 
@@ -567,7 +579,12 @@ def run_ours(args, world, rank, local):
     lowrank = args.verify == "lowrank"
     if lowrank and (WORKLOADS[args.workload][5] <= 0 or args.workload == "specvocab8b"):
         raise SystemExit("--verify lowrank needs a sampling low-rank workload (gptoss20b, qwen30b)")
-    x = make_inputs(args.workload, 1234 + rank, dev, lowrank=lowrank)
+    ranks = [int(v) for v in args.ranks.split(",")] if args.ranks else None
+    if ranks and (args.workload in ("specvocab8b", "qwen30b") or lowrank or
+                  len(ranks) != WORKLOADS[args.workload][4]):
+        raise SystemExit("--ranks needs one rank per head call of a low-rank workload "
+                         "(gamma calls), without --verify lowrank")
+    x = make_inputs(args.workload, 1234 + rank, dev, lowrank=lowrank, head_ranks=ranks)
     rnd = Round(x, ss)
     stream = torch.cuda.Stream(device=dev)
     units_per_step = x["n_calls"] * x["M"]
@@ -685,7 +702,8 @@ def run_ours(args, world, rank, local):
                     "Zipf-like target logits",
             "config": dict(config_dict(args.workload), **(
                 {"verify": "draft side from the head calls (z, log q, lse; spec_verify_lowrank), "
-                           "one W_up for all calls"} if lowrank else {})), "roofline": roof,
+                           "one W_up for all calls"} if lowrank else {}),
+                **({"ranks_per_position": ranks} if ranks else {})), "roofline": roof,
             "head_roofline": head_roof, "verify_roofline": ver_roof,
             "specvocab_union_rows": union_rows if x["u_full"] is not None else None,
             "gpu_launches": int(launches_per_step * args.steps),
@@ -790,6 +808,9 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama8b")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--ranks", default=None,
+                    help="comma-separated rank per drafted position (one head per position), "
+                         "e.g. 768,640,512,512,384,256")
     ap.add_argument("--verify", choices=["logits", "lowrank"], default="logits",
                     help="lowrank: the verifier takes the draft side from the head calls "
                          "(spec_verify_lowrank) instead of draft logits (sampling workloads)")

@@ -862,8 +862,10 @@ MmaPlan mma_plan(int r, int M, int V) {
   const int room = kSmemCap - 1024 - a_bytes;
   // wide stages (several K blocks per request run of each row) when the 4-D
   // view is exact (V % 8 == 0) and z leaves room for two of them: 4 K blocks
-  // when r is a multiple of 256, else a whole tile of up to 6 K blocks (the
-  // full ones by 4-D box, a ragged last one by 2-D box)
+  // when r is a multiple of 256; else a whole tile of up to 6 K blocks (the
+  // full ones by 4-D box, a ragged last one by 2-D box); else, when r is a
+  // multiple of 64, the largest count of 5 .. 2 full K blocks that divides
+  // the tile
   p.kps = 1;
   p.wb = 0;
   if (V % 8 == 0) {
@@ -873,6 +875,13 @@ MmaPlan mma_plan(int r, int M, int V) {
     } else if (p.kb <= 6 && r >= 64 && room / (p.kb * kBlockBytes) >= 2) {
       p.kps = p.kb;
       p.wb = r / 64;
+    } else if (r % 64 == 0) {
+      for (int k = 5; k >= 2; --k)
+        if (p.kb % k == 0 && room / (k * kBlockBytes) >= 2) {
+          p.kps = k;
+          p.wb = k;
+          break;
+        }
     }
   }
   const int stage = p.kps * kBlockBytes;

@@ -171,6 +171,18 @@ def test_head_qwen30b_shape_sampled_rows():
     np.testing.assert_allclose(out["lse"].cpu().numpy()[rows], ref["lse"], atol=2e-2, rtol=0)
 
 
+# ------------------------------------------------- position-adaptive rank ---
+@pytest.mark.parametrize("r", [384, 640, 768, 896, 1024, 2048])
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_head_rank_per_position(r, T):
+    """A different rank per drafted position means one head call per rank;
+    every rank from r = d/8 up to r = d/2 (K blocks past 512, where the
+    finish recomputes a sub-tile over several groups of chunks) runs on the
+    tensor cores and matches the oracle."""
+    counts, flips = run_case(200 + r, 8, 4096, r, 9000, "bf16", T, logits=True)
+    assert counts["exact"] >= 7
+
+
 # ----------------------------------------------------- static trimmed head ---
 def _trimmed_case(seed, M, d, V, Vk, sorted_ids=True):
     rng = np.random.default_rng(seed)
