@@ -70,15 +70,17 @@ struct KeysInShared {
 // Key T of the q-th largest of n keys (1 <= q <= n) and `need`, how many of
 // the keys equal to T are among the q largest.  Three histogram passes over
 // digits of 11, 11 and 10 bits, most significant first; every thread of the
-// block calls it.
+// block calls it.  With passes = 2 it stops after 22 bits: T is then the
+// lowest key sharing the q-th largest key's top 22 bits (a lower bound of
+// it; `need` is not meaningful).
 template <class Keys>
 __device__ void block_select_desc(const Keys& key_at, int n, int q, int* hist, int* s_warp,
-                                  int* s_sel, uint32_t& thr, int& need) {
+                                  int* s_sel, uint32_t& thr, int& need, int passes = 3) {
   const int tid = threadIdx.x;
   uint32_t prefix = 0, pmask = 0;
   need = q;
 #pragma unroll 1
-  for (int pass = 0; pass < 3; ++pass) {
+  for (int pass = 0; pass < passes; ++pass) {
     const int nb = pass < 2 ? 2048 : 1024;
     const int shift = pass == 0 ? 21 : pass == 1 ? 10 : 0;
     for (int i = tid; i < 2048; i += kTopkThreads) hist[i] = 0;
@@ -256,7 +258,8 @@ __global__ void __launch_bounds__(kTopkThreads) k_topk(const float* __restrict__
   if (S < V) q = min(S, (int)((5LL * k * S + 4LL * V - 1) / (4LL * V)) + 8);
   uint32_t t_low;
   int unused;
-  block_select_desc(KeysInShared{c_key}, S, q, hist, s_warp, s_sel, t_low, unused);
+  // (two passes: a threshold at or below the sampled rank is all step 2 needs)
+  block_select_desc(KeysInShared{c_key}, S, q, hist, s_warp, s_sel, t_low, unused, 2);
 
   // 2. (the sample's keys are no longer read: block_select_desc ended on a
   //    barrier) one pass over this CTA's ids: warp w walks a contiguous
