@@ -333,7 +333,7 @@ def trimmed_head_forward(hidden, w_kept, kept_ids, temperature=0.0, uniforms=Non
     return o
 
 
-N_KERNEL_KINDS = 13
+N_KERNEL_KINDS = 14
 
 
 def launch_count() -> int:

@@ -37,6 +37,9 @@ static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SS_OK : SS_ERR
 // a single row of z: the MMA takes the multiply-adds off the issue slots, so
 // the kernel only moves W_up.  fp32 heads, and bf16 shapes outside that range,
 // stream W_up through the CUDA cores.
+// From this many rows of h the down-projection runs on the tensor cores.
+constexpr int kDownMmaMinM = 64;
+
 static bool use_mma(bool bf16, int M, int r, int V) {
   return bf16 && M >= 1 && mma_plan(r, M, V).ok;
 }
@@ -187,8 +190,15 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
     wk.parg = cv.take<int>((size_t)M * mp.n_sub);
     unsigned* ctr = cv.take<unsigned>(2 * kMmaCtrs);
     const HeadOutputs outs{uniforms, out_tokens, out_logprob, out_row_max, out_row_lse};
-    cudaError_t e = launch_down_proj(bf16, hidden, w_down, M, d, r, true, z_ws, out_z, ctr,
-                                     2 * kMmaCtrs, stream);
+    // many rows of h: the down-projection as a split-K tensor-core GEMM, its
+    // fp32 slices in the (not yet used) partial arrays, contiguous from pmax
+    const size_t part_cap = 3 * align256((size_t)M * mp.n_sub * sizeof(float));
+    const DownMmaPlan dp = M >= kDownMmaMinM ? down_mma_plan(M, d, r, part_cap) : DownMmaPlan{};
+    cudaError_t e =
+        dp.ok ? launch_down_mma(dp, hidden, w_down, M, d, r, wk.pmax, z_ws, out_z, ctr,
+                                2 * kMmaCtrs, stream)
+              : launch_down_proj(bf16, hidden, w_down, M, d, r, true, z_ws, out_z, ctr,
+                                 2 * kMmaCtrs, stream);
     if (e == cudaSuccess && out_logits != nullptr)
       e = launch_head_mma(mp, z_ws, w_up, M, r, V, 0.f, wk, outs, out_logits, ctr, stream);
     if (e == cudaSuccess)

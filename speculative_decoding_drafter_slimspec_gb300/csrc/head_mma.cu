@@ -581,6 +581,138 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// ------------------------------------------------------- down-projection --
+// z = bf16(h W_down^T) for many rows of h, as a split-K tcgen05 GEMM: CTA
+// (tile, s) computes the 128 x 128 block of z at rows mt*128 of h and rows
+// nt*128 of W_down over K slice s (KBs 64-wide K blocks, loaded whole by TMA;
+// out-of-range rows and columns read as zero) into TMEM, and writes it in
+// fp32 to part[s] (M x r).  k_down_reduce then sums the slices in order and
+// rounds.  h and W_down are inputs, loaded while the previous library kernel
+// may still run; the partials are written only after it completes (their
+// workspace region may still be read by it).
+constexpr int kDownThreads = 128;
+constexpr int kDownMaxSlices = 32;  // K slices per block of z
+__global__ void __launch_bounds__(kDownThreads, 1)
+    k_down_mma(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
+               int M, int r, int KBs, int n_nt, float* __restrict__ part, unsigned* err) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* sA = smem;                              // KBs blocks of h
+  uint8_t* sB = smem + (size_t)KBs * kBlockBytes;  // KBs blocks of W_down
+  __shared__ uint64_t full, done;
+  __shared__ uint32_t s_tmem;
+  __shared__ int s_ok;
+  constexpr uint32_t kIdesc = idesc_bf16(kTileM, kTileN);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int s = blockIdx.y;                        // K slice
+  const int mt = blockIdx.x / n_nt, nt = blockIdx.x - mt * n_nt;
+  if (threadIdx.x == 0) {
+    mbar_init(&full, 1);
+    mbar_init(&done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(&s_tmem, kTileN);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  pdl_launch_dependents();
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    mbar_arrive_expect_tx(&full, (uint32_t)(2 * KBs * kBlockBytes));
+    for (int kb = 0; kb < KBs; ++kb) {
+      const int x = (s * KBs + kb) * 64;
+      tma_load_2d(sA + (size_t)kb * kBlockBytes, &tm_h, x, mt * kTileM, &full);
+      tma_load_2d(sB + (size_t)kb * kBlockBytes, &tm_w, x, nt * kTileN, &full);
+    }
+    ok = mbar_wait_bounded(&full, 0, err);
+    if (ok) {
+      tc_fence_after();
+      for (int kb = 0; kb < KBs; ++kb) {
+        const uint64_t ad = sw128_desc(smem_u32(sA + (size_t)kb * kBlockBytes));
+        const uint64_t bd = sw128_desc(smem_u32(sB + (size_t)kb * kBlockBytes));
+#pragma unroll
+        for (int k4 = 0; k4 < 4; ++k4)
+          mma_bf16(tmem, ad + 2 * k4, bd + 2 * k4, kIdesc, (kb | k4) != 0 ? 1u : 0u);
+      }
+    }
+    s_ok = ok ? 1 : 0;
+    mma_commit(&done);  // also after an abort: every issued MMA completes first
+  }
+  const bool done_ok = mbar_wait_bounded(&done, 0, err);
+  __syncthreads();
+  tc_fence_after();
+  const bool all_ok = s_ok != 0 && __syncthreads_and(done_ok ? 1 : 0) != 0;
+  pdl_wait_producer();
+  if (all_ok) {
+    // thread t holds row mt*128 + t of the block: 128 fp32 columns
+    const int row = mt * kTileM + warp * 32 + lane;
+    const uint32_t lane_addr = (uint32_t)(warp * 32) << 16;
+    float* dst = part + ((size_t)s * M + row) * r + nt * kTileN;
+#pragma unroll
+    for (int c4 = 0; c4 < kTileN / 64; ++c4) {
+      uint32_t v[2][32];
+      tmem_ld32_issue(tmem + lane_addr + (uint32_t)(c4 * 64), v[0]);
+      tmem_ld32_issue(tmem + lane_addr + (uint32_t)(c4 * 64 + 32), v[1]);
+      tmem_ld_wait();
+      if (row < M) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int c0 = nt * kTileN + c4 * 64 + h * 32;
+          if (c0 + 32 <= r) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(dst + c4 * 64 + h * 32 + j) =
+                  make_float4(__uint_as_float(v[h][j]), __uint_as_float(v[h][j + 1]),
+                              __uint_as_float(v[h][j + 2]), __uint_as_float(v[h][j + 3]));
+          } else {
+            for (int j = 0; j < 32; ++j)
+              if (c0 + j < r) dst[c4 * 64 + h * 32 + j] = __uint_as_float(v[h][j]);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    // no copy may still land in shared memory after an abort: wait (bounded)
+    // for the loads once more
+    if (lane == 0 && !all_ok) mbar_wait_bounded(&full, 0, err);
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTileN);
+  }
+}
+
+// z[m, j] = RNE_bf16(sum_s part[s][m][j]), the slices added in order; also
+// clears the up-projection's tile counters (as the CUDA-core down-projection
+// does).  A dependent launch: it waits for the slices.
+__global__ void __launch_bounds__(256)
+    k_down_reduce(const float* __restrict__ part, int M, int r, int S,
+                  uint16_t* __restrict__ z_ws, uint16_t* __restrict__ out_z,
+                  unsigned* __restrict__ ctr, int n_ctr) {
+  pdl_launch_dependents();
+  pdl_wait_producer();
+  if (ctr != nullptr && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < n_ctr; i += blockDim.x) ctr[i] = 0u;
+  const size_t n = (size_t)M * r;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (size_t)gridDim.x * blockDim.x) {
+    float v[kDownMaxSlices];  // every slice's load in flight, then the ordered sum
+#pragma unroll
+    for (int k = 0; k < kDownMaxSlices; ++k) v[k] = k < S ? __ldcg(part + (size_t)k * n + i) : 0.f;
+    float a = 0.f;
+#pragma unroll
+    for (int k = 0; k < kDownMaxSlices; ++k)
+      if (k < S) a = __fadd_rn(a, v[k]);
+    const uint16_t bits = f32_to_bf16_bits(a);
+    z_ws[i] = bits;
+    if (out_z) out_z[i] = bits;
+  }
+}
+
 // ------------------------------------------------------------------ finish --
 // Fixed-order block reductions over the 256 threads of the finish.
 struct BlockArg {
@@ -942,6 +1074,64 @@ static bool make_maps(const MmaPlan& p, const void* w_up, int V, int r, CUtensor
   if (p.kps > 1 && p.wb > 0) return make_map_wide(tw, w_up, V, r, p.wb);
   *tw = *tw2;
   return true;
+}
+
+DownMmaPlan down_mma_plan(int M, int d, int r, size_t part_cap) {
+  DownMmaPlan p{};
+  p.ok = false;
+  if (M <= 0 || r <= 0 || d % 8 != 0 || r % 8 != 0) return p;
+  p.n_mt = (M + kTileM - 1) / kTileM;
+  p.n_nt = (r + kTileN - 1) / kTileN;
+  const int tiles = p.n_mt * p.n_nt;
+  const int KB = (d + 63) / 64;
+  for (int S = std::max(1, std::min(std::min(KB, kDownMaxSlices), 128 / tiles)); S >= 1; --S) {
+    const int kbs = (KB + S - 1) / S;
+    const int s2 = (KB + kbs - 1) / kbs;  // no empty slices
+    if (kbs <= 6 && (size_t)s2 * M * r * sizeof(float) <= part_cap) {
+      p.S = s2;
+      p.kbs = kbs;
+      p.smem = 1024 + 2 * kbs * kBlockBytes;
+      p.ok = true;
+      return p;
+    }
+  }
+  return p;
+}
+
+cudaError_t launch_down_mma(const DownMmaPlan& p, const void* h, const void* w_down, int M, int d,
+                            int r, float* part, void* z_ws, void* out_z, unsigned* ctr, int n_ctr,
+                            cudaStream_t st) {
+  CUtensorMap th, tw;
+  if (!make_map(&th, h, M, d) || !make_map(&tw, w_down, r, d)) return cudaErrorInvalidValue;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(k_down_mma), kSmemCap);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.n_mt * p.n_nt), (unsigned)p.S);
+  cfg.blockDim = dim3(kDownThreads);
+  cfg.dynamicSmemBytes = p.smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  {
+    ProfScope ps(kKDownProj, st);
+    e = cudaLaunchKernelEx(&cfg, k_down_mma, th, tw, M, r, p.kbs, p.n_nt, part, error_word());
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cr = {};
+  const long long n = (long long)M * r;
+  cr.gridDim = dim3((unsigned)std::max<long long>(1, std::min<long long>((n + 255) / 256,
+                                                                        4LL * sm_count())));
+  cr.blockDim = dim3(256);
+  cr.stream = st;
+  cr.attrs = attr;
+  cr.numAttrs = 1;
+  ProfScope ps(kKDownReduce, st);
+  e = cudaLaunchKernelEx(&cr, k_down_reduce, (const float*)part, M, r, p.S, (uint16_t*)z_ws,
+                         (uint16_t*)out_z, ctr, n_ctr);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 cudaError_t launch_head_mma_resid(const MmaPlan& p, const void* z, const void* w_up, int B,

@@ -24,7 +24,7 @@ namespace ss {
 static const char* const kKindNames[kKindCount] = {
     "k_down_proj",   "k_head_stream", "k_head_finish", "k_verify_rows", "k_verify_decide",
     "k_verify_resid", "k_verify_finish", "k_topk",      "k_gather_logits", "k_cand_finish",
-    "k_head_mma",    "k_verify_first", "k_verify_qrow"};
+    "k_head_mma",    "k_verify_first", "k_verify_qrow", "k_down_reduce"};
 
 namespace {
 struct Rec {

@@ -18,7 +18,7 @@ unsigned* error_word();
 enum KernelKind {
   kKDownProj = 0, kKHeadStream, kKHeadFinish, kKVerifyRows, kKVerifyDecide, kKVerifyResid,
   kKVerifyFinish, kKTopk, kKGather, kKCandFinish, kKHeadMma, kKVerifyFirst, kKVerifyQRow,
-  kKindCount
+  kKDownReduce, kKindCount
 };
 
 // Counts one launch and, while profiling is on, brackets it with two events
@@ -114,6 +114,19 @@ struct MmaPlan {
   bool ok;
 };
 MmaPlan mma_plan(int r, int M, int V);
+// The down-projection as a split-K tcgen05 GEMM (head_mma.cu), for many rows
+// of h: S K slices of kbs 64-wide blocks per 128 x 128 block of z, their fp32
+// partials (S x M x r, at most part_cap bytes) summed in order by a second
+// kernel, which also clears n_ctr up-projection tile counters.
+struct DownMmaPlan {
+  int n_mt, n_nt, S, kbs, smem;
+  bool ok;
+};
+DownMmaPlan down_mma_plan(int M, int d, int r, size_t part_cap);
+cudaError_t launch_down_mma(const DownMmaPlan& plan, const void* h, const void* w_down, int M,
+                            int d, int r, float* part, void* z_ws, void* out_z, unsigned* ctr,
+                            int n_ctr, cudaStream_t st);
+
 // A row of the tcgen05 up-projection's residual mode: the final draw of a
 // verified sequence whose draft row is z W_up^T.  For vocabulary row v with
 // target logit t_v and recomputed draft logit l_v: p(v) = 2^((t_v - pmx) c)

@@ -171,6 +171,21 @@ def test_head_qwen30b_shape_sampled_rows():
     np.testing.assert_allclose(out["lse"].cpu().numpy()[rows], ref["lse"], atol=2e-2, rtol=0)
 
 
+# ------------------------------------------ many rows: tensor-core z = h W^T --
+@pytest.mark.parametrize("seed,M,d,r,V", [
+    (31, 200, 2056, 136, 5000),    # ragged K block, ragged second N tile, two M tiles
+    (32, 64, 4096, 512, 3000),     # the smallest batch on this path
+    (33, 256, 2048, 256, 8192),    # the Qwen-shaped batch
+])
+@pytest.mark.parametrize("T", [0.0, 1.0])
+def test_head_many_rows_split_k_down_projection(seed, M, d, r, V, T):
+    """From 64 rows of h the down-projection is a split-K tensor-core GEMM
+    (fp32 slices summed in order, then rounded): z within one rounding of
+    the oracle's, tokens and statistics as for every head."""
+    counts, flips = run_case(seed, M, d, r, V, "bf16", T, logits=True)
+    assert counts["exact"] >= M - 2
+
+
 # ------------------------------------------------- position-adaptive rank ---
 @pytest.mark.parametrize("r", [384, 640, 768, 896, 1024, 2048])
 @pytest.mark.parametrize("T", [0.0, 1.0])
