@@ -401,6 +401,7 @@ __global__ void __launch_bounds__(256)
                   const float* __restrict__ uniforms, int32_t* __restrict__ out_tokens,
                   int32_t* __restrict__ out_idx, float* __restrict__ out_prob) {
   constexpr int NT = 256;
+  pdl_launch_dependents();  // the next call's down-projection may start reading
   const int m = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const float* z = zc + (size_t)m * k;
   const int32_t* id = idx + (size_t)m * k;
@@ -588,7 +589,14 @@ cudaError_t launch_specvocab(const void* h, const void* w_down, const void* w_vo
     cand = cv.take<int32_t>((size_t)M * k);
     zc = cv.take<float>((size_t)M * k);
     if (out_scores) scores = out_scores;
-    e = launch_down_proj(true, h, w_down, M, d, d_prime, true, hp, nullptr, ctr, kMmaCtrs, st);
+    // h' = bf16(W_down h): for many rows a split-K tensor-core GEMM whose fp32
+    // slices live in the scores buffer until the router overwrites it
+    const DownMmaPlan dp = M >= 32 ? down_mma_plan(M, d, d_prime, (size_t)M * V * sizeof(float))
+                                   : DownMmaPlan{};
+    e = dp.ok ? launch_down_mma(dp, h, w_down, M, d, d_prime, scores, hp, nullptr, ctr, kMmaCtrs,
+                                st)
+              : launch_down_proj(true, h, w_down, M, d, d_prime, true, hp, nullptr, ctr, kMmaCtrs,
+                                 st);
     if (e != cudaSuccess) return e;
     const MmaPlan mp = mma_plan(d_prime, M, V);
     const MmaWork none{nullptr, nullptr, nullptr};
