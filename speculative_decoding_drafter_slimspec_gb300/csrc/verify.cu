@@ -10,7 +10,7 @@
 //   k_verify_rows    one warp per (row, 2048-float chunk) of the rows of a
 //                    range of positions: 16-byte streaming loads, online
 //                    (max, sum of exp at T, argmax) -> partials
-//   k_verify_first   one warp per sequence: position 0's accept test, between
+//   k_verify_first   one CTA per sequence: position 0's accept test, between
 //                    a pass over the position-0 rows and one over the rest
 //   k_verify_decide  one CTA per sequence: merges the partials of its rows,
 //                    greedy prefix match or the min(1, p/q) accept tests
@@ -19,6 +19,17 @@
 //                    straight from the partials)
 //   k_verify_finish  one CTA per sequence: inverse CDF over the chunk masses,
 //                    then an ordered scan of the one chunk that holds the draw
+//
+// The low-rank draft side (SlimSpec article, section 三: q is the drafter
+// head's softmax(z W_up^T / T)) reads no draft rows: the accept tests take
+// log q(x) from the head, the decide kernel gathers the z row of each
+// sequence's final draw, and the draw's draft row is recomputed by the
+// tcgen05 up-projection (head_mma.cu) -- written out for k_verify_resid /
+// k_verify_finish, or, from kFusedResidMinB sequences on, reduced in its
+// epilogue to sub-tile masses of max(0, p - q) and p for
+//   k_verify_lr_finish  one CTA per sequence: ordered scan of the sub-tile
+//                    masses, one 64-row sub-tile recomputed on CUDA cores,
+//                    an ordered walk
 #include <algorithm>
 
 #include "ss_common.cuh"
