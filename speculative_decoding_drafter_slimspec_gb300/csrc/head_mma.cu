@@ -739,6 +739,46 @@ __device__ __forceinline__ BlockArg block_argmax(BlockArg x, BlockArg* sh) {
   return r;
 }
 
+// One group of 64 16-byte chunks of K for rows 8w .. 8w+7 of a 64-row
+// sub-tile starting at v0 (n live rows): every load issued up front, then the
+// bf16 products accumulated in chunk order into acc.
+__device__ __forceinline__ void recompute_group(const uint8_t* __restrict__ w_up,
+                                                const uint8_t* __restrict__ z, int m, int r,
+                                                int v0, int n, int nch, int c0, int warp,
+                                                int lane, float (&acc)[8]) {
+  uint4 zc[2], wv[8][2];
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const int ch = c0 + lane + 32 * q;
+    zc[q] = ch < nch ? __ldg(reinterpret_cast<const uint4*>(z + ((size_t)m * r + ch * 8) * 2))
+                     : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int ii = 0; ii < 8; ++ii) {
+    const int i = warp * 8 + ii;
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const int ch = c0 + lane + 32 * q;
+      wv[ii][q] = (i < n && ch < nch) ? __ldg(reinterpret_cast<const uint4*>(
+                                            w_up + ((size_t)(v0 + i) * r + ch * 8) * 2))
+                                      : make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+#pragma unroll
+  for (int ii = 0; ii < 8; ++ii) {
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const uint32_t ww[4] = {wv[ii][q].x, wv[ii][q].y, wv[ii][q].z, wv[ii][q].w};
+      const uint32_t zz[4] = {zc[q].x, zc[q].y, zc[q].z, zc[q].w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        acc[ii] = fma_bf16_lo(ww[e], zz[e], acc[ii]);
+        acc[ii] = fma_bf16_hi(ww[e], zz[e], acc[ii]);
+      }
+    }
+  }
+}
+
 // One CTA of 8 warps per row of z.  Thread j owns the contiguous run of
 // sub-tile partials [j*per, (j+1)*per) in vocabulary order, per <= kFinPer,
 // loaded once into registers (all loads of the CTA in flight together).
@@ -862,43 +902,17 @@ __global__ void __launch_bounds__(kFinThreads)
   const int v0 = s_i[1] * kSubW;
   const int n = max(0, min(kSubW, V - v0));
   // recompute: warp w takes rows 8w .. 8w+7 of the sub-tile, lanes over K in
-  // groups of 64 16-byte chunks (every load of a group issued up front)
+  // groups of 64 16-byte chunks (every load of a group issued up front); one
+  // group (r <= 512) as straight-line code
   const int nch = r / 8;
   float acc[8];
 #pragma unroll
   for (int ii = 0; ii < 8; ++ii) acc[ii] = 0.f;
-  for (int c0 = 0; c0 < nch; c0 += 64) {
-    uint4 zc[2], wv[8][2];
-#pragma unroll
-    for (int q = 0; q < 2; ++q) {
-      const int ch = c0 + lane + 32 * q;
-      zc[q] = ch < nch ? __ldg(reinterpret_cast<const uint4*>(z + ((size_t)m * r + ch * 8) * 2))
-                       : make_uint4(0u, 0u, 0u, 0u);
-    }
-#pragma unroll
-    for (int ii = 0; ii < 8; ++ii) {
-      const int i = warp * 8 + ii;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int ch = c0 + lane + 32 * q;
-        wv[ii][q] = (i < n && ch < nch) ? __ldg(reinterpret_cast<const uint4*>(
-                                              w_up + ((size_t)(v0 + i) * r + ch * 8) * 2))
-                                        : make_uint4(0u, 0u, 0u, 0u);
-      }
-    }
-#pragma unroll
-    for (int ii = 0; ii < 8; ++ii) {
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint32_t ww[4] = {wv[ii][q].x, wv[ii][q].y, wv[ii][q].z, wv[ii][q].w};
-        const uint32_t zz[4] = {zc[q].x, zc[q].y, zc[q].z, zc[q].w};
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          acc[ii] = fma_bf16_lo(ww[e], zz[e], acc[ii]);
-          acc[ii] = fma_bf16_hi(ww[e], zz[e], acc[ii]);
-        }
-      }
-    }
+  if (nch <= 64) {
+    recompute_group(w_up, z, m, r, v0, n, nch, 0, warp, lane, acc);
+  } else {
+    for (int c0 = 0; c0 < nch; c0 += 64)
+      recompute_group(w_up, z, m, r, v0, n, nch, c0, warp, lane, acc);
   }
 #pragma unroll
   for (int ii = 0; ii < 8; ++ii) {
