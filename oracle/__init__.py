@@ -28,7 +28,7 @@ Sources (each function names the one it follows):
   (hypresin.com), 第三步: residual draw when the accepted block is short of the
   full length, one extra target token when the whole block is accepted.
 
-Readings taken where the articles are silent (all listed in the design doc):
+Readings taken where the articles are silent:
   * W_down is stored r x d and applied as h @ W_down.T.
   * The intermediate z (and SpecVocab's h') is rounded to nearest-even bf16 for
     bf16 workloads; fp32 workloads keep it unrounded.
