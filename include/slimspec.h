@@ -79,8 +79,12 @@ int ss_get_device_error(cudaStream_t stream);
  *
  *  hidden      M x d      dtype         w_down  r x d   dtype
  *  w_up        V x r      dtype
- *  M >= 0 (0 is a no-op), d % 8 == 0, r % 8 == 0, 8 <= r <= 1024 (bf16) or
- *  4 <= r <= 512 with r % 4 == 0 (f32), V >= 1
+ *  M >= 0 (0 is a no-op), d % 8 == 0, V >= 1, and
+ *    bf16: r % 8 == 0, 8 <= r <= 1024 at any M; 1024 < r <= 4096 while the
+ *          M x r rows of z fit in shared memory beside the W_up stages of
+ *          the tensor-core head (M <= 40 at r = 2048, M <= 16 at r = 4096);
+ *    f32:  r % 4 == 0, 4 <= r <= 256.
+ *  Other shapes return SS_ERR_UNSUPPORTED (their workspace size is 0).
  *  temperature >= 0 and finite; uniforms: M floats in [0,1) (T > 0), else
  *  may be NULL.
  *  out_tokens  M int32 (required)

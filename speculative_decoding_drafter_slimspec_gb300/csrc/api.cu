@@ -33,7 +33,7 @@ static bool temp_ok(float t) { return isfinite(t) && t >= 0.f; }
 static int cuda_status(cudaError_t e) { return e == cudaSuccess ? SS_OK : SS_ERR_CUDA; }
 
 // bf16 heads run the up-projection on the tensor cores whenever the shape
-// fits the tcgen05 kernel (r a multiple of 8 up to 512, M up to 256), even for
+// fits the tcgen05 kernel (r a multiple of 8 up to 4096, M up to 256), even for
 // a single row of z: the MMA takes the multiply-adds off the issue slots, so
 // the kernel only moves W_up.  fp32 heads, and bf16 shapes outside that range,
 // stream W_up through the CUDA cores.

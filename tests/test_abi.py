@@ -61,6 +61,19 @@ def _head(lib, **kw):
                                      a["stream"])
 
 
+@pytest.mark.parametrize("dtype,r,M,ok", [
+    ("bf16", 1024, 300, True), ("bf16", 1032, 300, False),  # r <= 1024 at any M
+    ("bf16", 2048, 40, True), ("bf16", 2048, 41, False),    # beyond: z must fit in smem
+    ("bf16", 4096, 16, True), ("bf16", 4096, 17, False), ("bf16", 4104, 1, False),
+    ("f32", 256, 8, True), ("f32", 260, 8, False), ("f32", 512, 8, False),
+])
+def test_head_supported_shapes(dtype, r, M, ok):
+    """The shape limits the header states, through the workspace query (0 =
+    unsupported) on the host."""
+    code = ss.SS_BF16 if dtype == "bf16" else ss.SS_F32
+    assert (ss.slimspec_head_workspace_size(M, 64, r, 128256, code) > 0) == ok
+
+
 def test_head_argument_errors(lib):
     E = ss.SS_ERR_INVALID_ARG
     assert _head(lib, M=-1) == E
