@@ -17,8 +17,8 @@ region).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
---impl reference times the CPU oracle (the only reference this build has) on
-the host cores, a bounded sample of the same workload per step.
+--impl reference times the CPU oracle on the host cores, a bounded sample of
+the same workload per step.
 Multi-GPU: replicas only (the round has no exchange step); one process per
 GPU under torchrun, barrier + max-over-ranks timing.
 """
