@@ -62,6 +62,19 @@ def test_router_scores_brute_force():
         assert s[0, v] == float(sum(Fraction(hp[0, j]) * Fraction(wv[v, j]) for j in range(2)))
 
 
+def test_router_hprime_is_rounded_to_bf16():
+    """Hand-worked: h = (1, 1), W_down = (1, 2^-9) makes the exact h' = 1 + 2^-9,
+    a quarter of the bf16 spacing above 1 (2^-7), so bf16 h' is exactly 1 and
+    the score through W_vocab = 3 is 3; the fp32 workload keeps 3 + 3 * 2^-9."""
+    h = np.array([[1.0, 1.0]])
+    wd = np.array([[1.0, 2.0 ** -9]])
+    wv = np.array([[3.0]])
+    hp, s = oracle.approx_scores(h, wd, wv, "bf16")
+    assert hp[0, 0] == 1.0 and s[0, 0] == 3.0
+    hp, s = oracle.approx_scores(h, wd, wv, "f32")
+    assert hp[0, 0] == 1.0 + 2.0 ** -9 and s[0, 0] == 3.0 + 3.0 * 2.0 ** -9
+
+
 def test_greedy_specvocab_token_is_candidate_argmax():
     inp = synth.specvocab_inputs(4, M=3, d=128, d_prime=8, V=1000)
     out = oracle.specvocab_head(inp["hidden"], inp["w_down"], inp["w_vocab"],

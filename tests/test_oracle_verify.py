@@ -81,6 +81,27 @@ def test_greedy_invariant_every_token_is_target_argmax():
         assert all(toks[j] == a[j] for j in range(len(toks)))
 
 
+def test_greedy_ties_go_to_the_lowest_index():
+    """Rows of small integers (many exact ties at the maximum): the target's
+    choice at every position is numpy's argmax, which returns the first
+    occurrence, so a draft token equal to a later tied maximum is rejected."""
+    rng = np.random.default_rng(11)
+    gamma, V = 4, 12
+    for _ in range(50):
+        t = rng.integers(0, 4, (gamma + 1, V)).astype(np.float64)
+        a = np.argmax(t, axis=1)
+        # the drafter picks the last tied maximum at a random position
+        cut = int(rng.integers(0, gamma))
+        x = a[:gamma].copy()
+        ties = np.nonzero(t[cut] == t[cut].max())[0]
+        x[cut] = ties[-1]
+        toks, n = oracle.verify_greedy(t, x)
+        want_n = cut if ties[-1] != a[cut] else (
+            next((j for j in range(cut + 1, gamma) if x[j] != a[j]), gamma))
+        assert n == want_n
+        assert toks[-1] == a[n]
+
+
 # ------------------------------------------------------------- sampling ----
 def _rand_dist(rng, V, zero_some=False):
     w = [Fraction(int(x)) for x in rng.integers(1, 9, V)]
