@@ -15,7 +15,10 @@ import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
-# (name, file, original text, planted text)
+# (name, file, original text, planted text).  Not listed: mistakes that give
+# the same results in exact arithmetic, such as an all-zero residual falling
+# back to q instead of p (the residual max(0, p - q) of two distributions is
+# all zero only when p = q).
 MUTATIONS = [
     ("accept test p and q swapped", "oracle/verify.py",
      "u[j] * q_rows[j][x] < p_rows[j][x]", "u[j] * p_rows[j][x] < q_rows[j][x]"),
@@ -53,6 +56,30 @@ MUTATIONS = [
      "        hp = round_to_bf16(hp)\n", "        hp = hp\n"),
     ("expected tokens drop the last run", "oracle/theory.py",
      "return total + run", "return total"),
+    ("inverse CDF falls back to the first positive weight", "oracle/head.py",
+     "return int(positive[-1])", "return int(positive[0])"),
+    ("logprob adds log W", "oracle/head.py",
+     "\"logprob\": (float(l[token]) - m) / T - logW",
+     "\"logprob\": (float(l[token]) - m) / T + logW"),
+    ("draw ignores the temperature", "oracle/head.py",
+     "w = np.exp((l - m) / T)", "w = np.exp(l - m)"),
+    ("residual takes |p - q|", "oracle/verify.py",
+     "resid = np.where(diff > 0, diff, diff * 0)", "resid = np.abs(diff)"),
+    ("softmax multiplies by T", "oracle/verify.py",
+     "w = np.exp((l - np.max(l)) / float(temperature))",
+     "w = np.exp((l - np.max(l)) * float(temperature))"),
+    ("greedy bonus from the last drafted row", "oracle/verify.py",
+     "return [int(x) for x in draft_tokens[:n]] + [a[n]], n",
+     "return [int(x) for x in draft_tokens[:n]] + [a[min(n, gamma - 1)]], n"),
+    ("SpecVocab q not normalised", "oracle/specvocab.py",
+     "q[i] = w / w.sum()", "q[i] = w"),
+    ("SpecVocab exact logits from the next row of h", "oracle/specvocab.py",
+     "zc[i] = np.asarray(u_full[cand[i]], np.float64) @ hidden[i]",
+     "zc[i] = np.asarray(u_full[cand[i]], np.float64) @ hidden[(i + 1) % M]"),
+    ("SpecVocab token not mapped to its vocabulary id", "oracle/specvocab.py",
+     "tokens[i] = cand[i][red[\"token\"]]", "tokens[i] = red[\"token\"]"),
+    ("closed form one power short", "oracle/theory.py",
+     "return (1 - alpha ** (gamma + 1)) / (1 - alpha)", "return (1 - alpha ** gamma) / (1 - alpha)"),
 ]
 
 
