@@ -180,3 +180,18 @@ def test_python_binding_refuses_cpu_tensors(lib):
     with pytest.raises(ValueError):
         ss.slimspec_head_forward(h, torch.zeros(32, 64, dtype=torch.bfloat16),
                                  torch.zeros(100, 32, dtype=torch.bfloat16))
+
+
+def test_missing_library_fails_loudly(lib, monkeypatch):
+    """No CPU fallback: with the shared library absent every call raises."""
+    import torch
+    monkeypatch.setattr(ss, "_LIB", None)
+    monkeypatch.setattr(ss, "lib_path", lambda: "/nonexistent/libslimspec.so")
+    with pytest.raises(RuntimeError, match="not built"):
+        ss.lib()
+    with pytest.raises(RuntimeError):
+        ss.slimspec_head_workspace_size(2, 64, 32, 100, ss.SS_BF16)
+    h = torch.zeros(2, 64, dtype=torch.bfloat16)
+    with pytest.raises((RuntimeError, ValueError)):
+        ss.slimspec_head_forward(h, torch.zeros(32, 64, dtype=torch.bfloat16),
+                                 torch.zeros(100, 32, dtype=torch.bfloat16))
