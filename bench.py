@@ -499,7 +499,8 @@ def run_reference(args, world, rank):
     d, r, V, M, gamma, T = WORKLOADS[args.workload]
     sample = (f"per step: 1 head row + 1 verified sequence over {S} of {V} vocabulary rows, "
               f"scaled to the round ({x['n_calls'] * M} head rows + {x['B']} sequences)")
-    line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": 1,
+    # n_gpus is the launch's N; the oracle itself runs on rank 0's host cores only
+    line = {"impl": "reference", "metric": METRIC, "value": rate, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * x["n_calls"] * M / rate, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
