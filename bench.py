@@ -632,6 +632,7 @@ def run_ours(args, world, rank, local):
     units, secs = aggregate(units_per_step * args.steps, sec_local, world)
     value = units / secs
     assert ss.ss_get_device_error() == ss.SS_OK
+    step_dist = step_time_distribution(graph, stream, min(args.steps, 500))
 
     # per-kernel device time: the step captured again with the library's
     # event pairs around every launch, replayed and read after each replay
@@ -698,6 +699,7 @@ def run_ours(args, world, rank, local):
     ver_ms = sum(ms for name, (n, ms) in prof.items() if name.startswith("k_verify")) / n_prof
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": secs * 1000.0 / args.steps,
+            "ms_per_step_dist": step_dist,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic: seeded N(0,1/fan_in) bf16 weights, N(0,1) hidden states, "
                     "Zipf-like target logits",
@@ -729,6 +731,30 @@ def run_ours(args, world, rank, local):
                       f"{x['V']} vocabulary rows ({secs_cpu:.1f} s of CPU work), scaled to the "
                       f"round ({units_per_step} head rows + {x['B']} sequences)"}
     print(json.dumps(line), flush=True)
+
+
+def quantiles(values, fracs):
+    """Nearest-rank quantiles of a list of numbers."""
+    v = sorted(values)
+    return [v[min(len(v) - 1, int(f * (len(v) - 1) + 0.5))] for f in fracs]
+
+
+def step_time_distribution(graph, stream, n):
+    """p10 / median / p90 of the step time over n more replays of the captured
+    step, each between its own pair of CUDA events (taken after the timed
+    region, which has only one pair; the events add a little to each step)."""
+    import torch
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for a, b in evs:
+            a.record(stream)
+            graph.replay()
+            b.record(stream)
+    stream.synchronize()
+    p10, p50, p90 = quantiles([a.elapsed_time(b) for a, b in evs], (0.1, 0.5, 0.9))
+    return {"p10": p10, "median": p50, "p90": p90, "steps": n,
+            "how": "an event pair around each replay, after the timed region"}
 
 
 def run_e2e(args, x, ss, stream, world):

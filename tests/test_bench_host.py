@@ -82,3 +82,10 @@ def test_specvocab_gather_bytes():
     kb = bench.kernel_bytes(x, 50000.0, 0)
     assert kb["k_gather_logits"] == 50000 * 4096 * 2 + 32 * 4096 * 2
     assert kb["k_topk"] == 32 * 151936 * 4
+
+
+def test_quantiles_nearest_rank():
+    v = list(range(11))            # 0 .. 10
+    assert bench.quantiles(v, (0.1, 0.5, 0.9)) == [1, 5, 9]
+    assert bench.quantiles([3.0], (0.1, 0.5, 0.9)) == [3.0, 3.0, 3.0]
+    assert bench.quantiles([5, 1, 3], (0.0, 1.0)) == [1, 5]
