@@ -41,7 +41,7 @@ extern "C" {
 typedef enum {
   SS_OK = 0,
   SS_ERR_INVALID_ARG = 1,   /* null / misaligned pointer, bad size or value   */
-  SS_ERR_UNSUPPORTED = 2,   /* valid request this build has no kernel for     */
+  SS_ERR_UNSUPPORTED = 2,   /* valid request the library has no kernel for   */
   SS_ERR_WORKSPACE = 3,     /* workspace missing, misaligned or too small     */
   SS_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed    */
   SS_ERR_TIMEOUT = 5,       /* a bounded device-side wait ran out             */

@@ -32,7 +32,7 @@ def topk_lowest_index(scores_row, k: int) -> np.ndarray:
     """The k highest-scoring ids of one row, ties broken toward the lowest id.
 
     Section 2.2.2 picks k_t = topk(s, k); the articles do not say how ties are
-    broken, and this build breaks them toward the lower id.  The ids are
+    broken, and the oracle breaks them toward the lower id.  The ids are
     returned in ascending id order (the order the exact stage and its
     inverse-CDF walk them in).
     """

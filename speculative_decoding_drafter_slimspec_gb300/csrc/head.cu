@@ -723,7 +723,7 @@ cudaError_t launch_down_proj(bool bf16, const void* h, const void* w, int M, int
   return cudaGetLastError();
 }
 
-// The geometries this build instantiates: (bf16, lanes per row, chunks per
+// The geometries the library instantiates: (bf16, lanes per row, chunks per
 // lane, rows of z per warp, warps per ring).
 #define SS_HEAD_GEOMS(X)  \
   X(true, 32, 1, 1, 1, 16)  \

@@ -76,7 +76,7 @@ def test_head_bf16_intermediate_rounding_exact():
 
 
 def test_low_rank_equals_dense():
-    """Spec invariant: with W = W_up W_down, the unrounded low-rank head
+    """Low-rank = dense: with W = W_up W_down, the unrounded low-rank head
     equals the dense head h W^T (fp64, relative 1e-12)."""
     inp = synth.head_inputs(3, M=3, d=96, r=16, V=777, dtype="f32")
     lr = oracle.slimspec_head(inp["hidden"], inp["w_down"], inp["w_up"], "f32", 0.0)
