@@ -74,6 +74,27 @@ def test_head_supported_shapes(dtype, r, M, ok):
     assert (ss.slimspec_head_workspace_size(M, 64, r, 128256, code) > 0) == ok
 
 
+@pytest.mark.parametrize("call,ok", [
+    (lambda: ss.specvocab_head_workspace_size(4, 4096, 1024, 5000, 2048), True),
+    (lambda: ss.specvocab_head_workspace_size(4, 4096, 1032, 5000, 2048), False),  # d' <= 1024
+    (lambda: ss.specvocab_head_workspace_size(4, 4104, 256, 5000, 2048), False),   # d <= 4096
+    (lambda: ss.specvocab_head_workspace_size(4, 4096, 256, 5000, 4096), True),
+    (lambda: ss.specvocab_head_workspace_size(4, 4096, 256, 5000, 4097), False),   # k <= 4096
+    (lambda: ss.specvocab_head_workspace_size(4, 4096, 256, 3000, 3001), False),   # k <= V
+    (lambda: ss.trimmed_head_workspace_size(16, 4096, 32768), True),
+    (lambda: ss.trimmed_head_workspace_size(17, 4096, 32768), False),  # h must fit beside W
+    (lambda: ss.trimmed_head_workspace_size(8, 4104, 32768), False),   # d <= 4096
+    (lambda: ss.spec_verify_workspace_size(8, 32, 1000, 1.0), True),
+    (lambda: ss.spec_verify_workspace_size(8, 33, 1000, 1.0), False),  # gamma <= 32
+    (lambda: ss.spec_verify_lowrank_workspace_size(8, 32, 1000, 64), True),
+    (lambda: ss.spec_verify_lowrank_workspace_size(8, 33, 1000, 64), False),
+])
+def test_other_supported_shapes(call, ok):
+    """The limits the header states for the other entry points, through their
+    workspace queries (0 = unsupported) on the host."""
+    assert (call() > 0) == ok
+
+
 def test_head_argument_errors(lib):
     E = ss.SS_ERR_INVALID_ARG
     assert _head(lib, M=-1) == E
