@@ -24,6 +24,10 @@ Sources (each function names the one it follows):
   resamples a rejection from the renormalised positive part of p - q, and the
   output distribution equals p exactly.  Section "这笔账划不划算，看一个数":
   the closed form for expected tokens per round and its table at gamma = 4.
+* Salmon, Moraes, Dror & Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3"
+  (SC'11), section 4: the Philox4x32-10 counter-based generator that both
+  sides draw their uniforms from when the caller passes a seed and an offset
+  instead of its own uniforms.
 * "SpecTr-GBV article" -- SpecTr-GBV: Multi-Draft Block Verification
   (hypresin.com), 第三步: residual draw when the accepted block is short of the
   full length, one extra target token when the whole block is accepted.
@@ -33,8 +37,9 @@ Readings taken where the articles are silent:
   * The intermediate z (and SpecVocab's h') is rounded to nearest-even bf16 for
     bf16 workloads; fp32 workloads keep it unrounded.
   * Ties in argmax, top-k and inverse-CDF go to the lowest vocabulary index.
-  * Sampling uses one caller-supplied uniform u per draw and inverse-CDF over
-    the weights in ascending vocabulary order.
+  * Sampling uses one uniform u per draw (the caller's own, or Philox4x32-10
+    at the draw's (seed, offset, row, slot) counter) and inverse-CDF over the
+    weights in ascending vocabulary order.
   * Temperature divides both target and draft logits.
   * An all-zero residual falls back to p at that position.
 
@@ -48,6 +53,7 @@ from .head import down_projection, up_projection, dense_logits, row_reduce, \
 from .specvocab import approx_scores, topk_lowest_index, specvocab_head
 from .verify import softmax_t, verify_greedy, verify_decide, verify_sampling, verify_batch, \
     verify_lowrank_batch
+from .philox import philox_block, philox4x32_10, uniforms as philox_uniforms
 from . import theory
 
 __all__ = [
@@ -55,4 +61,5 @@ __all__ = [
     "row_reduce", "inverse_cdf", "slimspec_head", "dense_head", "trimmed_head", "approx_scores",
     "topk_lowest_index", "specvocab_head", "softmax_t", "verify_greedy",
     "verify_decide", "verify_sampling", "verify_batch", "verify_lowrank_batch", "theory",
+    "philox_block", "philox4x32_10", "philox_uniforms",
 ]

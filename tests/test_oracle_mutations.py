@@ -78,6 +78,24 @@ MUTATIONS = [
      "zc[i] = np.asarray(u_full[cand[i]], np.float64) @ hidden[(i + 1) % M]"),
     ("SpecVocab token not mapped to its vocabulary id", "oracle/specvocab.py",
      "tokens[i] = cand[i][red[\"token\"]]", "tokens[i] = red[\"token\"]"),
+    ("Philox multipliers swapped", "oracle/philox.py",
+     "PHILOX_M4x32 = (0xD2511F53, 0xCD9E8D57)", "PHILOX_M4x32 = (0xCD9E8D57, 0xD2511F53)"),
+    ("Philox nine rounds", "oracle/philox.py", "ROUNDS = 10", "ROUNDS = 9"),
+    ("Philox key bumped before the first round", "oracle/philox.py",
+     "        if i > 0:  # the key schedule", "        if i >= 0:  # the key schedule"),
+    ("Philox round keeps c1 in place of the low product", "oracle/philox.py",
+     "(p1 >> bits) ^ c1 ^ k0, p1 & mask,", "(p1 >> bits) ^ c1 ^ k0, c1,"),
+    ("vectorised Philox drops the second key word", "oracle/philox.py",
+     "(p0 >> s32) ^ c3 ^ k1, p0 & m32)", "(p0 >> s32) ^ c3, p0 & m32)"),
+    ("uniform from the last output word", "oracle/philox.py",
+     "x0 = philox4x32_10(ctr, key)[..., 0]", "x0 = philox4x32_10(ctr, key)[..., 3]"),
+    ("offset words swapped in the counter", "oracle/philox.py",
+     "ctr = np.stack([row, slot, np.full_like(row, offset & _MASK32),\n"
+     "                    np.full_like(row, offset >> 32)], axis=-1)",
+     "ctr = np.stack([row, slot, np.full_like(row, offset >> 32),\n"
+     "                    np.full_like(row, offset & _MASK32)], axis=-1)"),
+    ("uniform keeps 23 bits", "oracle/philox.py",
+     "return (x0 >> 8) * 2.0 ** -24", "return (x0 >> 9) * 2.0 ** -23"),
     ("closed form one power short", "oracle/theory.py",
      "return (1 - alpha ** (gamma + 1)) / (1 - alpha)", "return (1 - alpha ** gamma) / (1 - alpha)"),
 ]
