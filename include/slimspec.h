@@ -19,8 +19,16 @@
  *  * `workspace` is caller-owned device scratch of at least the size the
  *    matching *_workspace_size() reports (256-byte aligned).  Its contents on
  *    entry do not matter; two calls in flight at once need two workspaces.
- *  * Sampling draws use caller-supplied uniforms in [0, 1) (one per draw, see
- *    each call).  Temperature 0 means greedy and the uniforms are not read.
+ *  * Sampling draws take one uniform in [0, 1) each.  A call that samples
+ *    (temperature > 0) takes `seed`, `offset` and a nullable `uniforms`:
+ *    with `uniforms` NULL, draw (row, slot) uses the Philox4x32-10 stream
+ *    (Salmon, Moraes, Dror & Shaw, "Parallel Random Numbers: As Easy as 1, 2,
+ *    3", SC'11) at key = (seed mod 2^32, seed >> 32) and counter = (row, slot,
+ *    offset mod 2^32, offset >> 32), u = (first output word >> 8) * 2^-24;
+ *    with `uniforms` given, it uses uniforms[row * slots + slot] instead (a
+ *    hook for exact tests).  Each call names its rows and slots.  Advance
+ *    `offset` between calls so that no two calls share a counter.
+ *    Temperature 0 means greedy: nothing is drawn.
  *  * Ties in every argmax, top-k and inverse-CDF go to the lowest vocabulary
  *    index.  Results are deterministic: the same inputs give the same bits.
  *  * Device-side anomalies (a draft token outside [0, V), a bounded wait that
@@ -56,10 +64,47 @@ const char* ss_status_string(int status);
 /* Library ABI version (major * 100 + minor). */
 int ss_version(void);
 
+/* ------------------------------------------------------------------------ *
+ * The Philox4x32-10 stream on the device (the paper above, section 4).
+ *
+ * ss_philox_uniforms: out[row * slots + slot] = the uniform the sampling
+ *   calls draw at (seed, offset, row, slot) when given no uniforms; rows,
+ *   slots >= 0 with rows * slots < 2^31 (else SS_ERR_UNSUPPORTED); out is
+ *   rows x slots float32.
+ * ss_philox4x32_10: raw blocks; blocks is n x 6 uint32 (counter words c0..c3,
+ *   key words k0, k1), out is n x 4 uint32 (the ten-round output words).
+ * Both asynchronous on `stream`; SS_ERR_INVALID_ARG on a null or unaligned
+ * pointer or a negative size.
+ * ------------------------------------------------------------------------ */
+int ss_philox_uniforms(uint64_t seed, uint64_t offset, int rows, int slots, float* out,
+                       cudaStream_t stream);
+int ss_philox4x32_10(const uint32_t* blocks, int n, uint32_t* out, cudaStream_t stream);
+
 /* Reads and clears the device error word of the current device after
  * synchronising `stream`.  Returns SS_OK, SS_ERR_TIMEOUT, SS_ERR_DEVICE_INDEX
  * or SS_ERR_CUDA. */
 int ss_get_device_error(cudaStream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * Failure detection (the articles have no counterpart).  Every wait of a
+ * kernel on its own pipeline (a TMA stage, an MMA accumulator, a tile id) is
+ * bounded; when one runs out the kernel records SS_ERR_TIMEOUT in the error
+ * word, lets what it already issued land (drain waits, always bounded at
+ * 1 s), frees its tensor memory and returns, leaving the context usable.
+ * ss_set_wait_limit_ns: the limit of the pipeline waits on the current
+ *   device, 0 .. 10^10 ns (default 10^9).  A short limit can make a slow but
+ *   healthy call fail.
+ * ss_set_stall_test: with `on` non-zero, the MMA issuer of the tensor-core
+ *   up-projection first waits on a barrier that nothing arrives on, so every
+ *   call on the current device that runs it (bf16 low-rank heads, the trimmed
+ *   head, the SpecVocab router, the low-rank verifier's recompute) times out
+ *   and its outputs are undefined -- a way to test the timeout path without
+ *   a fault.
+ * Both synchronise the device first and apply to kernels launched after they
+ * return.
+ * ------------------------------------------------------------------------ */
+int ss_set_wait_limit_ns(uint64_t limit_ns);
+int ss_set_stall_test(int on);
 
 /* ------------------------------------------------------------------------ *
  * SlimSpec low-rank drafter head, fused with its per-row reduction.
@@ -73,7 +118,8 @@ int ss_get_device_error(cudaStream_t stream);
  *   l[m, v]   = z[m] . W_up[v]^T   for v < V    (fp32 accumulate)
  *   greedy (temperature == 0): token = lowest v attaining max_v l[m, v]
  *   sampling (temperature > 0): w_v = exp((l[m,v] - max)/T); token = smallest
- *     v whose ascending-order partial sum of w exceeds uniforms[m] * sum_v w_v
+ *     v whose ascending-order partial sum of w exceeds u_m * sum_v w_v, u_m
+ *     the uniform of draw (row m, slot 0)
  * The M x V logits are reduced on chip and never written unless out_logits
  * is given (debug).
  *
@@ -85,8 +131,8 @@ int ss_get_device_error(cudaStream_t stream);
  *          the tensor-core head (M <= 40 at r = 2048, M <= 16 at r = 4096);
  *    f32:  r % 4 == 0, 4 <= r <= 256.
  *  Other shapes return SS_ERR_UNSUPPORTED (their workspace size is 0).
- *  temperature >= 0 and finite; uniforms: M floats in [0,1) (T > 0), else
- *  may be NULL.
+ *  temperature >= 0 and finite.  uniforms, when given, are M floats in
+ *  [0, 1).
  *  out_tokens  M int32 (required)
  *  out_logprob M float   log softmax(l/T)[token]; 0 when greedy   (nullable)
  *  out_row_max M float   max_v l[m, v]                           (nullable)
@@ -98,9 +144,9 @@ size_t slimspec_head_workspace_size(int M, int d, int r, int V, int dtype);
 
 int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_up,
                           int M, int d, int r, int V, int dtype, float temperature,
-                          const float* uniforms, int32_t* out_tokens,
-                          float* out_logprob, float* out_row_max, float* out_row_lse,
-                          void* out_z, float* out_logits, void* workspace,
+                          uint64_t seed, uint64_t offset, const float* uniforms,
+                          int32_t* out_tokens, float* out_logprob, float* out_row_max,
+                          float* out_row_lse, void* out_z, float* out_logits, void* workspace,
                           size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
@@ -114,20 +160,25 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
  * workspace.  The scratch is a fixed array of SS_NOALLOC_SCRATCH_BYTES inside
  * the library, present on every GPU that loads it until the process exits.
  * A request whose slimspec_head_workspace_size() exceeds that returns
- * SS_ERR_WORKSPACE before anything is launched (on a 152-SM GB300 it fits up
- * to M = 16 rows at V = 201088).  The first call on a device looks up the
- * array's device address (cudaGetSymbolAddress) and caches it; make that
- * first call before any stream capture.  All calls share the array and each
- * leaves its contents behind: calls that overlap on the GPU race.  It
- * allocates nothing.
+ * SS_ERR_WORKSPACE before anything is launched: bf16 heads fit up to M = 109
+ * rows at the GPT-OSS shape (r = 360, V = 201088), 167 at the Llama shape
+ * (r = 512, V = 128256) and 144 at the Qwen shape (r = 256, V = 151936);
+ * slimspec_head_workspace_size() gives the bytes of any other shape.  The
+ * first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) and caches it with the id of the device's current
+ * context; a call that finds another context current (after a
+ * cudaDeviceReset, say) looks it up again.  Make those calls outside stream
+ * capture.  All calls share the array and each leaves its contents behind:
+ * calls that overlap on the GPU race.  It allocates nothing.
  * ------------------------------------------------------------------------ */
 #define SS_NOALLOC_SCRATCH_BYTES (4u << 20) /* 4 MiB */
 
 int slimspec_head_forward_noalloc(const void* hidden, const void* w_down, const void* w_up,
                                   int M, int d, int r, int V, int dtype, float temperature,
-                                  const float* uniforms, int32_t* out_tokens,
-                                  float* out_logprob, float* out_row_max, float* out_row_lse,
-                                  void* out_z, float* out_logits, cudaStream_t stream);
+                                  uint64_t seed, uint64_t offset, const float* uniforms,
+                                  int32_t* out_tokens, float* out_logprob, float* out_row_max,
+                                  float* out_row_lse, void* out_z, float* out_logits,
+                                  cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * Static trimmed head: the dense head over a fixed subset of the vocabulary.
@@ -142,13 +193,14 @@ int slimspec_head_forward_noalloc(const void* hidden, const void* w_down, const 
  *  kept_ids  V_kept int32 vocabulary ids (not checked)
  *  d % 8 == 0; d <= 4096; h must fit in shared memory beside the W stages
  *  (M <= 16 at d = 4096), else SS_ERR_UNSUPPORTED
- *  outputs and uniforms as for slimspec_head_forward (logprob and lse over
- *  the kept set).
+ *  outputs, seed, offset and uniforms as for slimspec_head_forward (logprob
+ *  and lse over the kept set).
  * ------------------------------------------------------------------------ */
 size_t trimmed_head_workspace_size(int M, int d, int V_kept);
 
 int trimmed_head_forward(const void* hidden, const void* w_kept, const int32_t* kept_ids, int M,
-                         int d, int V_kept, float temperature, const float* uniforms,
+                         int d, int V_kept, float temperature, uint64_t seed, uint64_t offset,
+                         const float* uniforms,
                          int32_t* out_tokens, float* out_logprob, float* out_row_max,
                          float* out_row_lse, void* workspace, size_t workspace_bytes,
                          cudaStream_t stream);
@@ -162,23 +214,25 @@ int trimmed_head_forward(const void* hidden, const void* w_kept, const int32_t* 
  *   K[m]  = the k largest s[m, v] (ties to the lowest v), ascending id order
  *   z'[m, j] = U[K[m, j]] . h[m]          exact logits of the candidates
  *   q[m]  = softmax(z'[m] / T); token = K[m, j*] with j* the greedy argmax
- *           (T == 0) or the inverse-CDF draw with uniforms[m] over the
- *           candidates in ascending id order.
+ *           (T == 0) or the inverse-CDF draw of row m (draw (row m, slot 0))
+ *           over the candidates in ascending id order.
  *  hidden M x d, w_down d' x d, w_vocab V x d', u_full V x d (all bf16)
  *  d % 8 == 0, d' % 8 == 0, d' <= 1024, d <= 4096, 1 <= k <= min(V, 4096)
- *  out_tokens    M int32 (required)
- *  out_topk_idx  M x k int32 candidate ids, ascending            (nullable)
- *  out_topk_prob M x k float q over the candidates (T > 0)       (nullable)
- *  out_scores    M x V float approximate scores (debug)          (nullable)
+ *  out_tokens      M int32 (required)
+ *  out_topk_idx    M x k int32 candidate ids, ascending            (nullable)
+ *  out_topk_prob   M x k float q over the candidates (T > 0; one-hot
+ *                  at the argmax when greedy)                      (nullable)
+ *  out_topk_logits M x k float z', the candidates' exact logits   (nullable)
+ *  out_scores      M x V float approximate scores (debug)          (nullable)
  * ------------------------------------------------------------------------ */
 size_t specvocab_head_workspace_size(int M, int d, int d_prime, int V, int k);
 
 int specvocab_head_forward(const void* hidden, const void* w_down, const void* w_vocab,
                            const void* u_full, int M, int d, int d_prime, int V, int k,
-                           float temperature, const float* uniforms,
-                           int32_t* out_tokens, int32_t* out_topk_idx,
-                           float* out_topk_prob, float* out_scores, void* workspace,
-                           size_t workspace_bytes, cudaStream_t stream);
+                           float temperature, uint64_t seed, uint64_t offset,
+                           const float* uniforms, int32_t* out_tokens, int32_t* out_topk_idx,
+                           float* out_topk_prob, float* out_topk_logits, float* out_scores,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* The top-k stage of the SpecVocab head on its own ([SpecVocab] section
  * 2.2.2): for each of M rows of V float32 scores, the k largest, ties to the
@@ -201,10 +255,12 @@ int ss_topk_rows(const float* scores, int M, int V, int k, int32_t* out_idx,
  *     at the first rejection n the token is the inverse-CDF draw with
  *     u[b, gamma] from max(0, p_n - q_n) (from p_n if that is all zero); if all
  *     gamma are kept, the bonus token is drawn from p_gamma with u[b, gamma].
+ *     u[b, j] is draw (row b, slot j) of gamma + 1 slots.
  *  target_logits B x (gamma+1) x V float32
  *  draft_logits  B x gamma x V float32 (may be NULL when T == 0)
  *  draft_tokens  B x gamma int32, each in [0, V) (checked on the device)
- *  uniforms      B x (gamma+1) floats in [0,1) (T > 0), else may be NULL
+ *  uniforms      NULL (Philox at seed, offset), or B x (gamma+1) floats in
+ *                [0, 1)
  *  1 <= gamma <= 32, 1 <= V <= 524288, B >= 0; SS_ERR_UNSUPPORTED when
  *    B*(gamma+1)*V >= 2^40 or B*(2*gamma+1)*ceil(V/2048) >= 2^31
  *  out_tokens    B x (gamma+1) int32: the n+1 emitted tokens, then -1
@@ -218,7 +274,8 @@ size_t spec_verify_workspace_size(int B, int gamma, int V, float temperature);
 
 int spec_verify(const float* target_logits, const float* draft_logits,
                 const int32_t* draft_tokens, int B, int gamma, int V,
-                float temperature, const float* uniforms, int32_t* out_tokens,
+                float temperature, uint64_t seed, uint64_t offset,
+                const float* uniforms, int32_t* out_tokens,
                 int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
                 cudaStream_t stream);
 
@@ -241,7 +298,7 @@ int spec_verify(const float* target_logits, const float* draft_logits,
  *  w_up          V x r bf16, the head's up-projection
  *  draft_logprob, draft_lse   float32, indexed like the rows of z
  *  draft_tokens  int32, indexed like the rows of z (checked on the device)
- *  uniforms      B x (gamma+1) float32
+ *  seed, offset, uniforms as for spec_verify
  *  temperature > 0; 1 <= gamma <= 32; r % 8 == 0, r <= 512; B <= 256;
  *  V <= 524288; z, w_up and target_logits 16-byte aligned
  *  out_tokens, out_num_accepted as for spec_verify.
@@ -253,9 +310,9 @@ size_t spec_verify_lowrank_workspace_size(int B, int gamma, int V, int r);
 int spec_verify_lowrank(const float* target_logits, const void* z, const void* w_up,
                         const float* draft_logprob, const float* draft_lse, int seq_stride,
                         int pos_stride, int r, const int32_t* draft_tokens, int B, int gamma,
-                        int V, float temperature, const float* uniforms, int32_t* out_tokens,
-                        int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
-                        cudaStream_t stream);
+                        int V, float temperature, uint64_t seed, uint64_t offset,
+                        const float* uniforms, int32_t* out_tokens, int32_t* out_num_accepted,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ------------------------------------------------------------------------ *
  * Instrumentation (no counterpart in the articles; used by the benchmark).

@@ -13,7 +13,12 @@ Public calls (same names as the C ABI):
     spec_verify             greedy / sampling verification
     spec_verify_lowrank     sampling verification with the draft side from the head
     trimmed_head_forward    dense head over a kept subset of the vocabulary
+    ss_philox_uniforms      the Philox4x32-10 uniforms a sampling call draws
+    ss_philox4x32_10        raw Philox4x32-10 blocks
     ss_get_device_error     device error word (synchronises the stream)
+
+Sampling calls draw their uniforms from the library's Philox4x32-10 stream at
+(seed, offset) unless ``uniforms`` is given (a hook for exact tests).
 """
 from __future__ import annotations
 
@@ -30,7 +35,8 @@ __all__ = [
     "specvocab_head_forward", "ss_topk_rows", "spec_verify", "spec_verify_lowrank",
     "ss_get_device_error", "slimspec_head_workspace_size", "specvocab_head_workspace_size",
     "spec_verify_workspace_size", "spec_verify_lowrank_workspace_size", "ss_topk_workspace_size",
-    "trimmed_head_forward", "trimmed_head_workspace_size",
+    "trimmed_head_forward", "trimmed_head_workspace_size", "ss_philox_uniforms",
+    "ss_philox4x32_10", "ss_set_wait_limit_ns", "ss_set_stall_test",
 ]
 
 SS_OK, SS_ERR_INVALID_ARG, SS_ERR_UNSUPPORTED, SS_ERR_WORKSPACE = 0, 1, 2, 3
@@ -47,28 +53,33 @@ _SIGS = {
     "ss_version": (_i, []),
     "ss_get_device_error": (_i, [_vp]),
     "slimspec_head_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
-    "slimspec_head_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp, _vp,
-                                   _vp, _vp, _vp, _vp, _sz, _vp]),
-    "slimspec_head_forward_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp,
-                                           _vp, _vp, _vp, _vp, _vp, _vp]),
+    "ss_philox_uniforms": (_i, [_u64, _u64, _i, _i, _vp, _vp]),
+    "ss_philox4x32_10": (_i, [_vp, _i, _vp, _vp]),
+    "slimspec_head_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _u64, _u64, _vp, _vp,
+                                   _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "slimspec_head_forward_noalloc": (_i, [_vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _u64, _u64,
+                                           _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "specvocab_head_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
-    "specvocab_head_forward": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _vp, _vp, _vp,
-                                    _vp, _vp, _vp, _sz, _vp]),
+    "specvocab_head_forward": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _u64, _u64, _vp,
+                                    _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "ss_topk_workspace_size": (_sz, [_i, _i, _i]),
     "ss_topk_rows": (_i, [_vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "spec_verify_workspace_size": (_sz, [_i, _i, _i, _f]),
-    "spec_verify": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "spec_verify": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _u64, _u64, _vp, _vp, _vp, _vp, _sz,
+                         _vp]),
     "spec_verify_lowrank_workspace_size": (_sz, [_i, _i, _i, _i]),
     "trimmed_head_workspace_size": (_sz, [_i, _i, _i]),
-    "trimmed_head_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _vp, _vp, _vp, _vp, _vp, _vp,
-                                  _sz, _vp]),
-    "spec_verify_lowrank": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _f, _vp,
-                                 _vp, _vp, _vp, _sz, _vp]),
+    "trimmed_head_forward": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _u64, _u64, _vp, _vp, _vp,
+                                  _vp, _vp, _vp, _sz, _vp]),
+    "spec_verify_lowrank": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _vp, _i, _i, _i, _f, _u64,
+                                 _u64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "ss_launch_count": (ctypes.c_longlong, []),
     "ss_profile_start": (_i, []),
     "ss_profile_stop": (_i, []),
     "ss_profile_read": (_i, [_vp, _vp, _i, _i]),
     "ss_profile_kind_name": (ctypes.c_char_p, [_i]),
+    "ss_set_wait_limit_ns": (_i, [_u64]),
+    "ss_set_stall_test": (_i, [_i]),
 }
 
 
@@ -171,12 +182,14 @@ def ss_topk_workspace_size(M, V, k) -> int:
 
 
 # -------------------------------------------------------------- entry points --
-def slimspec_head_forward(hidden, w_down, w_up, temperature=0.0, uniforms=None, *,
-                          want_stats=True, want_z=False, want_logits=False,
+def slimspec_head_forward(hidden, w_down, w_up, temperature=0.0, uniforms=None, *, seed=0,
+                          offset=0, want_stats=True, want_z=False, want_logits=False,
                           workspace=None, out=None, stream=None) -> dict:
     """Low-rank head h -> h W_down^T -> . W_up^T fused with the row reduction.
 
     hidden (M, d), w_down (r, d), w_up (V, r): same dtype (bf16 or fp32), CUDA.
+    Sampling (temperature > 0) draws row m's uniform from Philox4x32-10 at
+    (seed, offset, row m, slot 0), or takes uniforms[m] when given.
     Returns a dict with 'tokens' (M int32) and, as requested, 'logprob',
     'row_max', 'lse' (M float32), 'z' (M, r) and 'logits' (M, V float32).
     ``out`` may supply preallocated output tensors under the same keys.
@@ -204,8 +217,9 @@ def slimspec_head_forward(hidden, w_down, w_up, temperature=0.0, uniforms=None, 
     nbytes = slimspec_head_workspace_size(M, d, r, V, code)
     ws = _workspace(nbytes, dev, workspace)
     st = lib().slimspec_head_forward(
-        _ptr(hidden), _ptr(w_down), _ptr(w_up), M, d, r, V, code, float(temperature),
-        _ptr(uniforms), _ptr(o["tokens"]), _ptr(o.get("logprob")), _ptr(o.get("row_max")),
+        _ptr(hidden), _ptr(w_down), _ptr(w_up), M, d, r, V, code, float(temperature), int(seed),
+        int(offset), _ptr(uniforms), _ptr(o["tokens"]), _ptr(o.get("logprob")),
+        _ptr(o.get("row_max")),
         _ptr(o.get("lse")), _ptr(o.get("z")), _ptr(o.get("logits")), _ptr(ws), ws.numel(),
         _stream(stream))
     _check(st, "slimspec_head_forward")
@@ -213,9 +227,14 @@ def slimspec_head_forward(hidden, w_down, w_up, temperature=0.0, uniforms=None, 
 
 
 def specvocab_head_forward(hidden, w_down, w_vocab, u_full, k, temperature=0.0, uniforms=None,
-                           *, want_topk=True, want_prob=False, want_scores=False,
-                           workspace=None, out=None, stream=None) -> dict:
-    """SpecVocab head: router scores, top-k, exact candidate logits, draw (bf16)."""
+                           *, seed=0, offset=0, want_topk=True, want_prob=False,
+                           want_logits=False, want_scores=False, workspace=None, out=None,
+                           stream=None) -> dict:
+    """SpecVocab head: router scores, top-k, exact candidate logits, draw (bf16).
+
+    Returns 'tokens' and, as requested, 'topk_idx' (M, k) ascending ids,
+    'topk_prob' (M, k) q over them, 'topk_logits' (M, k) their exact logits and
+    'scores' (M, V) the router's approximate scores."""
     M, d = hidden.shape
     dp, d2 = w_down.shape
     V, dp2 = w_vocab.shape
@@ -232,6 +251,9 @@ def specvocab_head_forward(hidden, w_down, w_vocab, u_full, k, temperature=0.0, 
     if want_prob:
         if "topk_prob" not in o:
             o["topk_prob"] = torch.empty(M, k, dtype=torch.float32, device=dev)
+    if want_logits:
+        if "topk_logits" not in o:
+            o["topk_logits"] = torch.empty(M, k, dtype=torch.float32, device=dev)
     if want_scores:
         if "scores" not in o:
             o["scores"] = torch.empty(M, V, dtype=torch.float32, device=dev)
@@ -239,8 +261,9 @@ def specvocab_head_forward(hidden, w_down, w_vocab, u_full, k, temperature=0.0, 
     ws = _workspace(nbytes, dev, workspace)
     st = lib().specvocab_head_forward(
         _ptr(hidden), _ptr(w_down), _ptr(w_vocab), _ptr(u_full), M, d, dp, V, k,
-        float(temperature), _ptr(uniforms), _ptr(o["tokens"]), _ptr(o.get("topk_idx")),
-        _ptr(o.get("topk_prob")), _ptr(o.get("scores")), _ptr(ws), ws.numel(), _stream(stream))
+        float(temperature), int(seed), int(offset), _ptr(uniforms), _ptr(o["tokens"]),
+        _ptr(o.get("topk_idx")), _ptr(o.get("topk_prob")), _ptr(o.get("topk_logits")),
+        _ptr(o.get("scores")), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "specvocab_head_forward")
     return o
 
@@ -257,9 +280,10 @@ def ss_topk_rows(scores, k, *, out=None, stream=None):
 
 
 def spec_verify(target_logits, draft_logits, draft_tokens, temperature=0.0, uniforms=None, *,
-                workspace=None, out=None, stream=None) -> dict:
+                seed=0, offset=0, workspace=None, out=None, stream=None) -> dict:
     """Verification of B sequences: target (B, g+1, V), draft (B, g, V) fp32,
-    draft_tokens (B, g) int32, uniforms (B, g+1) fp32 when temperature > 0."""
+    draft_tokens (B, g) int32.  Sampling draws u[b, j] from Philox4x32-10 at
+    (seed, offset, row b, slot j), or takes uniforms (B, g+1) fp32 when given."""
     B, g1, V = target_logits.shape
     gamma = g1 - 1
     dev = target_logits.device
@@ -272,21 +296,21 @@ def spec_verify(target_logits, draft_logits, draft_tokens, temperature=0.0, unif
     ws = _workspace(nbytes, dev, workspace)
     st = lib().spec_verify(
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, gamma, V,
-        float(temperature), _ptr(uniforms), _ptr(o["tokens"]), _ptr(o["num_accepted"]),
-        _ptr(ws), ws.numel(), _stream(stream))
+        float(temperature), int(seed), int(offset), _ptr(uniforms), _ptr(o["tokens"]),
+        _ptr(o["num_accepted"]), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "spec_verify")
     return o
 
 
 def spec_verify_lowrank(target_logits, z, w_up, draft_logprob, draft_lse, draft_tokens,
-                        temperature, uniforms, *, position_major=True, workspace=None, out=None,
-                        stream=None) -> dict:
+                        temperature, uniforms=None, *, seed=0, offset=0, position_major=True,
+                        workspace=None, out=None, stream=None) -> dict:
     """Sampling verification of B sequences with the draft side from the
     low-rank head: target (B, g+1, V) fp32; z (g*B, r) bf16 in position-major
     order (row j*B + b: g head calls of B rows), or (B*g, r) sequence-major
     with position_major=False; draft_logprob, draft_lse fp32 in the same
     order; w_up (V, r) bf16; draft_tokens int32 in the same order;
-    uniforms (B, g+1)."""
+    uniforms (B, g+1), or None for the Philox stream at (seed, offset)."""
     B, g1, V = target_logits.shape
     gamma = g1 - 1
     r = z.shape[-1]
@@ -301,14 +325,16 @@ def spec_verify_lowrank(target_logits, z, w_up, draft_logprob, draft_lse, draft_
     ws = _workspace(nbytes, dev, workspace)
     st = lib().spec_verify_lowrank(
         _ptr(target_logits), _ptr(z), _ptr(w_up), _ptr(draft_logprob), _ptr(draft_lse), ss, sp,
-        r, _ptr(draft_tokens), B, gamma, V, float(temperature), _ptr(uniforms),
+        r, _ptr(draft_tokens), B, gamma, V, float(temperature), int(seed), int(offset),
+        _ptr(uniforms),
         _ptr(o["tokens"]), _ptr(o["num_accepted"]), _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "spec_verify_lowrank")
     return o
 
 
 def trimmed_head_forward(hidden, w_kept, kept_ids, temperature=0.0, uniforms=None, *,
-                         want_stats=True, workspace=None, out=None, stream=None) -> dict:
+                         seed=0, offset=0, want_stats=True, workspace=None, out=None,
+                         stream=None) -> dict:
     """Dense head over the kept vocabulary rows w_kept (V_kept, d) bf16 with
     their ids kept_ids (V_kept,) int32; hidden (M, d) bf16.  Returns 'tokens'
     (vocabulary ids) and, with want_stats, 'logprob', 'row_max', 'lse' over
@@ -326,10 +352,32 @@ def trimmed_head_forward(hidden, w_kept, kept_ids, temperature=0.0, uniforms=Non
     nbytes = trimmed_head_workspace_size(M, d, Vk)
     ws = _workspace(nbytes, dev, workspace)
     st = lib().trimmed_head_forward(
-        _ptr(hidden), _ptr(w_kept), _ptr(kept_ids), M, d, Vk, float(temperature), _ptr(uniforms),
+        _ptr(hidden), _ptr(w_kept), _ptr(kept_ids), M, d, Vk, float(temperature), int(seed),
+        int(offset), _ptr(uniforms),
         _ptr(o["tokens"]), _ptr(o.get("logprob")), _ptr(o.get("row_max")), _ptr(o.get("lse")),
         _ptr(ws), ws.numel(), _stream(stream))
     _check(st, "trimmed_head_forward")
+    return o
+
+
+def ss_philox_uniforms(seed, offset, rows, slots, *, device=None, stream=None):
+    """The (rows, slots) float32 uniforms a sampling call draws at (seed,
+    offset) when given no uniforms of its own, computed on the device."""
+    dev = device if device is not None else torch.device("cuda", torch.cuda.current_device())
+    o = torch.empty(rows, slots, dtype=torch.float32, device=dev)
+    _check(lib().ss_philox_uniforms(int(seed), int(offset), rows, slots, _ptr(o),
+                                    _stream(stream)), "ss_philox_uniforms")
+    return o
+
+
+def ss_philox4x32_10(blocks, *, stream=None):
+    """Raw Philox4x32-10: blocks (n, 6) int32/uint32 words (counter c0..c3, key
+    k0, k1) on a CUDA device -> (n, 4) output words as int32 (bit patterns)."""
+    n = blocks.shape[0]
+    if blocks.dim() != 2 or blocks.shape[1] != 6 or blocks.element_size() != 4:
+        raise ValueError("blocks must be (n, 6) 32-bit words")
+    o = torch.empty(n, 4, dtype=torch.int32, device=blocks.device)
+    _check(lib().ss_philox4x32_10(_ptr(blocks), n, _ptr(o), _stream(stream)), "ss_philox4x32_10")
     return o
 
 
@@ -360,6 +408,17 @@ def profile_read(keep: bool = False) -> dict:
            "ss_profile_read")
     return {lib().ss_profile_kind_name(k).decode(): (launches[k], ms[k])
             for k in range(n) if launches[k]}
+
+
+def ss_set_wait_limit_ns(limit_ns: int):
+    """Limit of the kernels' pipeline waits on the current device (default 1 s)."""
+    _check(lib().ss_set_wait_limit_ns(int(limit_ns)), "ss_set_wait_limit_ns")
+
+
+def ss_set_stall_test(on: bool):
+    """Test switch: the tensor-core up-projection waits on a barrier nothing
+    arrives on, so its calls time out (SS_ERR_TIMEOUT) instead of running."""
+    _check(lib().ss_set_stall_test(1 if on else 0), "ss_set_stall_test")
 
 
 def ss_get_device_error(stream=None) -> int:

@@ -5,6 +5,7 @@
 // and enqueues the kernels of head.cu / verify.cu / specvocab.cu on the
 // caller's stream.  No entry point allocates, frees or synchronises.
 #include <math.h>
+#include <stddef.h>
 #include <stdint.h>
 
 #include "../../include/slimspec.h"
@@ -13,8 +14,9 @@
 
 namespace ss {
 
-// Per-device error word (one instance per device the library is loaded on).
-__device__ unsigned int g_error_word = 0;
+// Per-device control block (one instance per device the library is loaded
+// on): the error word, the stall test switch, the pipeline wait limit.
+__device__ DeviceControl g_control = {0u, 0u, kWaitLimitNs};
 
 unsigned* error_word() {
   static unsigned* cached[64] = {nullptr};
@@ -22,8 +24,8 @@ unsigned* error_word() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
   if (cached[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
-    cached[dev] = static_cast<unsigned*>(p);
+    if (cudaGetSymbolAddress(&p, g_control) != cudaSuccess) return nullptr;
+    cached[dev] = &static_cast<DeviceControl*>(p)->err;
   }
   return cached[dev];
 }
@@ -81,19 +83,37 @@ const char* ss_status_string(int status) {
   }
 }
 
-int ss_version(void) { return 100; }
+int ss_version(void) { return 200; }
 
 int ss_get_device_error(cudaStream_t stream) {
   if (cudaStreamSynchronize(stream) != cudaSuccess) return SS_ERR_CUDA;
   unsigned v = 0;
-  if (cudaMemcpyFromSymbol(&v, g_error_word, sizeof(v)) != cudaSuccess) return SS_ERR_CUDA;
+  if (cudaMemcpyFromSymbol(&v, g_control, sizeof(v), offsetof(DeviceControl, err)) != cudaSuccess)
+    return SS_ERR_CUDA;
   if (v != 0) {
     const unsigned zero = 0;
-    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(zero)) != cudaSuccess) return SS_ERR_CUDA;
+    if (cudaMemcpyToSymbol(g_control, &zero, sizeof(zero), offsetof(DeviceControl, err)) !=
+        cudaSuccess)
+      return SS_ERR_CUDA;
   }
   if (v & kErrTimeout) return SS_ERR_TIMEOUT;
   if (v & kErrIndex) return SS_ERR_DEVICE_INDEX;
   return SS_OK;
+}
+
+int ss_set_wait_limit_ns(uint64_t limit_ns) {
+  if (limit_ns > 10 * kWaitLimitNs) return SS_ERR_INVALID_ARG;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SS_ERR_CUDA;
+  const unsigned long long v = limit_ns;
+  return cuda_status(
+      cudaMemcpyToSymbol(g_control, &v, sizeof(v), offsetof(DeviceControl, wait_limit_ns)));
+}
+
+int ss_set_stall_test(int on) {
+  if (cudaDeviceSynchronize() != cudaSuccess) return SS_ERR_CUDA;
+  const unsigned v = on ? 1u : 0u;
+  return cuda_status(
+      cudaMemcpyToSymbol(g_control, &v, sizeof(v), offsetof(DeviceControl, stall_head)));
 }
 
 // ------------------------------------------------------------------- head --
@@ -122,16 +142,16 @@ size_t trimmed_head_workspace_size(int M, int d, int V_kept) {
 }
 
 int trimmed_head_forward(const void* hidden, const void* w_kept, const int32_t* kept_ids, int M,
-                         int d, int V_kept, float temperature, const float* uniforms,
-                         int32_t* out_tokens, float* out_logprob, float* out_row_max,
-                         float* out_row_lse, void* workspace, size_t workspace_bytes,
-                         cudaStream_t stream) {
+                         int d, int V_kept, float temperature, uint64_t seed, uint64_t offset,
+                         const float* uniforms, int32_t* out_tokens, float* out_logprob,
+                         float* out_row_max, float* out_row_lse, void* workspace,
+                         size_t workspace_bytes, cudaStream_t stream) {
   if (M < 0 || d <= 0 || d % 8 != 0 || V_kept <= 0 || !temp_ok(temperature))
     return SS_ERR_INVALID_ARG;
   if ((long long)V_kept * d * 2 >= (1LL << 40)) return SS_ERR_UNSUPPORTED;
   if (M == 0) return SS_OK;
   if (!hidden || !w_kept || !kept_ids || !out_tokens) return SS_ERR_INVALID_ARG;
-  if (temperature > 0.f && (!uniforms || !aligned(uniforms, 4))) return SS_ERR_INVALID_ARG;
+  if (uniforms && !aligned(uniforms, 4)) return SS_ERR_INVALID_ARG;
   if (!aligned(hidden, 16) || !aligned(w_kept, 16) || !aligned(kept_ids, 4) ||
       !aligned(out_tokens, 4) || (out_logprob && !aligned(out_logprob, 4)) ||
       (out_row_max && !aligned(out_row_max, 4)) || (out_row_lse && !aligned(out_row_lse, 4)))
@@ -149,7 +169,8 @@ int trimmed_head_forward(const void* hidden, const void* w_kept, const int32_t* 
   // the rows of h are the tensor-core kernel's z; its tile counters start at 0
   cudaError_t e = cudaMemsetAsync(ctr, 0, kMmaCtrs * sizeof(unsigned), stream);
   if (e != cudaSuccess) return cuda_status(e);
-  const HeadOutputs outs{uniforms, out_tokens, out_logprob, out_row_max, out_row_lse, kept_ids};
+  const HeadOutputs outs{Draws{uniforms, seed, offset}, out_tokens, out_logprob, out_row_max,
+                         out_row_lse, kept_ids};
   e = launch_head_mma(mp, hidden, w_kept, M, d, V_kept, temperature, wk, outs, nullptr, ctr,
                       stream);
   return cuda_status(e);
@@ -161,10 +182,11 @@ size_t slimspec_head_workspace_size(int M, int d, int r, int V, int dtype) {
 }
 
 int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_up, int M, int d,
-                          int r, int V, int dtype, float temperature, const float* uniforms,
-                          int32_t* out_tokens, float* out_logprob, float* out_row_max,
-                          float* out_row_lse, void* out_z, float* out_logits, void* workspace,
-                          size_t workspace_bytes, cudaStream_t stream) {
+                          int r, int V, int dtype, float temperature, uint64_t seed,
+                          uint64_t offset, const float* uniforms, int32_t* out_tokens,
+                          float* out_logprob, float* out_row_max, float* out_row_lse, void* out_z,
+                          float* out_logits, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream) {
   int st = head_check(M, d, r, V, dtype);
   if (st != SS_OK) return st;
   if (!temp_ok(temperature)) return SS_ERR_INVALID_ARG;
@@ -175,7 +197,7 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
       (out_row_max && !aligned(out_row_max, 4)) || (out_row_lse && !aligned(out_row_lse, 4)) ||
       (out_z && !aligned(out_z, 4)) || (out_logits && !aligned(out_logits, 4)))
     return SS_ERR_INVALID_ARG;
-  if (temperature > 0.f && (!uniforms || !aligned(uniforms, 4))) return SS_ERR_INVALID_ARG;
+  if (uniforms && !aligned(uniforms, 4)) return SS_ERR_INVALID_ARG;
   const bool bf16 = dtype == SS_BF16;
   const size_t need = head_ws_bytes(M, r, V, bf16);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return SS_ERR_WORKSPACE;
@@ -189,7 +211,8 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
     wk.psum = cv.take<float>((size_t)M * mp.n_sub);
     wk.parg = cv.take<int>((size_t)M * mp.n_sub);
     unsigned* ctr = cv.take<unsigned>(2 * kMmaCtrs);
-    const HeadOutputs outs{uniforms, out_tokens, out_logprob, out_row_max, out_row_lse};
+    const HeadOutputs outs{Draws{uniforms, seed, offset}, out_tokens, out_logprob, out_row_max,
+                           out_row_lse};
     // many rows of h: the down-projection as a split-K tensor-core GEMM, its
     // fp32 slices in the (not yet used) partial arrays, contiguous from pmax
     const size_t part_cap = 3 * align256((size_t)M * mp.n_sub * sizeof(float));
@@ -217,7 +240,8 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
   part.csum = cv.take<float>((size_t)M * plan.grid);
   part.carg = cv.take<int>((size_t)M * plan.grid);
   part.ctr = cv.take<unsigned>((size_t)plan.n_launch);
-  const HeadOutputs outs{uniforms, out_tokens, out_logprob, out_row_max, out_row_lse};
+  const HeadOutputs outs{Draws{uniforms, seed, offset}, out_tokens, out_logprob, out_row_max,
+                           out_row_lse};
 
   cudaError_t e = launch_down_proj(bf16, hidden, w_down, M, d, r, bf16, z_ws, out_z, part.ctr,
                                    plan.n_launch, stream);
@@ -245,8 +269,9 @@ size_t specvocab_head_workspace_size(int M, int d, int d_prime, int V, int k) {
 
 int specvocab_head_forward(const void* hidden, const void* w_down, const void* w_vocab,
                            const void* u_full, int M, int d, int d_prime, int V, int k,
-                           float temperature, const float* uniforms, int32_t* out_tokens,
-                           int32_t* out_topk_idx, float* out_topk_prob, float* out_scores,
+                           float temperature, uint64_t seed, uint64_t offset,
+                           const float* uniforms, int32_t* out_tokens, int32_t* out_topk_idx,
+                           float* out_topk_prob, float* out_topk_logits, float* out_scores,
                            void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   int st = sv_check(M, d, d_prime, V, k);
   if (st != SS_OK) return st;
@@ -256,14 +281,16 @@ int specvocab_head_forward(const void* hidden, const void* w_down, const void* w
   if (!aligned(hidden, 16) || !aligned(w_down, 16) || !aligned(w_vocab, 16) || !aligned(u_full, 16))
     return SS_ERR_INVALID_ARG;
   if (!aligned(out_tokens, 4) || (out_topk_idx && !aligned(out_topk_idx, 4)) ||
-      (out_topk_prob && !aligned(out_topk_prob, 4)) || (out_scores && !aligned(out_scores, 4)))
+      (out_topk_prob && !aligned(out_topk_prob, 4)) ||
+      (out_topk_logits && !aligned(out_topk_logits, 4)) || (out_scores && !aligned(out_scores, 4)))
     return SS_ERR_INVALID_ARG;
-  if (temperature > 0.f && (!uniforms || !aligned(uniforms, 4))) return SS_ERR_INVALID_ARG;
+  if (uniforms && !aligned(uniforms, 4)) return SS_ERR_INVALID_ARG;
   const size_t need = specvocab_ws_bytes(M, d, d_prime, V, k);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return SS_ERR_WORKSPACE;
   return cuda_status(launch_specvocab(hidden, w_down, w_vocab, u_full, M, d, d_prime, V, k,
-                                      temperature, uniforms, out_tokens, out_topk_idx,
-                                      out_topk_prob, out_scores, workspace, stream));
+                                      temperature, Draws{uniforms, seed, offset}, out_tokens,
+                                      out_topk_idx, out_topk_prob, out_topk_logits, out_scores,
+                                      workspace, stream));
 }
 
 size_t ss_topk_workspace_size(int M, int V, int k) {
@@ -294,9 +321,9 @@ size_t spec_verify_lowrank_workspace_size(int B, int gamma, int V, int r) {
 int spec_verify_lowrank(const float* target_logits, const void* z, const void* w_up,
                         const float* draft_logprob, const float* draft_lse, int seq_stride,
                         int pos_stride, int r, const int32_t* draft_tokens, int B, int gamma,
-                        int V, float temperature, const float* uniforms, int32_t* out_tokens,
-                        int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
-                        cudaStream_t stream) {
+                        int V, float temperature, uint64_t seed, uint64_t offset,
+                        const float* uniforms, int32_t* out_tokens, int32_t* out_num_accepted,
+                        void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (B < 0 || gamma < 1 || gamma > 32 || V <= 0 || r <= 0 || seq_stride < 0 || pos_stride < 0 ||
       !(temperature > 0.f) || !temp_ok(temperature))
     return SS_ERR_INVALID_ARG;
@@ -307,24 +334,25 @@ int spec_verify_lowrank(const float* target_logits, const void* z, const void* w
   // the recompute: B <= 256 rows; its finish holds a z row in two chunks per lane
   if (r > 512 || !mma_plan(r, B, V).ok) return SS_ERR_UNSUPPORTED;
   if (!target_logits || !z || !w_up || !draft_logprob || !draft_lse || !draft_tokens ||
-      !uniforms || !out_tokens || !out_num_accepted)
+      !out_tokens || !out_num_accepted)
     return SS_ERR_INVALID_ARG;
   if (!aligned(target_logits, 16) || !aligned(z, 16) || !aligned(w_up, 16) ||
       !aligned(draft_logprob, 4) || !aligned(draft_lse, 4) || !aligned(draft_tokens, 4) ||
-      !aligned(uniforms, 4) || !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4))
+      (uniforms && !aligned(uniforms, 4)) || !aligned(out_tokens, 4) ||
+      !aligned(out_num_accepted, 4))
     return SS_ERR_INVALID_ARG;
   const size_t need = verify_lowrank_ws_bytes(B, gamma, V, r);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return SS_ERR_WORKSPACE;
   return cuda_status(launch_verify_lowrank(target_logits, z, w_up, draft_logprob, draft_lse,
                                            seq_stride, pos_stride, r, draft_tokens, B, gamma, V,
-                                           temperature, uniforms, out_tokens, out_num_accepted,
-                                           workspace, stream));
+                                           temperature, Draws{uniforms, seed, offset}, out_tokens,
+                                           out_num_accepted, workspace, stream));
 }
 
 int spec_verify(const float* target_logits, const float* draft_logits, const int32_t* draft_tokens,
-                int B, int gamma, int V, float temperature, const float* uniforms,
-                int32_t* out_tokens, int32_t* out_num_accepted, void* workspace,
-                size_t workspace_bytes, cudaStream_t stream) {
+                int B, int gamma, int V, float temperature, uint64_t seed, uint64_t offset,
+                const float* uniforms, int32_t* out_tokens, int32_t* out_num_accepted,
+                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
   if (B < 0 || gamma < 1 || gamma > 32 || V <= 0 || !temp_ok(temperature))
     return SS_ERR_INVALID_ARG;
   if ((long long)B * (gamma + 1) * V >= (1LL << 40)) return SS_ERR_UNSUPPORTED;
@@ -335,7 +363,7 @@ int spec_verify(const float* target_logits, const float* draft_logits, const int
   if (B == 0) return SS_OK;
   const bool sample = temperature > 0.f;
   if (!target_logits || !draft_tokens || !out_tokens || !out_num_accepted) return SS_ERR_INVALID_ARG;
-  if (sample && (!draft_logits || !uniforms)) return SS_ERR_INVALID_ARG;
+  if (sample && !draft_logits) return SS_ERR_INVALID_ARG;
   if (!aligned(target_logits, 16) || (draft_logits && !aligned(draft_logits, 16)) ||
       !aligned(draft_tokens, 4) || !aligned(out_tokens, 4) || !aligned(out_num_accepted, 4) ||
       (uniforms && !aligned(uniforms, 4)))
@@ -343,8 +371,25 @@ int spec_verify(const float* target_logits, const float* draft_logits, const int
   const size_t need = verify_ws_bytes(B, gamma, V, sample);
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return SS_ERR_WORKSPACE;
   return cuda_status(launch_verify(target_logits, draft_logits, draft_tokens, B, gamma, V,
-                                   temperature, uniforms, out_tokens, out_num_accepted, workspace,
-                                   stream));
+                                   temperature, Draws{uniforms, seed, offset}, out_tokens,
+                                   out_num_accepted, workspace, stream));
+}
+
+// ------------------------------------------------------- Philox uniforms --
+int ss_philox_uniforms(uint64_t seed, uint64_t offset, int rows, int slots, float* out,
+                       cudaStream_t stream) {
+  if (rows < 0 || slots < 0) return SS_ERR_INVALID_ARG;
+  if ((long long)rows * slots == 0) return SS_OK;
+  if ((long long)rows * slots >= (1LL << 31)) return SS_ERR_UNSUPPORTED;
+  if (!out || !aligned(out, 4)) return SS_ERR_INVALID_ARG;
+  return cuda_status(launch_philox_uniforms(seed, offset, rows, slots, out, stream));
+}
+
+int ss_philox4x32_10(const uint32_t* blocks, int n, uint32_t* out, cudaStream_t stream) {
+  if (n < 0) return SS_ERR_INVALID_ARG;
+  if (n == 0) return SS_OK;
+  if (!blocks || !out || !aligned(blocks, 4) || !aligned(out, 4)) return SS_ERR_INVALID_ARG;
+  return cuda_status(launch_philox_blocks(blocks, n, out, stream));
 }
 
 }  // extern "C"

@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(256) k_down_proj(const uint8_t* __restrict__ h
 
 // -------------------------------------------------------- per-row finish ----
 struct HeadOut {
-  const float* uniforms;
+  Draws draws;  // row m draws (row m, slot 0)
   int32_t* tokens;
   float* logprob;
   float* row_max;
@@ -374,7 +374,8 @@ __device__ __forceinline__ void finish_row(int m, const uint8_t* __restrict__ w,
     acc = __fadd_rn(acc, cmass[k]);
   }
   const float W = warp_sum_fixed(acc);
-  const float target = __ldg(out.uniforms + m) * W;
+  const float target =
+      draw_uniform(out.draws.uniforms, out.draws.seed, out.draws.offset, m, 0, 1) * W;
   // 3. the CTA, then the sub-tile inside it, where the running mass passes u * W
   float before1 = 0.f, before2 = 0.f;
   const int cta = ordered_crossing_regs<kFinChunks>(grid, target, cmass, before1, lane);
@@ -423,9 +424,13 @@ __device__ __forceinline__ void finish_row(int m, const uint8_t* __restrict__ w,
     if (n_chunks > 1) issue_chunk(1);
   }
   bool ok = true;
+  int kfail = n_chunks;
   for (int k = 0; k < n_chunks; ++k) {
     ok = ok && __all_sync(0xFFFFFFFFu, mbar_wait_bounded(&fbar[k & 1], (k >> 1) & 1, err));
-    if (!ok) break;
+    if (!ok) {
+      kfail = k;
+      break;
+    }
     const int r0 = k * crows, nr = min(crows, n - r0);
     const uint32_t sb = smem_u32(fsmem + (k & 1) * (kFinBytes / 2));
 #pragma unroll 1
@@ -445,8 +450,17 @@ __device__ __forceinline__ void finish_row(int m, const uint8_t* __restrict__ w,
       issue_chunk(k + 2);
     }
   }
-  if (!ok) {  // a copy did not arrive in time: leave the row's token invalid
-    if (lane == 0) out.tokens[m] = -1;
+  if (!ok) {
+    // a copy did not arrive in time: leave the row's token invalid, after
+    // the copies still in flight into this warp's buffers have landed
+    // (chunks kfail and kfail + 1: each later one is issued only after the
+    // one two before it was consumed)
+    if (lane == 0) {
+      out.tokens[m] = -1;
+      for (int k = kfail; k < n_chunks && k < kfail + 2; ++k)
+        mbar_wait_drain(&fbar[k & 1], (k >> 1) & 1, err);
+    }
+    __syncwarp();
     return;
   }
   __syncwarp();
@@ -633,7 +647,7 @@ __global__ void __launch_bounds__(32 * G::WARPS, 1)
       // warp's ring before the CTA's shared memory is released.
       for (int k = s; k < n_stages && k < s + G::NST; ++k) {
         int row0;
-        if (stage_rows(k, row0) > 0) mbar_wait_bounded(&bars[k % G::NST], (k / G::NST) & 1, err);
+        if (stage_rows(k, row0) > 0) mbar_wait_drain(&bars[k % G::NST], (k / G::NST) & 1, err);
       }
     }
   }
@@ -792,7 +806,7 @@ static cudaError_t stream_one(const void* w_up, const void* z_ws, int M, int r, 
   cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), G::SMEM);
   if (e != cudaSuccess) return e;
   const int grid = plan.grid;
-  HeadOut out{o.uniforms, o.tokens, o.logprob, o.row_max, o.row_lse};
+  HeadOut out{o.draws, o.tokens, o.logprob, o.row_max, o.row_lse};
   for (int m0 = 0, k = 0; m0 < M; m0 += G::MTL, ++k) {
     ProfScope ps(kKHeadStream, st);
     const HeadPart hp{part.pmax, part.psum, part.parg, part.cmax, part.csum, part.carg};

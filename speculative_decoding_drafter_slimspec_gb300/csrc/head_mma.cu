@@ -277,7 +277,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kStageBytes = (kWide ? KPS : 1) * kBlockBytes;
   const int SPT = kWide ? KB / KPS : KB;       // stages per vocabulary tile
   __shared__ uint64_t full[kMaxStages], empty[kMaxStages], a_full, acc_full[2], acc_empty[2];
-  __shared__ uint64_t tile_full[kTileRing], tile_empty[kTileRing], mma_done;
+  __shared__ uint64_t tile_full[kTileRing], tile_empty[kTileRing], mma_done, never;
   __shared__ int s_tile[kTileRing];    // vocabulary tile ids, -1 = no more
   __shared__ int s_fills[kMaxStages];  // TMA fills issued per stage (drained before exit)
   __shared__ uint32_t s_tmem;
@@ -302,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&acc_empty[0], kEpiWarps);
     mbar_init(&acc_empty[1], kEpiWarps);
     mbar_init(&mma_done, 1);
+    mbar_init(&never, 1);  // nothing arrives on it: the stall test's wait
     s_abort = 0;
     fence_mbar_init();
   }
@@ -390,7 +391,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == kMmaWarp) {
     // ---------------------------------------------------------- MMA issuer --
     if (lane == 0) {
-      bool ok = mbar_wait_bounded(&a_full, 0, err);
+      // the failure-detection test: with the control block's switch on, the
+      // issuer first waits on a barrier that nothing arrives on, runs out of
+      // time, and the whole CTA takes its abort path
+      bool ok = !(err != nullptr && control(err)->stall_head != 0u) ||
+                mbar_wait_bounded(&never, 0, err);
+      ok = ok && mbar_wait_bounded(&a_full, 0, err);
       tc_fence_after();
       int it = 0;
       for (int i = 0; ok; ++i) {
@@ -428,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) s_abort = 1;
       // every MMA this thread issued has completed before TMEM is freed
       mma_commit(&mma_done);
-      mbar_wait_bounded(&mma_done, 0, err);
+      mbar_wait_drain(&mma_done, 0, err);
     }
     __syncwarp();
   } else {
@@ -574,7 +580,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // may still be in flight there.
     if (lane == 0 && *(volatile int*)&s_abort)
       for (int s = 0; s < NST; ++s)
-        if (s_fills[s] > 0) mbar_wait_bounded(&full[s], (s_fills[s] - 1) & 1, err);
+        if (s_fills[s] > 0) mbar_wait_drain(&full[s], (s_fills[s] - 1) & 1, err);
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kCols);
@@ -640,7 +646,7 @@ __global__ void __launch_bounds__(kDownThreads, 1)
     s_ok = ok ? 1 : 0;
     mma_commit(&done);  // also after an abort: every issued MMA completes first
   }
-  const bool done_ok = mbar_wait_bounded(&done, 0, err);
+  const bool done_ok = mbar_wait_drain(&done, 0, err);
   __syncthreads();
   tc_fence_after();
   const bool all_ok = s_ok != 0 && __syncthreads_and(done_ok ? 1 : 0) != 0;
@@ -679,7 +685,7 @@ __global__ void __launch_bounds__(kDownThreads, 1)
   if (warp == 0) {
     // no copy may still land in shared memory after an abort: wait (bounded)
     // for the loads once more
-    if (lane == 0 && !all_ok) mbar_wait_bounded(&full, 0, err);
+    if (lane == 0 && !all_ok) mbar_wait_drain(&full, 0, err);
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, kTileN);
@@ -802,7 +808,10 @@ __global__ void __launch_bounds__(kFinThreads)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x;
   pdl_launch_dependents();  // the next call's down-projection may start reading
-  const float u = (kSample && m < M) ? __ldg(out.uniforms + m) : 0.f;  // an input
+  // an input (or the counter-based stream): read before the wait
+  const float u = (kSample && m < M) ? draw_uniform(out.draws.uniforms, out.draws.seed,
+                                                    out.draws.offset, m, 0, 1)
+                                     : 0.f;
   pdl_wait_producer();
   if (m >= M) return;
   const int per = (n_sub + kFinThreads - 1) / kFinThreads;
@@ -829,7 +838,10 @@ __global__ void __launch_bounds__(kFinThreads)
   const float gmax = best.v;
   if (!kSample) {
     if (threadIdx.x == 0) {
-      out.tokens[m] = out.id_map != nullptr ? out.id_map[best.i] : best.i;
+      // (an index outside the vocabulary only comes from partials an aborted
+      // up-projection never wrote: no token then, and no id-map read)
+      const bool in = best.i >= 0 && best.i < V;
+      out.tokens[m] = !in ? -1 : out.id_map != nullptr ? out.id_map[best.i] : best.i;
       if (out.logprob) out.logprob[m] = 0.f;
       if (out.row_max) out.row_max[m] = gmax;
       if (out.row_lse) out.row_lse[m] = gmax;

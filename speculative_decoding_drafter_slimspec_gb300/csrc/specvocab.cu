@@ -398,7 +398,7 @@ __global__ void __launch_bounds__(256)
 // owns the contiguous range [t*seg, (t+1)*seg).
 __global__ void __launch_bounds__(256)
     k_cand_finish(const float* __restrict__ zc, const int32_t* __restrict__ idx, int k, float c,
-                  const float* __restrict__ uniforms, int32_t* __restrict__ out_tokens,
+                  Draws dr, int32_t* __restrict__ out_tokens,
                   int32_t* __restrict__ out_idx, float* __restrict__ out_prob) {
   constexpr int NT = 256;
   pdl_launch_dependents();  // the next call's down-projection may start reading
@@ -451,7 +451,7 @@ __global__ void __launch_bounds__(256)
     float run = 0.f;
     for (int q = 0; q < 8; ++q) { const float x = s_f[q]; s_f[q] = run; run = __fadd_rn(run, x); }
     s_W = run;
-    s_resid = uniforms[m] * run;
+    s_resid = draw_uniform(dr.uniforms, dr.seed, dr.offset, m, 0, 1) * run;
   }
   __syncthreads();
   const float W = s_W, target = s_resid;
@@ -573,9 +573,9 @@ size_t specvocab_ws_bytes(int M, int d, int d_prime, int V, int k) {
 
 cudaError_t launch_specvocab(const void* h, const void* w_down, const void* w_vocab,
                              const void* u_full, int M, int d, int d_prime, int V, int k,
-                             float temperature, const float* uniforms, int32_t* out_tokens,
-                             int32_t* out_idx, float* out_prob, float* out_scores, void* ws,
-                             cudaStream_t st) {
+                             float temperature, const Draws& draws, int32_t* out_tokens,
+                             int32_t* out_idx, float* out_prob, float* out_logits,
+                             float* out_scores, void* ws, cudaStream_t st) {
   if (M <= 0) return cudaSuccess;
   Carver cv(ws);
   void* hp = cv.take<uint8_t>((size_t)M * d_prime * 2);
@@ -600,7 +600,7 @@ cudaError_t launch_specvocab(const void* h, const void* w_down, const void* w_vo
     if (e != cudaSuccess) return e;
     const MmaPlan mp = mma_plan(d_prime, M, V);
     const MmaWork none{nullptr, nullptr, nullptr};
-    const HeadOutputs no_out{nullptr, nullptr, nullptr, nullptr, nullptr};
+    const HeadOutputs no_out{Draws{nullptr, 0, 0}, nullptr, nullptr, nullptr, nullptr};
     e = launch_head_mma(mp, hp, w_vocab, M, d_prime, V, 0.f, none, no_out, scores, ctr, st);
     if (e != cudaSuccess) return e;
   } else {
@@ -617,7 +617,7 @@ cudaError_t launch_specvocab(const void* h, const void* w_down, const void* w_vo
   cand = cv.take<int32_t>((size_t)M * k);
   zc = cv.take<float>((size_t)M * k);
   if (out_scores) scores = out_scores;
-  const HeadOutputs router_out{nullptr, router_arg, nullptr, nullptr, nullptr};
+  const HeadOutputs router_out{Draws{nullptr, 0, 0}, router_arg, nullptr, nullptr, nullptr};
 
   e = launch_down_proj(true, h, w_down, M, d, d_prime, true, hp, nullptr, part.ctr,
                        plan.n_launch, st);
@@ -628,6 +628,7 @@ cudaError_t launch_specvocab(const void* h, const void* w_down, const void* w_vo
   }
   e = launch_topk(scores, M, V, k, cand, nullptr, st);
   if (e != cudaSuccess) return e;
+  if (out_logits) zc = out_logits;  // the candidates' exact logits, requested as an output
   const dim3 grid(M, (k + 63) / 64);
   const int cpl = (d + 255) / 256;
   {
@@ -644,7 +645,7 @@ cudaError_t launch_specvocab(const void* h, const void* w_down, const void* w_vo
   }
   const float c = temperature > 0.f ? (float)(1.4426950408889634 / (double)temperature) : 0.f;
   ProfScope ps(kKCandFinish, st);
-  k_cand_finish<<<M, 256, 0, st>>>(zc, cand, k, c, uniforms, out_tokens, out_idx, out_prob);
+  k_cand_finish<<<M, 256, 0, st>>>(zc, cand, k, c, draws, out_tokens, out_idx, out_prob);
   return cudaGetLastError();
 }
 

@@ -1,8 +1,9 @@
 // ss_common.cuh -- device helpers shared by the sm_103a kernels of libslimspec.
 //
 // Holds: the per-device error word, bounded mbarrier waits, 1-D bulk copies
-// (cp.async.bulk) into shared memory, bf16 unpacking, lane reductions and the
-// (max, sum, argmax) running state of an online softmax.
+// (cp.async.bulk) into shared memory, bf16 unpacking, lane reductions, the
+// (max, sum, argmax) running state of an online softmax and the Philox4x32-10
+// uniforms of the sampling draws.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -15,10 +16,27 @@ namespace ss {
 // ------------------------------------------------------------------ errors --
 enum : unsigned { kErrTimeout = 1u, kErrIndex = 2u };
 
-// Kernels receive the device address of the library's per-device error word
-// and record anomalies in it with atomicOr (see ss_get_device_error).
+// A bounded wait gives up after this many nanoseconds and reports kErrTimeout.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
+
+// The per-device control block of the library.  Kernels receive the device
+// address of its first word, the error word, as `err` and record anomalies
+// there with atomicOr (see ss_get_device_error); the other words are read
+// only by the bounded waits: the limit of the pipeline waits (host-settable,
+// kWaitLimitNs by default) and a test switch that makes the tensor-core
+// head's MMA issuer wait on a barrier nothing arrives on.
+struct DeviceControl {
+  unsigned err;
+  unsigned stall_head;
+  unsigned long long wait_limit_ns;
+};
+
 __device__ __forceinline__ void raise_error(unsigned* err, unsigned bits) {
   if (err) atomicOr(err, bits);
+}
+
+__device__ __forceinline__ const volatile DeviceControl* control(const unsigned* err) {
+  return reinterpret_cast<const volatile DeviceControl*>(err);
 }
 
 // ------------------------------------------------------------ time / waits --
@@ -27,9 +45,6 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-
-// A bounded wait gives up after this many nanoseconds and reports kErrTimeout.
-constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -60,18 +75,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Waits for the phase with the given parity to complete.  Returns false (and
-// records kErrTimeout) if it has not completed within kWaitLimitNs.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* err) {
+// records kErrTimeout) if it has not completed within `limit_ns`.
+__device__ __forceinline__ bool mbar_wait_for(uint64_t* bar, uint32_t parity, unsigned* err,
+                                              uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
   while (true) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) {
+    if (global_ns() - t0 > limit_ns) {
       raise_error(err, kErrTimeout);
       return false;
     }
   }
+}
+
+// A wait of the pipeline (a stage to fill or free, an accumulator, a tile
+// id): bounded by the control block's host-settable limit.  After one of
+// these runs out, the caller abandons the pipeline and drains.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, unsigned* err) {
+  if (mbar_try_wait(bar, parity)) return true;
+  return mbar_wait_for(bar, parity, err, err ? control(err)->wait_limit_ns : kWaitLimitNs);
+}
+
+// A drain wait (copies or MMAs already issued, before their shared memory or
+// TMEM is released): always the fixed kWaitLimitNs, whatever the pipeline
+// limit, so that nothing in flight outlives the CTA.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, unsigned* err) {
+  return mbar_wait_for(bar, parity, err, kWaitLimitNs);
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
@@ -307,6 +338,47 @@ __device__ __forceinline__ int ordered_crossing_regs(int n, float target, const 
     before = before_last;
   }
   return sel;
+}
+
+// ------------------------------------------------------ Philox uniforms --
+// Philox4x32-10: J. K. Salmon, M. A. Moraes, R. O. Dror, D. E. Shaw, "Parallel
+// Random Numbers: As Easy as 1, 2, 3" (SC'11), section 4.  A round multiplies
+// counter words 0 and 2 by the paper's two 32-bit multipliers (full 64-bit
+// products), then permutes: word 0 = hi(M1 c2) ^ c1 ^ k0, word 1 = lo(M1 c2),
+// word 2 = hi(M0 c0) ^ c3 ^ k1, word 3 = lo(M0 c0).  The key advances by the
+// Weyl constants between rounds; ten rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    if (i > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+  }
+  return c;
+}
+
+// Uniform in [0, 1) of draw (row, slot) of the call (seed, offset): key =
+// (seed mod 2^32, seed >> 32), counter = (row, slot, offset mod 2^32,
+// offset >> 32), u = (first output word >> 8) * 2^-24 (exact in fp32).
+__device__ __forceinline__ float philox_uniform(uint64_t seed, uint64_t offset, uint32_t row,
+                                                uint32_t slot) {
+  const uint4 x = philox4x32_10(
+      make_uint4(row, slot, (uint32_t)offset, (uint32_t)(offset >> 32)), (uint32_t)seed,
+      (uint32_t)(seed >> 32));
+  return (float)(x.x >> 8) * 5.9604644775390625e-8f;  // 2^-24
+}
+
+// The uniform of draw (row, slot): the caller's uniforms[row * n_slots +
+// slot] when given, else the Philox stream at (seed, offset).
+__device__ __forceinline__ float draw_uniform(const float* uniforms, uint64_t seed,
+                                              uint64_t offset, uint32_t row, uint32_t slot,
+                                              uint32_t n_slots) {
+  if (uniforms != nullptr) return __ldg(uniforms + (size_t)row * n_slots + slot);
+  return philox_uniform(seed, offset, row, slot);
 }
 
 // Orderable 32-bit key of a float: larger float <=> larger key; -0 == +0.

@@ -39,6 +39,14 @@ int resident_blocks(const void* kernel, int threads, size_t smem);
 // a stream is being captured later.
 cudaError_t set_smem_once(const void* kernel, int bytes);
 
+// Where a call's sampling draws come from: the caller's uniforms (rows x
+// slots, row-major), or, when that is null, Philox4x32-10 at counter (row,
+// slot, offset) under key seed (see draw_uniform in ss_common.cuh).
+struct Draws {
+  const float* uniforms;
+  uint64_t seed, offset;
+};
+
 // Rounds a byte count up to the 256-byte workspace granule.
 inline size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -88,7 +96,7 @@ struct HeadPartials {
   unsigned* ctr;  // one completion counter per launch (zeroed by the down-projection)
 };
 struct HeadOutputs {
-  const float* uniforms;
+  Draws draws;    // one per row of z: (row m, slot 0)
   int32_t* tokens;
   float* logprob;
   float* row_max;
@@ -164,11 +172,11 @@ size_t verify_lowrank_ws_bytes(int B, int gamma, int V, int r);
 cudaError_t launch_verify_lowrank(const float* target, const void* z, const void* w_up,
                                   const float* logprob, const float* lse, int seq_stride,
                                   int pos_stride, int r, const int32_t* tokens, int B, int gamma,
-                                  int V, float temperature, const float* uniforms,
+                                  int V, float temperature, const Draws& draws,
                                   int32_t* out_tokens, int32_t* out_nacc, void* ws,
                                   cudaStream_t st);
 cudaError_t launch_verify(const float* target, const float* draft, const int32_t* tokens, int B,
-                          int gamma, int V, float temperature, const float* uniforms,
+                          int gamma, int V, float temperature, const Draws& draws,
                           int32_t* out_tokens, int32_t* out_nacc, void* ws, cudaStream_t st);
 
 // ------------------------------------------------------------- specvocab --
@@ -178,8 +186,14 @@ cudaError_t launch_topk(const float* scores, int M, int V, int k, int32_t* out_i
 size_t specvocab_ws_bytes(int M, int d, int d_prime, int V, int k);
 cudaError_t launch_specvocab(const void* h, const void* w_down, const void* w_vocab,
                              const void* u_full, int M, int d, int d_prime, int V, int k,
-                             float temperature, const float* uniforms, int32_t* out_tokens,
-                             int32_t* out_idx, float* out_prob, float* out_scores, void* ws,
-                             cudaStream_t st);
+                             float temperature, const Draws& draws, int32_t* out_tokens,
+                             int32_t* out_idx, float* out_prob, float* out_logits,
+                             float* out_scores, void* ws, cudaStream_t st);
+// Philox4x32-10 on the device (the generator behind Draws with no uniforms):
+// n blocks of (counter[4], key[2]) words -> out (n x 4 words); the (rows x
+// slots) uniforms of one call.
+cudaError_t launch_philox_blocks(const uint32_t* in, int n, uint32_t* out, cudaStream_t st);
+cudaError_t launch_philox_uniforms(uint64_t seed, uint64_t offset, int rows, int slots, float* out,
+                                   cudaStream_t st);
 
 }  // namespace ss

@@ -208,12 +208,12 @@ template <bool kSample>
 __device__ __forceinline__ PosInputs load_position(const float* __restrict__ target,
                                                    const DraftSide& ds,
                                                    const int32_t* __restrict__ tokens,
-                                                   const float* __restrict__ uniforms, int b,
-                                                   int j, int gamma, int V) {
+                                                   const Draws& dr, int b, int j, int gamma,
+                                                   int V) {
   const int g1 = gamma + 1;
   PosInputs in{tokens[(size_t)b * ds.ts + (size_t)j * ds.tp], 0.f, 0.f, 0.f};
   if (kSample) {
-    in.u = uniforms[(size_t)b * g1 + j];
+    in.u = draw_uniform(dr.uniforms, dr.seed, dr.offset, b, j, g1);
     if (ds.rows == nullptr) in.lq = ds.logprob[(size_t)b * ds.ss + (size_t)j * ds.sp];
     if (in.x >= 0 && in.x < V) {
       in.lp = target[((size_t)b * g1 + j) * V + in.x];
@@ -251,15 +251,14 @@ __global__ void __launch_bounds__(96)
     k_verify_first(const float* __restrict__ target, DraftSide ds,
                    const int32_t* __restrict__ tokens, int B, int gamma, int V, float c,
                    int n_chunks, const float* __restrict__ vmax, const float* __restrict__ vsum,
-                   const int* __restrict__ varg, const float* __restrict__ uniforms,
-                   int* __restrict__ seq_ok) {
+                   const int* __restrict__ varg, Draws dr, int* __restrict__ seq_ok) {
   __shared__ RowState s_st[2];
   __shared__ PosInputs s_in;
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.x;
   if (warp == 2) {  // inputs that do not depend on the row pass
-    if (lane == 0) s_in = load_position<kSample>(target, ds, tokens, uniforms, b, 0, gamma, V);
+    if (lane == 0) s_in = load_position<kSample>(target, ds, tokens, dr, b, 0, gamma, V);
   }
   pdl_wait_producer();
   if (warp == 0 || (kSample && warp == 1 && ds.rows != nullptr)) {
@@ -290,7 +289,7 @@ __global__ void __launch_bounds__(544)
     k_verify_decide(const float* __restrict__ target, DraftSide ds,
                     const int32_t* __restrict__ tokens, int B, int gamma, int V, float c,
                     int n_chunks, const float* __restrict__ vmax, const float* __restrict__ vsum,
-                    const int* __restrict__ varg, const float* __restrict__ uniforms,
+                    const int* __restrict__ varg, Draws dr,
                     const int* __restrict__ seq_ok, int32_t* __restrict__ out_tokens,
                     int32_t* __restrict__ out_nacc, VerifyInfo* __restrict__ info,
                     unsigned* err) {
@@ -307,7 +306,7 @@ __global__ void __launch_bounds__(544)
   if (lowrank && b == 0 && threadIdx.x < kMmaCtrs) ds.mma_ctr[threadIdx.x] = 0u;  // recompute's
   if (warp == n_merge) {
     if (lane < gamma) {
-      const PosInputs in = load_position<kSample>(target, ds, tokens, uniforms, b, lane, gamma, V);
+      const PosInputs in = load_position<kSample>(target, ds, tokens, dr, b, lane, gamma, V);
       if (in.x < 0 || in.x >= V) raise_error(err, kErrIndex);
       s_in[lane] = in;
     }
@@ -450,7 +449,7 @@ __global__ void __launch_bounds__(256)
                     int qp, int B, int gamma, int V, float c, int n_chunks,
                     const float* __restrict__ vmax,
                     const float* __restrict__ vsum, const VerifyInfo* __restrict__ info,
-                    const float* __restrict__ rmass, const float* __restrict__ uniforms,
+                    const float* __restrict__ rmass, Draws dr,
                     int32_t* __restrict__ out_tokens) {
   constexpr int NT = 256, PER = kVChunk / NT;  // contiguous elements per thread
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -486,7 +485,7 @@ __global__ void __launch_bounds__(256)
     float mass[NC];
 #pragma unroll
     for (int k = 0; k < NC; ++k) mass[k] = mode == 0 ? rm[k] : pmass[k];
-    const float target_mass = uniforms[(size_t)b * g1 + gamma] * R;
+    const float target_mass = draw_uniform(dr.uniforms, dr.seed, dr.offset, b, gamma, g1) * R;
     float before = 0.f;
     const int sel = ordered_crossing_regs<NC>(n_chunks, target_mass, mass, before, lane);
     if (lane == 0) {
@@ -568,8 +567,8 @@ __global__ void __launch_bounds__(256)
     k_verify_lr_finish(const ResidRow* __restrict__ rows, const VerifyInfo* __restrict__ info,
                        const uint8_t* __restrict__ w_up, const uint16_t* __restrict__ z_sel, int r,
                        int V, float c, int n_sub, const float* __restrict__ rmass,
-                       const float* __restrict__ pmass, const float* __restrict__ uniforms,
-                       int gamma, int32_t* __restrict__ out_tokens) {
+                       const float* __restrict__ pmass, Draws dr, int gamma,
+                       int32_t* __restrict__ out_tokens) {
   constexpr int NT = 256, kW = 64;
   __shared__ float s_wsum[NT / 32], s_rsum[NT / 32];
   __shared__ float s_w[kW];
@@ -579,7 +578,7 @@ __global__ void __launch_bounds__(256)
   const int g1 = gamma + 1;
   const ResidRow rr = rows[b];
   const int n = info[b].n;
-  const float u = uniforms[(size_t)b * g1 + gamma];
+  const float u = draw_uniform(dr.uniforms, dr.seed, dr.offset, b, gamma, g1);
   const int per = (n_sub + NT - 1) / NT;
   const int j0 = min(n_sub, tid * per), nj = min(n_sub, j0 + per) - j0;
   float rm[kLrPer], pm[kLrPer];
@@ -784,7 +783,7 @@ cudaError_t launch_pdl(Kern kern, int grid, int block, cudaStream_t st, Args... 
 // `w_up`, the drafter's V x r up-projection, for the recompute).
 cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
                         const int32_t* tokens, int B, int gamma, int V, float temperature,
-                        const float* uniforms, int32_t* out_tokens, int32_t* out_nacc, void* ws,
+                        const Draws& dr, int32_t* out_tokens, int32_t* out_nacc, void* ws,
                         cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
   const bool sample = temperature > 0.f;
@@ -853,10 +852,10 @@ cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
       ProfScope ps(kKVerifyFirst, st);
       e = sample ? launch_pdl(k_verify_first<true>, B, 96, st, target, ds, tokens, B, gamma,
                               V, c, n_chunks, (const float*)vmax, (const float*)vsum,
-                              (const int*)varg, uniforms, seq_ok)
+                              (const int*)varg, dr, seq_ok)
                  : launch_pdl(k_verify_first<false>, B, 96, st, target, ds, tokens, B,
                               gamma, V, c, n_chunks, (const float*)vmax, (const float*)vsum,
-                              (const int*)varg, uniforms, seq_ok);
+                              (const int*)varg, dr, seq_ok);
       if (e != cudaSuccess) return e;
     }
     if ((e = rows_pass(1, gamma, seq_ok, true)) != cudaSuccess) return e;
@@ -870,11 +869,11 @@ cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
     ProfScope ps(kKVerifyDecide, st);
     e = sample ? launch_pdl(k_verify_decide<true>, B, dthreads, st, target, ds, tokens, B,
                             gamma, V, c, n_chunks, (const float*)vmax, (const float*)vsum,
-                            (const int*)varg, uniforms, ok, out_tokens, out_nacc, info,
+                            (const int*)varg, dr, ok, out_tokens, out_nacc, info,
                             error_word())
                : launch_pdl(k_verify_decide<false>, B, dthreads, st, target, ds, tokens, B,
                             gamma, V, c, n_chunks, (const float*)vmax, (const float*)vsum,
-                            (const int*)varg, uniforms, ok, out_tokens, out_nacc, info,
+                            (const int*)varg, dr, ok, out_tokens, out_nacc, info,
                             error_word());
     if (e != cudaSuccess) return e;
   }
@@ -887,7 +886,7 @@ cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
     if (e != cudaSuccess) return e;
     ProfScope ps(kKVerifyFinish, st);
     k_verify_lr_finish<<<B, 256, 0, st>>>(ds.rrows, info, (const uint8_t*)w_up, ds.z_sel, ds.r,
-                                          V, c, n_sub, rm, pm, uniforms, gamma, out_tokens);
+                                          V, c, n_sub, rm, pm, dr, gamma, out_tokens);
     return cudaGetLastError();
   }
   if (sample) {
@@ -897,7 +896,7 @@ cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
       // the final draws' draft rows z W_up^T on the tensor cores, written out
       const MmaPlan mp = mma_plan(ds.r, B, V);
       const MmaWork none{nullptr, nullptr, nullptr};
-      const HeadOutputs no_out{nullptr, nullptr, nullptr, nullptr, nullptr};
+      const HeadOutputs no_out{Draws{nullptr, 0, 0}, nullptr, nullptr, nullptr, nullptr};
       e = launch_head_mma(mp, ds.z_sel, w_up, B, ds.r, V, 0.f, none, no_out, q_rows, ds.mma_ctr,
                           st, kKVerifyQRow);
       if (e != cudaSuccess) return e;
@@ -916,27 +915,27 @@ cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
     }
     ProfScope ps(kKVerifyFinish, st);
     k_verify_finish<<<B, 256, 0, st>>>(target, qbase, qs, qp, B, gamma, V, c, n_chunks, vmax,
-                                       vsum, info, rmass, uniforms, out_tokens);
+                                       vsum, info, rmass, dr, out_tokens);
   }
   return cudaGetLastError();
 }
 }  // namespace
 
 cudaError_t launch_verify(const float* target, const float* draft, const int32_t* tokens, int B,
-                          int gamma, int V, float temperature, const float* uniforms,
+                          int gamma, int V, float temperature, const Draws& draws,
                           int32_t* out_tokens, int32_t* out_nacc, void* ws, cudaStream_t st) {
   DraftSide ds{};
   ds.rows = draft;
   ds.ts = gamma;
   ds.tp = 1;
-  return verify_impl(target, ds, nullptr, tokens, B, gamma, V, temperature, uniforms, out_tokens,
+  return verify_impl(target, ds, nullptr, tokens, B, gamma, V, temperature, draws, out_tokens,
                      out_nacc, ws, st);
 }
 
 cudaError_t launch_verify_lowrank(const float* target, const void* z, const void* w_up,
                                   const float* logprob, const float* lse, int seq_stride,
                                   int pos_stride, int r, const int32_t* tokens, int B, int gamma,
-                                  int V, float temperature, const float* uniforms,
+                                  int V, float temperature, const Draws& draws,
                                   int32_t* out_tokens, int32_t* out_nacc, void* ws,
                                   cudaStream_t st) {
   DraftSide ds{};
@@ -949,7 +948,7 @@ cudaError_t launch_verify_lowrank(const float* target, const void* z, const void
   ds.ts = seq_stride;
   ds.tp = pos_stride;
   ds.r = r;
-  return verify_impl(target, ds, w_up, tokens, B, gamma, V, temperature, uniforms, out_tokens,
+  return verify_impl(target, ds, w_up, tokens, B, gamma, V, temperature, draws, out_tokens,
                      out_nacc, ws, st);
 }
 

@@ -19,6 +19,7 @@ def lib():
 
 FAKE = ctypes.c_void_p(1 << 20)      # 16-byte aligned, never dereferenced
 MISAL = ctypes.c_void_p((1 << 20) + 8)
+MISAL4 = ctypes.c_void_p((1 << 20) + 2)  # not even 4-byte aligned
 NULL = None
 
 
@@ -27,7 +28,7 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) == set(ss._SIGS)
     for n in names:
         assert hasattr(lib, n), n
-    assert lib.ss_version() == 100
+    assert lib.ss_version() == 200
 
 
 def test_status_strings(lib):
@@ -52,13 +53,13 @@ def test_workspace_sizes(lib):
 
 def _head(lib, **kw):
     a = dict(hidden=FAKE, w_down=FAKE, w_up=FAKE, M=2, d=64, r=32, V=100, dtype=ss.SS_BF16,
-             T=0.0, u=NULL, tok=FAKE, lp=NULL, mx=NULL, lse=NULL, z=NULL, logits=NULL,
-             ws=FAKE, wsb=1 << 20, stream=NULL)
+             T=0.0, seed=0, offset=0, u=NULL, tok=FAKE, lp=NULL, mx=NULL, lse=NULL, z=NULL,
+             logits=NULL, ws=FAKE, wsb=1 << 20, stream=NULL)
     a.update(kw)
     return lib.slimspec_head_forward(a["hidden"], a["w_down"], a["w_up"], a["M"], a["d"], a["r"],
-                                     a["V"], a["dtype"], a["T"], a["u"], a["tok"], a["lp"],
-                                     a["mx"], a["lse"], a["z"], a["logits"], a["ws"], a["wsb"],
-                                     a["stream"])
+                                     a["V"], a["dtype"], a["T"], a["seed"], a["offset"], a["u"],
+                                     a["tok"], a["lp"], a["mx"], a["lse"], a["z"], a["logits"],
+                                     a["ws"], a["wsb"], a["stream"])
 
 
 @pytest.mark.parametrize("dtype,r,M,ok", [
@@ -107,7 +108,7 @@ def test_head_argument_errors(lib):
     assert _head(lib, hidden=NULL) == E
     assert _head(lib, tok=NULL) == E
     assert _head(lib, w_up=MISAL) == E
-    assert _head(lib, T=1.0, u=NULL) == E           # sampling needs uniforms
+    assert _head(lib, T=1.0, u=MISAL4) == E          # uniforms, when given, 4-byte aligned
     assert _head(lib, r=8192) == ss.SS_ERR_UNSUPPORTED
     assert _head(lib, ws=NULL) == ss.SS_ERR_WORKSPACE
     assert _head(lib, wsb=16) == ss.SS_ERR_WORKSPACE
@@ -118,7 +119,7 @@ def test_head_argument_errors(lib):
 def test_verify_argument_errors(lib):
     def call(B=2, g=3, V=100, T=0.0, tgt=FAKE, dr=NULL, tok=FAKE, u=NULL, ot=FAKE, on=FAKE,
              ws=FAKE, wsb=1 << 20):
-        return lib.spec_verify(tgt, dr, tok, B, g, V, T, u, ot, on, ws, wsb, NULL)
+        return lib.spec_verify(tgt, dr, tok, B, g, V, T, 0, 0, u, ot, on, ws, wsb, NULL)
     E = ss.SS_ERR_INVALID_ARG
     assert call(B=-1) == E
     assert call(g=0) == E
@@ -127,7 +128,7 @@ def test_verify_argument_errors(lib):
     assert call(T=float("nan")) == E
     assert call(tgt=NULL) == E
     assert call(T=0.7) == E                          # sampling needs draft logits
-    assert call(T=0.7, dr=FAKE) == E                 # ... and uniforms
+    assert call(T=0.7, dr=FAKE, u=MISAL4) == E        # uniforms, when given, aligned
     assert call(tgt=MISAL) == E
     assert call(wsb=8) == ss.SS_ERR_WORKSPACE
     assert call(B=0) == ss.SS_OK
@@ -136,8 +137,8 @@ def test_verify_argument_errors(lib):
 def test_verify_lowrank_argument_errors(lib):
     def call(B=2, g=3, V=104, r=64, T=1.0, ss_=1, sp=2, tgt=FAKE, z=FAKE, w=FAKE, lp=FAKE,
              lse=FAKE, tok=FAKE, u=FAKE, ws=FAKE, wsb=1 << 24):
-        return lib.spec_verify_lowrank(tgt, z, w, lp, lse, ss_, sp, r, tok, B, g, V, T, u, FAKE,
-                                       FAKE, ws, wsb, NULL)
+        return lib.spec_verify_lowrank(tgt, z, w, lp, lse, ss_, sp, r, tok, B, g, V, T, 0, 0, u,
+                                       FAKE, FAKE, ws, wsb, NULL)
     E = ss.SS_ERR_INVALID_ARG
     assert call(T=0.0) == E                          # sampling only
     assert call(T=float("inf")) == E
@@ -148,7 +149,7 @@ def test_verify_lowrank_argument_errors(lib):
     assert call(ss_=-1) == E
     assert call(z=NULL) == E
     assert call(lse=NULL) == E
-    assert call(u=NULL) == E
+    assert call(u=MISAL4) == E
     assert call(z=MISAL) == E
     assert call(w=MISAL) == E
     assert call(r=12) == ss.SS_ERR_UNSUPPORTED        # r % 8 != 0: no recompute kernel
@@ -162,14 +163,14 @@ def test_verify_lowrank_argument_errors(lib):
 
 def test_trimmed_head_argument_errors(lib):
     def call(M=2, d=64, Vk=100, T=0.0, h=FAKE, w=FAKE, ids=FAKE, u=NULL, ws=FAKE, wsb=1 << 24):
-        return lib.trimmed_head_forward(h, w, ids, M, d, Vk, T, u, FAKE, NULL, NULL, NULL, ws,
-                                        wsb, NULL)
+        return lib.trimmed_head_forward(h, w, ids, M, d, Vk, T, 0, 0, u, FAKE, NULL, NULL, NULL,
+                                        ws, wsb, NULL)
     E = ss.SS_ERR_INVALID_ARG
     assert call(M=-1) == E
     assert call(d=12) == E
     assert call(Vk=0) == E
     assert call(ids=NULL) == E
-    assert call(T=1.0) == E                          # sampling needs uniforms
+    assert call(T=1.0, u=MISAL4) == E                # uniforms, when given, aligned
     assert call(h=MISAL) == E
     assert call(d=8192) == ss.SS_ERR_UNSUPPORTED     # beyond the tensor-core plan
     assert call(M=64, d=4096) == ss.SS_ERR_UNSUPPORTED  # h does not fit beside the stages
@@ -179,20 +180,40 @@ def test_trimmed_head_argument_errors(lib):
 
 
 def test_specvocab_and_topk_argument_errors(lib):
-    def sv(M=2, d=64, dp=16, V=100, k=10, T=0.0, ws=FAKE, wsb=1 << 24):
-        return lib.specvocab_head_forward(FAKE, FAKE, FAKE, FAKE, M, d, dp, V, k, T, NULL, FAKE,
-                                          NULL, NULL, NULL, ws, wsb, NULL)
+    def sv(M=2, d=64, dp=16, V=100, k=10, T=0.0, u=NULL, lg=NULL, ws=FAKE, wsb=1 << 24):
+        return lib.specvocab_head_forward(FAKE, FAKE, FAKE, FAKE, M, d, dp, V, k, T, 0, 0, u,
+                                          FAKE, NULL, NULL, lg, NULL, ws, wsb, NULL)
     assert sv(k=0) == ss.SS_ERR_INVALID_ARG
     assert sv(k=101) == ss.SS_ERR_INVALID_ARG
     assert sv(dp=12) == ss.SS_ERR_INVALID_ARG
     assert sv(d=8192) == ss.SS_ERR_UNSUPPORTED
-    assert sv(T=1.0) == ss.SS_ERR_INVALID_ARG         # no uniforms
+    assert sv(T=1.0, u=MISAL4) == ss.SS_ERR_INVALID_ARG  # misaligned uniforms
+    assert sv(lg=MISAL4) == ss.SS_ERR_INVALID_ARG  # misaligned logits
     assert sv(wsb=1) == ss.SS_ERR_WORKSPACE
     assert sv(M=0) == ss.SS_OK
     assert lib.ss_topk_rows(FAKE, 2, 100, 0, FAKE, NULL, 0, NULL) == ss.SS_ERR_INVALID_ARG
     assert lib.ss_topk_rows(FAKE, 2, 100, 101, FAKE, NULL, 0, NULL) == ss.SS_ERR_INVALID_ARG
     assert lib.ss_topk_rows(NULL, 2, 100, 5, FAKE, NULL, 0, NULL) == ss.SS_ERR_INVALID_ARG
     assert lib.ss_topk_rows(FAKE, 0, 100, 5, FAKE, NULL, 0, NULL) == ss.SS_OK
+
+
+def test_philox_argument_errors(lib):
+    E = ss.SS_ERR_INVALID_ARG
+    assert lib.ss_philox_uniforms(1, 2, -1, 4, FAKE, NULL) == E
+    assert lib.ss_philox_uniforms(1, 2, 4, -1, FAKE, NULL) == E
+    assert lib.ss_philox_uniforms(1, 2, 4, 4, NULL, NULL) == E
+    assert lib.ss_philox_uniforms(1, 2, 4, 4, MISAL4, NULL) == E
+    assert lib.ss_philox_uniforms(1, 2, 1 << 16, 1 << 15, FAKE, NULL) == ss.SS_ERR_UNSUPPORTED
+    assert lib.ss_philox_uniforms(2 ** 64 - 1, 2 ** 64 - 1, 0, 7, NULL, NULL) == ss.SS_OK
+    assert lib.ss_philox4x32_10(FAKE, -1, FAKE, NULL) == E
+    assert lib.ss_philox4x32_10(NULL, 3, FAKE, NULL) == E
+    assert lib.ss_philox4x32_10(FAKE, 3, NULL, NULL) == E
+    assert lib.ss_philox4x32_10(NULL, 0, NULL, NULL) == ss.SS_OK
+
+
+def test_wait_limit_range(lib):
+    assert lib.ss_set_wait_limit_ns(10 ** 10 + 1) == ss.SS_ERR_INVALID_ARG
+    assert lib.ss_set_wait_limit_ns(2 ** 64 - 1) == ss.SS_ERR_INVALID_ARG
 
 
 def test_python_binding_refuses_cpu_tensors(lib):

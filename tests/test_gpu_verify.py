@@ -97,6 +97,62 @@ def test_verify_tiny_vocab_many_sequences():
     assert abs(np.mean(n > 0) - acc) < 4 * np.sqrt(acc * (1 - acc) / B) + 1e-3
 
 
+def _tied_rows(seed, B, g, V):
+    """Integer-valued target rows whose maximum (8) is held by several ids of
+    every row, spread over the row's 2048-float chunks; draft rows = target +
+    small integers.  Returns (target, draft, lowest tied id per row)."""
+    rng = np.random.default_rng(seed)
+    target = rng.integers(-20, 5, (B, g + 1, V)).astype(np.float32)
+    low = np.zeros((B, g + 1), np.int64)
+    tied = {}
+    for b in range(B):
+        for j in range(g + 1):
+            ids = np.sort(rng.choice(V, 2 + (b + j) % 5, replace=False))
+            target[b, j, ids] = 8.0
+            low[b, j] = ids[0]
+            tied[b, j] = ids
+    draft = (target[:, :g] + rng.integers(-2, 3, (B, g, V))).astype(np.float32)
+    return target, draft, low, tied
+
+
+@pytest.mark.parametrize("V", [5003, 131072])
+def test_verify_greedy_exact_ties_lowest_index(V):
+    """Several ids share each target row's maximum: the target's choice is
+    the lowest of them.  A draft at the lowest tied id is kept, one at a
+    higher tied id is rejected and replaced by the lowest; bit-exact with the
+    oracle (the larger V also runs the position-0 split)."""
+    B, g = 24, 4
+    target, draft, low, tied = _tied_rows(31 + V, B, g, V)
+    x = low[:, :g].astype(np.int32).copy()
+    for b in range(B):
+        if b % 3 == 1:
+            x[b, 2] = tied[b, 2][-1]           # a higher tied id at position 2
+        elif b % 3 == 2:
+            x[b, 0] = tied[b, 0][1]            # the second-lowest tied id at position 0
+    v = {"target": target, "draft": draft}
+    toks, n = run_verify(v, x, 0.0)
+    check(v, x, 0.0, toks, n)
+    assert np.all(n[0::3] == g) and np.all(n[1::3] == 2) and np.all(n[2::3] == 0)
+    np.testing.assert_array_equal(toks[0::3, g], low[0::3, g])
+    np.testing.assert_array_equal(toks[1::3, 2], low[1::3, 2])
+    np.testing.assert_array_equal(toks[2::3, 0], low[2::3, 0])
+
+
+@pytest.mark.parametrize("T", [1.0, 0.5])
+def test_verify_sampling_on_tied_integer_rows(T):
+    """Sampling on rows of exact ties (integer logits): every accept decision,
+    residual and bonus draw meets the parity rules."""
+    B, g, V = 32, 4, 5003
+    target, draft, low, tied = _tied_rows(77, B, g, V)
+    rng = np.random.default_rng(78)
+    v = {"target": target, "draft": draft, "u_draft": synth.uniforms(rng, (B, g)),
+         "u_verify": synth.uniforms(rng, (B, g + 1))}
+    x = _drafts(v, T)
+    toks, n = run_verify(v, x, T)
+    c = check(v, x, T, toks, n)
+    assert c["exact"] >= B - 2
+
+
 def test_verify_bad_token_reports_device_error():
     v = synth.verify_logits(5, B=2, gamma=3, V=500, kind="normal")
     x = np.array([[1, 2, 3], [4, 600, 5]], np.int32)   # 600 >= V
