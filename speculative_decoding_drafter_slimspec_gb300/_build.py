@@ -4,6 +4,10 @@ Each .cu file under csrc/ is compiled to an object in parallel, then the
 objects are linked into a shared library with the CUDA runtime linked
 statically (so loading the library needs no libcudart on the loader path).
 The library lands next to this file; build products are git-ignored.
+
+Beside it, libsstimeline.so (csrc/timeline.cpp, host C++ against CUPTI) is
+the benchmark's kernel timeline; it is built when the toolkit has CUPTI and
+skipped otherwise (the library itself never uses it).
 """
 from __future__ import annotations
 
@@ -17,6 +21,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libslimspec.so")
+TIMELINE_LIB = os.path.join(HERE, "libsstimeline.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-Xptxas", "-warn-spills"]
@@ -41,8 +46,32 @@ def _newest_input() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
+def build_timeline(force: bool = False):
+    """Compiles libsstimeline.so (if out of date); returns its path, or None
+    when the toolkit has no CUPTI or no host compiler."""
+    src = os.path.join(CSRC, "timeline.cpp")
+    if not force and os.path.exists(TIMELINE_LIB) and \
+            os.path.getmtime(TIMELINE_LIB) >= os.path.getmtime(src):
+        return TIMELINE_LIB
+    cuda = os.path.dirname(os.path.dirname(os.path.realpath(_nvcc())))
+    inc, lib = os.path.join(cuda, "include"), os.path.join(cuda, "lib64")
+    cxx = shutil.which("g++") or shutil.which("c++")
+    if cxx is None or not os.path.exists(os.path.join(inc, "cupti.h")):
+        return None
+    tmp = TIMELINE_LIB + ".tmp"
+    r = subprocess.run([cxx, "-O2", "-shared", "-fPIC", "-std=c++17", f"-I{inc}", src, "-o", tmp,
+                        f"-L{lib}", "-lcupti", f"-Wl,-rpath,{lib}"], capture_output=True,
+                       text=True)
+    if r.returncode != 0:
+        sys.stderr.write(f"libsstimeline.so not built (no kernel timeline):\n{r.stderr[-2000:]}")
+        return None
+    os.replace(tmp, TIMELINE_LIB)
+    return TIMELINE_LIB
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compiles (if out of date) and returns the path of libslimspec.so."""
+    build_timeline(force)
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _newest_input():
         return LIB
     nvcc = _nvcc()

@@ -89,3 +89,42 @@ def test_quantiles_nearest_rank():
     assert bench.quantiles(v, (0.1, 0.5, 0.9)) == [1, 5, 9]
     assert bench.quantiles([3.0], (0.1, 0.5, 0.9)) == [3.0, 3.0, 3.0]
     assert bench.quantiles([5, 1, 3], (0.0, 1.0)) == [1, 5]
+
+
+def test_timeline_exclusive_times_add_up_to_busy_time():
+    """Overlapping launches (a dependent launch starting before its
+    predecessor ends) are charged only past the latest end before them, so a
+    replay's exclusive times sum to its busy time, never to more."""
+    from speculative_decoding_drafter_slimspec_gb300 import timeline
+    recs = [("k_a", 0, 100), ("k_b", 80, 130), ("k_c", 90, 120), ("k_d", 150, 160)]
+    excl, busy = timeline.exclusive_times(recs)
+    assert excl == [100, 30, 0, 10]
+    assert busy == 140 <= 160
+
+
+def test_timeline_summary_per_kernel():
+    from speculative_decoding_drafter_slimspec_gb300 import timeline
+    one = [("k_head_mma", 0, 100), ("k_head_mma_finish", 90, 110), ("k_verify_rows", 120, 150)]
+    recs = one + [(k, s + 1000, e + 1000) for k, s, e in one] + [("other", 5, 6)]
+    out = timeline.summarize(recs, per_replay=3)
+    assert out["replays"] == 2
+    k = out["kernels"]
+    assert k["k_head_mma"]["us_per_launch"] == 0.1
+    assert k["k_head_mma_finish"]["exclusive_us_per_step"] == 0.01
+    assert abs(sum(v["share"] for v in k.values()) - 1.0) < 1e-12
+    assert out["busy_us"] == 0.14 and out["wall_us"] == 0.15
+
+
+def test_kernel_kind_from_mangled_names():
+    from speculative_decoding_drafter_slimspec_gb300 import timeline
+    assert timeline.kernel_kind("_ZN2ss10k_head_mmaILb0ELi0ELb1EEEvPKt") == "k_head_mma"
+    assert timeline.kernel_kind("_ZN2ss15k_verify_decideILb0EEEvPKf") == "k_verify_decide"
+    assert timeline.kernel_kind("void ss::k_topk(float const*, int)") == "k_topk"
+
+
+def test_head_call_and_verify_bytes():
+    x = _llama()
+    assert bench.head_call_bytes(x) == 128256 * 512 * 2 + 512 * 4096 * 2 + 8 * 4096 * 2 + 8 * 4
+    assert bench.verify_all_bytes(x) == 8 * 7 * 128256 * 4 + 8 * 6 * 4
+    xs = dict(x, T=1.0)
+    assert bench.verify_all_bytes(xs) == 8 * 7 * 128256 * 4 + 8 * 6 * 128256 * 4 + 8 * 6 * 4
