@@ -443,6 +443,8 @@ def head_call_period(tsum, n_calls) -> dict | None:
     phases, periods = [], []
     for grp in tsum["replay_records"]:
         ends = [e for kind, _, e in grp if kind in head_kinds]
+        if len(ends) < n_calls:   # a head without a separate finish launch
+            ends = [e for kind, _, e in grp if kind == "k_head_mma"]
         if len(ends) < n_calls:
             return None
         ends = sorted(ends)[:n_calls]
