@@ -383,8 +383,10 @@ __device__ __forceinline__ float final_weight(const VerifyInfo& in, int mode, fl
 
 // ------------------------------------------------------------------ K10 ----
 // One warp per (sequence, chunk): mass of the final draw's distribution over
-// the chunk.  Residual rows are read with 16 x 16-byte loads of each of the
-// two rows in flight per lane; bonus rows come straight from the partials.
+// the chunk.  Residual rows are read in two steps of 8 x 16-byte loads of
+// each of the two rows in flight per lane (all 16 at once took 170 registers,
+// one CTA per SM, and measured 5% slower over the whole verification); bonus
+// rows come straight from the partials.
 __global__ void __launch_bounds__(256)
     k_verify_resid(const float* __restrict__ target, const float* __restrict__ draft, int qs,
                    int qp, int B, int gamma, int V, float c, int n_chunks,
@@ -414,21 +416,24 @@ __global__ void __launch_bounds__(256)
       if (vec) {
         const float4* t4 = reinterpret_cast<const float4*>(t);
         const float4* q4 = reinterpret_cast<const float4*>(q);
-        const int q0 = lo >> 2, q1 = hi >> 2;
-        float4 a[16], bq[16];
+        const int q1 = hi >> 2;
+#pragma unroll 1
+        for (int q0 = lo >> 2; q0 < q1; q0 += 32 * 8) {
+          float4 a[8], bq[8];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int i = q0 + lane + 32 * k;
-          if (i < q1) { a[k] = __ldg(t4 + i); bq[k] = __ldg(q4 + i); }
-        }
+          for (int k = 0; k < 8; ++k) {
+            const int i = q0 + lane + 32 * k;
+            if (i < q1) { a[k] = __ldg(t4 + i); bq[k] = __ldg(q4 + i); }
+          }
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int i = q0 + lane + 32 * k;
-          if (i < q1) {
-            s = __fadd_rn(s, final_weight(in, 0, a[k].x, bq[k].x, c));
-            s = __fadd_rn(s, final_weight(in, 0, a[k].y, bq[k].y, c));
-            s = __fadd_rn(s, final_weight(in, 0, a[k].z, bq[k].z, c));
-            s = __fadd_rn(s, final_weight(in, 0, a[k].w, bq[k].w, c));
+          for (int k = 0; k < 8; ++k) {
+            const int i = q0 + lane + 32 * k;
+            if (i < q1) {
+              s = __fadd_rn(s, final_weight(in, 0, a[k].x, bq[k].x, c));
+              s = __fadd_rn(s, final_weight(in, 0, a[k].y, bq[k].y, c));
+              s = __fadd_rn(s, final_weight(in, 0, a[k].z, bq[k].z, c));
+              s = __fadd_rn(s, final_weight(in, 0, a[k].w, bq[k].w, c));
+            }
           }
         }
       } else {
