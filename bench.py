@@ -932,7 +932,8 @@ def measure_round(args, ss, dev, local, world, workload, lowrank=False, ranks=No
         out["clocks"] = sampler.summary(wall0, time.time())
         out["clocks"]["window"] = win
     # per-kernel figures from the replayed step's CUPTI timeline
-    tsum = graph_timeline(graph, stream, max(10, min(50, args.steps)), launches_per_step)
+    tsum = None if args.no_timeline else \
+        graph_timeline(graph, stream, max(10, min(50, args.steps)), launches_per_step)
     ver_in_round = verify_phase(tsum)
     peak, peak_kind = measured_peaks()
     kb = kernel_bytes(x, union_rows, ver_rows)
@@ -1125,6 +1126,9 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-single-thread", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-timeline", action="store_true",
+                    help="skip the CUPTI kernel timeline (for runs under ncu, which uses CUPTI "
+                         "itself); the line then has no per-kernel figures")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the compact lines of the other configurations (llama8b)")
     ap.add_argument("--no-dense", action="store_true",
