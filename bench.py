@@ -937,7 +937,7 @@ def measure_round(args, ss, dev, local, world, workload, lowrank=False, ranks=No
     ver_in_round = verify_phase(tsum)
     peak, peak_kind = measured_peaks()
     kb = kernel_bytes(x, union_rows, ver_rows)
-    roof = head_roof = ver_roof = call_roof = None
+    roof = head_roof = call_roof = None
     kern = {}
     if tsum and tsum["kernels"]:
         kern = tsum["kernels"]
@@ -962,14 +962,6 @@ def measure_round(args, ss, dev, local, world, workload, lowrank=False, ranks=No
                                        "algorithmic_flops_per_launch": flops}
             if roof and roof["kernel"] == hk:
                 roof = dict(head_roof)
-        if "k_verify_rows" in kern:
-            ver_roof = hbm_roofline("k_verify_rows", kb["k_verify_rows"],
-                                    kern["k_verify_rows"]["us_per_launch"] / 1e6, peak,
-                                    peak_kind, workload)
-            ver_roof["launches_per_step"] = kern["k_verify_rows"]["launches_per_step"]
-            ver_roof["rows_needed"] = ver_rows
-            ver_roof["rows_total"] = x["B"] * (x["gamma"] + 1) + (
-                x["B"] * x["gamma"] if x["T"] > 0 and not x.get("lowrank", False) else 0)
         if x["u_full"] is None:
             hc = head_call_period(tsum, x["n_calls"])
             if hc:
@@ -982,7 +974,7 @@ def measure_round(args, ss, dev, local, world, workload, lowrank=False, ranks=No
                     call_roof["steady"] = {"achieved": st["achieved"], "frac": st["frac"],
                                            "frac_of_8tbs": st["frac_of_8tbs"]}
         tsum.pop("replay_records", None)
-    out.update(roofline=roof, head_roofline=head_roof, verify_roofline=ver_roof,
+    out.update(roofline=roof, head_roofline=head_roof,
                head_call_roofline=call_roof, kernels=kern,
                timeline={k: v for k, v in (tsum or {}).items() if k != "kernels"},
                union_rows=union_rows)
@@ -994,6 +986,14 @@ def measure_round(args, ss, dev, local, world, workload, lowrank=False, ranks=No
     vt["roofline_all_rows"] = {k: vr[k] for k in ("achieved", "peak", "unit", "frac",
                                                   "frac_of_8tbs", "algorithmic_bytes_per_launch")}
     out["verify"] = vt
+    # the rows the accept chain needs over the same time: how close the
+    # verification comes to reading only those
+    ver_roof = hbm_roofline("verification (all kernels, timed alone)", ver_rows * x["V"] * 4,
+                            vt["us_per_call"] / 1e6, peak, peak_kind)
+    ver_roof["rows_needed"] = ver_rows
+    ver_roof["rows_total"] = x["B"] * (x["gamma"] + 1) + (
+        x["B"] * x["gamma"] if x["T"] > 0 and not x.get("lowrank", False) else 0)
+    out["verify_roofline"] = ver_roof
     if full:
         out["ms_per_step_dist"] = step_time_distribution(graph, stream, min(args.steps, 500))
     del graph

@@ -77,7 +77,9 @@ __global__ void __launch_bounds__(256)
                   const int* __restrict__ seq_ok, float* __restrict__ vmax,
                   float* __restrict__ vsum, int* __restrict__ varg) {
   pdl_launch_dependents();
-  pdl_wait_producer();
+  // the logit rows are inputs: read and reduced while a preceding kernel may
+  // still run; the flags and the partials wait for it (below)
+  if (seq_ok != nullptr) pdl_wait_producer();
   const int lane = threadIdx.x & 31;
   const unsigned gw = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const unsigned nw = gridDim.x * (blockDim.x >> 5);
@@ -144,6 +146,7 @@ __global__ void __launch_bounds__(256)
     }
 #pragma unroll
     for (int bit = 0; bit < 5; ++bit) s = shfl_merge<kSample>(s, 1 << bit, c);
+    pdl_wait_producer();  // (returns at once after the first time)
     if (lane == 0) {
       const size_t o = (size_t)row * n_chunks + ch;
       vmax[o] = s.mx;
@@ -865,7 +868,9 @@ cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
     }
     if ((e = rows_pass(1, gamma, seq_ok, true)) != cudaSuccess) return e;
   } else {
-    if ((e = rows_pass(0, gamma, nullptr, false)) != cudaSuccess) return e;
+    // greedy: a dependent launch, streaming the rows while the preceding
+    // kernel finishes
+    if ((e = rows_pass(0, gamma, nullptr, !sample)) != cudaSuccess) return e;
   }
   {
     const int rows = (sample && !lowrank) ? 2 * gamma + 1 : gamma + 1;
