@@ -63,6 +63,7 @@ constexpr int kMaxStages = 16;
 constexpr int kTileRing = 8;              // tile ids in flight between the warps
 constexpr int kStaticTiles = 2;           // tiles b, b + grid of CTA b; the rest are claimed
 constexpr int kSmemCap = 223 * 1024;      // dynamic; static barriers use the rest
+constexpr int kSmemCapDual = 226 * 1024;  // the dual plan: all but 1 KB of the 227 KB a CTA may use
 constexpr int kFinThreads = 256;
 constexpr int kFinPer = 24;               // partials per finish thread: n_sub <= 6144
 
@@ -244,9 +245,9 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&v)[32], int vid0, int
 // Every CTA holds one M tile of up to 128 rows of z: CTA b takes M tile
 // b % m_tiles and streams the vocabulary tiles of that M tile with the other
 // gridDim.x / m_tiles CTAs of it (their own tile counter).  With two M tiles
-// each W_up tile is read by two CTAs; the second read mostly hits L2, and
-// each CTA keeps room for more W_up stages in flight than one holding both
-// tiles of z would.  kMode 0: softmax partials; kMode 1: the fp32 scores
+// each W_up tile is then read by two CTAs (the second read mostly from L2);
+// the dual plan below instead keeps both tiles of z in every CTA, when three
+// W_up stages still fit beside them, so that each SM takes W_up in once.  kMode 0: softmax partials; kMode 1: the fp32 scores
 // D[m, v] are written to out_scores (M x V); kMode 2: the residual masses of
 // a verified sequence's final draw (ResidRow), the target values of each
 // tile loaded ahead of its accumulator, into part.pmax (residual) and
@@ -255,9 +256,13 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&v)[32], int vid0, int
 // a stage is KPS K blocks -- WB full ones as one 4-D box of 128 rows x WB*128
 // contiguous bytes (every row's bytes of the stage in one request run: fewer
 // DRAM page openings per byte), then, when r is not a multiple of 64, the
-// ragged last block as a 2-D box.  tile_ctr is zeroed by the down-projection
-// that precedes this grid.
-template <bool kSample, int kMode, bool kWide>
+// ragged last block as a 2-D box.  kDual (softmax partials, 2-D stages,
+// 128 < M <= 256): every CTA holds both M tiles of z and issues both MMA
+// chains on each W_up stage, into four TMEM accumulators (two tiles x double
+// buffering), so each SM takes in W_up once instead of once per M tile;
+// m_tiles is then 1 and all CTAs share one tile counter.  tile_ctr is zeroed
+// by the down-projection that precedes this grid.
+template <bool kSample, int kMode, bool kWide, bool kDual = false>
 __global__ void __launch_bounds__(kThreads, 1)
     k_head_mma(const uint16_t* __restrict__ z, const __grid_constant__ CUtensorMap tm_w,
                const __grid_constant__ CUtensorMap tm_w2, int M, int m_tiles, int R, int V, int KB,
@@ -271,9 +276,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int cb = (int)blockIdx.x / m_tiles;    // its index among that tile's CTAs
   const int gm = (int)gridDim.x / m_tiles;     // CTAs per M tile
   const int m0 = mtc * kTileM;                 // first row of z of this CTA
-  const int Ml = min(kTileM, M - m0);          // rows of z of this CTA
+  const int Ml = min(kTileM, M - m0);          // rows of z of this CTA (its first M tile)
+  const int Ml1 = kDual ? M - kTileM : 0;      // rows of its second M tile (dual)
   uint8_t* sA = smem;                          // KB compact blocks of z
-  uint8_t* sB = smem + z_bytes(Ml, KB);        // NST stages of W_up
+  uint8_t* sA1 = smem + z_bytes(Ml, KB);       // the second M tile's blocks (dual)
+  uint8_t* sB = sA1 + (kDual ? z_bytes(Ml1, KB) : 0);  // NST stages of W_up
   const int kStageBytes = (kWide ? KPS : 1) * kBlockBytes;
   const int SPT = kWide ? KB / KPS : KB;       // stages per vocabulary tile
   __shared__ uint64_t full[kMaxStages], empty[kMaxStages], a_full, acc_full[2], acc_empty[2];
@@ -282,7 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ int s_fills[kMaxStages];  // TMA fills issued per stage (drained before exit)
   __shared__ uint32_t s_tmem;
   __shared__ int s_abort;
-  constexpr uint32_t kCols = 2 * kTileN;  // double-buffered accumulators
+  constexpr int kMT = kDual ? 2 : 1;                  // M tiles per CTA
+  constexpr uint32_t kCols = 2 * kMT * kTileN;        // double-buffered accumulators
   constexpr uint32_t kIdesc = idesc_bf16(kTileM, kTileN);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -423,8 +431,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t adesc = sw128_desc(smem_u32(sA + z_block_off(Ml, kb)));
 #pragma unroll
             for (int k4 = 0; k4 < 4; ++k4)
-              mma_bf16(tmem + (uint32_t)(buf * kTileN), adesc + 2 * k4, bdesc + 2 * k4, kIdesc,
-                       (kb | k4) != 0 ? 1u : 0u);
+              mma_bf16(tmem + (uint32_t)(buf * kMT * kTileN), adesc + 2 * k4, bdesc + 2 * k4,
+                       kIdesc, (kb | k4) != 0 ? 1u : 0u);
+            if (kDual) {  // the second M tile, on the same stage
+              const uint64_t adesc1 = sw128_desc(smem_u32(sA1 + z_block_off(Ml1, kb)));
+#pragma unroll
+              for (int k4 = 0; k4 < 4; ++k4)
+                mma_bf16(tmem + (uint32_t)((buf * kMT + 1) * kTileN), adesc1 + 2 * k4,
+                         bdesc + 2 * k4, kIdesc, (kb | k4) != 0 ? 1u : 0u);
+            }
           }
           mma_commit(&empty[s]);  // the stage is free once these MMAs complete
         }
@@ -450,14 +465,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       // flight at once (under a full memory queue each round trip takes
       // microseconds); pieces past r are zero-filled by the copy itself.
       pdl_wait_producer();
-      const int n_items = Ml * KB * 8;  // (row i, K block, 16-byte chunk), chunk fastest
-      for (int it = ew * 32 + lane; it < n_items; it += 32 * kEpiWarps) {
-        const int c8 = it & 7, q = it >> 3;
-        const int i = q / KB, kb = q - i * KB;
-        const int k0 = kb * 64 + c8 * 8;
-        const bool in = k0 < R;
-        cp_async16_zfill(sA + z_block_off(Ml, kb) + i * 128 + ((c8 ^ (i & 7)) * 16),
-                         z + (size_t)(m0 + i) * R + (in ? k0 : 0), in ? 16u : 0u);
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        const int mrows = mt == 0 ? Ml : Ml1, mbase = m0 + mt * kTileM;
+        uint8_t* dstA = mt == 0 ? sA : sA1;
+        const int n_items = mrows * KB * 8;  // (row i, K block, 16-byte chunk), chunk fastest
+        for (int it = ew * 32 + lane; it < n_items; it += 32 * kEpiWarps) {
+          const int c8 = it & 7, q = it >> 3;
+          const int i = q / KB, kb = q - i * KB;
+          const int k0 = kb * 64 + c8 * 8;
+          const bool in = k0 < R;
+          cp_async16_zfill(dstA + z_block_off(mrows, kb) + i * 128 + ((c8 ^ (i & 7)) * 16),
+                           z + (size_t)(mbase + i) * R + (in ? k0 : 0), in ? 16u : 0u);
+        }
       }
       cp_async_wait_all();
       fence_proxy_async_smem();  // visible to the tensor cores (async proxy)
@@ -465,9 +485,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(&a_full);
     }
     const int half = ew / 4;                 // the 64-column half of each tile
-    const int row = m0 + quad * 32 + lane;   // row of z owned by this thread
+    const int row = m0 + quad * 32 + lane;   // row of z owned by this thread (first M tile)
     const bool live = quad * 32 + lane < Ml;
-    const bool warp_live = quad * 32 < Ml;   // any live row in this warp
     const uint32_t lane_addr = (uint32_t)(quad * 32) << 16;
     const int n_sub = 2 * n_tiles;
     ResidRow rr{nullptr, 0.f, 0.f, 0.f, 1};
@@ -500,7 +519,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = mbar_wait_bounded(&acc_full[buf], (i >> 1) & 1, err);
       if (!__all_sync(0xFFFFFFFFu, ok) || *(volatile int*)&s_abort) break;
       tc_fence_after();
-      {
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        // (dual) the second M tile's rows and accumulator
+        const int row = m0 + mt * kTileM + quad * 32 + lane;
+        const int mrows = mt == 0 ? Ml : Ml1;
+        const bool live = quad * 32 + lane < mrows;
+        const bool warp_live = quad * 32 < mrows;
+        const uint32_t acc_col = (uint32_t)((buf * kMT + mt) * kTileN);
         const int h = half;
         RowState st = row_state_empty();
         if (warp_live) {
@@ -508,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint32_t v2[2][32];
 #pragma unroll
           for (int cc = 0; cc < 2; ++cc)
-            tmem_ld32_issue(tmem + lane_addr + (uint32_t)(buf * kTileN + h * kSubW + cc * 32),
+            tmem_ld32_issue(tmem + lane_addr + acc_col + (uint32_t)(h * kSubW + cc * 32),
                             v2[cc]);
           tmem_ld_wait();
           if (kMode == 2) {
@@ -1054,15 +1080,45 @@ MmaPlan mma_plan(int r, int M, int V) {
   return p;
 }
 
-template <bool kSample, int kMode, bool kWide>
+// Both M tiles of z in every CTA (softmax partials, 128 < M <= 256), with 2-D
+// W_up stages in the room left: chosen when at least four stages fit.
+MmaPlan mma_plan_dual(int r, int M, int V) {
+  MmaPlan p{};
+  p.ok = false;
+  if (M <= kTileM || M > 2 * kTileM || r % 8 != 0 || r > 4096) return p;
+  p.mt = 1;  // one tile counter; each CTA takes both M tiles of every tile it draws
+  p.dual = true;
+  p.kb = (r + 63) / 64;
+  const int a_bytes = z_bytes(kTileM, p.kb) + z_bytes(M - kTileM, p.kb);
+  const int room = kSmemCapDual - 1024 - a_bytes;
+  p.kps = 1;
+  p.wb = 0;
+  if (V % 8 == 0 && r % 128 == 0 && room >= 2 * 2 * kBlockBytes) {
+    p.kps = 2;  // stages of two K blocks: 256 contiguous bytes of each row per request run
+    p.wb = 2;
+  }
+  const int stage = p.kps * kBlockBytes;
+  p.nst = room > 0 ? std::min(p.kps > 1 ? 4 : kMaxStages, room / stage) : 0;
+  if (p.nst < (p.kps > 1 ? 2 : 4)) return p;
+  p.smem = 1024 + a_bytes + p.nst * stage;
+  p.n_tiles = (V + kTileN - 1) / kTileN;
+  p.grid = std::max(1, std::min(sm_count(), p.n_tiles));
+  p.n_sub = 2 * p.n_tiles;
+  if (p.n_sub > kFinThreads * kFinPer) return p;
+  p.ok = true;
+  return p;
+}
+
+template <bool kSample, int kMode, bool kWide, bool kDual = false>
 static cudaError_t launch_mma_kps(const MmaPlan& p, const void* z, const CUtensorMap& tw,
                                   const CUtensorMap& tw2, int M, int r, int V, float c,
                                   const MmaPart& part, float* scores, unsigned* ctr,
                                   cudaStream_t st, KernelKind kind,
                                   const ResidRow* rrows = nullptr) {
-  auto kern = k_head_mma<kSample, kMode, kWide>;
+  auto kern = k_head_mma<kSample, kMode, kWide, kDual>;
   // the limit is set once per kernel: make it the largest size any plan asks for
-  cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), kSmemCap);
+  cudaError_t e =
+      set_smem_once(reinterpret_cast<const void*>(kern), kDual ? kSmemCapDual : kSmemCap);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid);
@@ -1195,10 +1251,26 @@ cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up
     e = launch_mma_one<false, 1>(p, z_ws, tw, tw2, M, r, V, c, part, scores, ctr, st, kind);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
-  if (sample)
+  // both M tiles in every CTA when they and four stages fit (128 < M <= 256)
+  const MmaPlan pd = M > kTileM ? mma_plan_dual(r, M, V) : MmaPlan{};
+  if (pd.ok) {
+    CUtensorMap dw, dw2;
+    if (!make_maps(pd, w_up, V, r, &dw, &dw2)) return cudaErrorInvalidValue;
+    if (pd.kps > 1)
+      e = sample ? launch_mma_kps<true, 0, true, true>(pd, z_ws, dw, dw2, M, r, V, c, part,
+                                                       nullptr, ctr, st, kind)
+                 : launch_mma_kps<false, 0, true, true>(pd, z_ws, dw, dw2, M, r, V, c, part,
+                                                        nullptr, ctr, st, kind);
+    else
+      e = sample ? launch_mma_kps<true, 0, false, true>(pd, z_ws, dw, dw2, M, r, V, c, part,
+                                                        nullptr, ctr, st, kind)
+                 : launch_mma_kps<false, 0, false, true>(pd, z_ws, dw, dw2, M, r, V, c, part,
+                                                         nullptr, ctr, st, kind);
+  } else if (sample) {
     e = launch_mma_one<true, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st, kind);
-  else
+  } else {
     e = launch_mma_one<false, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st, kind);
+  }
   if (e != cudaSuccess) return e;
   // the per-row finish, launched to overlap the tail of the MMA grid
   cudaLaunchConfig_t cfg = {};

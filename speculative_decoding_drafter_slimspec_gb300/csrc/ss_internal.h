@@ -119,6 +119,7 @@ struct MmaPlan {
   int n_tiles;  // 128-row vocabulary tiles
   int grid;     // CTAs (one per SM; a multiple of mt)
   int n_sub;    // 64-row partials per row of z (2 per tile)
+  bool dual;    // every CTA holds both M tiles of z (see mma_plan_dual)
   bool ok;
 };
 MmaPlan mma_plan(int r, int M, int V);
