@@ -278,7 +278,7 @@ class Round:
                                         seed=SEED, offset=OFFSET + j, want_stats=False,
                                         workspace=self.head_ws, out=self.head_out[j])
 
-    def verify(self, target, draft=None, tokens=None, out=None):
+    def verify(self, target, draft=None, tokens=None, out=None, lazy=False):
         x, ss = self.x, self.ss
         T, off = x["T"], OFFSET + x["n_calls"]
         out = out if out is not None else self.ver_out
@@ -288,7 +288,7 @@ class Round:
                                           lr["lse"], lr["tokens"], T, None, seed=SEED,
                                           offset=off, position_major=True,
                                           workspace=self.ver_ws, out=out)
-        return ss.spec_verify(target, draft, tokens, T, None, seed=SEED, offset=off,
+        return ss.spec_verify(target, draft, tokens, T, None, seed=SEED, offset=off, lazy=lazy,
                               workspace=self.ver_ws, out=out)
 
     def step(self):
@@ -518,10 +518,11 @@ def clock_window(graph, stream, seconds: float, step_ms: float) -> dict:
             "how": "replays right after the timed region, sampled every 200 ms"}
 
 
-def timed_verify(x, rnd, ss, stream, steps) -> dict:
+def timed_verify(x, rnd, ss, stream, steps, lazy=False) -> dict:
     """spec_verify (or spec_verify_lowrank) alone: a graph of one call per
     copy of the target (and draft) rows, enough copies that the rows read
-    between two reads of one copy exceed L2; steps/s = calls / time."""
+    between two reads of one copy exceed L2; steps/s = calls / time.  lazy:
+    the position-by-position schedule (spec_verify_lazy) instead."""
     import torch
     per_copy = x["B"] * (x["gamma"] + 1) * x["V"] * 4 + (
         x["B"] * x["gamma"] * x["V"] * 4 if x["draft"] is not None else 0)
@@ -531,12 +532,12 @@ def timed_verify(x, rnd, ss, stream, steps) -> dict:
           if x["draft"] is not None else [None] * n_copies)
     with torch.cuda.stream(stream):
         for i in range(n_copies):
-            rnd.verify(tg[i], dr[i], x["tokens"])
+            rnd.verify(tg[i], dr[i], x["tokens"], lazy=lazy)
     stream.synchronize()
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, stream=stream, capture_error_mode="thread_local"):
         for i in range(n_copies):
-            rnd.verify(tg[i], dr[i], x["tokens"])
+            rnd.verify(tg[i], dr[i], x["tokens"], lazy=lazy)
     reps = max(3, steps // n_copies + 1)
     with torch.cuda.stream(stream):
         for _ in range(3):
@@ -993,6 +994,14 @@ def measure_round(args, ss, dev, local, world, workload, lowrank=False, ranks=No
     ver_roof["rows_needed"] = ver_rows
     ver_roof["rows_total"] = x["B"] * (x["gamma"] + 1) + (
         x["B"] * x["gamma"] if x["T"] > 0 and not x.get("lowrank", False) else 0)
+    if not x.get("lowrank", False):
+        # the lazy schedule (spec_verify_lazy): exactly the needed rows, one
+        # row pass and one decision per position
+        vl = timed_verify(x, rnd, ss, stream, args.steps, lazy=True)
+        lr = hbm_roofline("verification, lazy schedule (timed alone)", ver_rows * x["V"] * 4,
+                          vl["us_per_call"] / 1e6, peak, peak_kind)
+        ver_roof["lazy_schedule"] = {"us_per_call": vl["us_per_call"], "achieved": lr["achieved"],
+                                     "frac": lr["frac"], "frac_of_8tbs": lr["frac_of_8tbs"]}
     out["verify_roofline"] = ver_roof
     if full:
         out["ms_per_step_dist"] = step_time_distribution(graph, stream, min(args.steps, 500))
@@ -1037,7 +1046,8 @@ def compact(meas) -> dict:
         r = meas.get(k)
         if r:
             out[k] = {kk: r[kk] for kk in ("kernel", "achieved", "frac", "frac_of_8tbs",
-                                           "us_per_launch", "traffic", "steady")
+                                           "us_per_launch", "traffic", "steady",
+                                           "lazy_schedule")
                       if kk in r}
     v = meas["verify"]
     out["verify"] = {"us_per_call": v["us_per_call"], "steps_per_s": v["steps_per_s"],

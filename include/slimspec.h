@@ -279,6 +279,22 @@ int spec_verify(const float* target_logits, const float* draft_logits,
                 int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
                 cudaStream_t stream);
 
+/* The same verification on the lazy schedule of [Explainer] "小模型起草，大模型
+ * 批改" (stop at the first mismatch): the rows of position j are read only for
+ * the sequences that kept positions 0 .. j-1, and position j is decided before
+ * position j+1 is read, so exactly the rows the accept chain needs are read
+ * (one row pass and one decision launch per position).  spec_verify instead
+ * decides position 0 alone first and then reads every later row of the
+ * sequences that kept it, which is faster on the shapes measured here.
+ * Arguments, workspace (spec_verify_workspace_size), errors and results are
+ * those of spec_verify; the results are identical. */
+int spec_verify_lazy(const float* target_logits, const float* draft_logits,
+                     const int32_t* draft_tokens, int B, int gamma, int V,
+                     float temperature, uint64_t seed, uint64_t offset,
+                     const float* uniforms, int32_t* out_tokens,
+                     int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * Sampling verification with the draft side taken from the low-rank head.
  *

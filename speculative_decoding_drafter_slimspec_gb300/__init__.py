@@ -32,7 +32,7 @@ __all__ = [
     "SS_OK", "SS_ERR_INVALID_ARG", "SS_ERR_UNSUPPORTED", "SS_ERR_WORKSPACE",
     "SS_ERR_CUDA", "SS_ERR_TIMEOUT", "SS_ERR_DEVICE_INDEX", "SlimspecError",
     "lib", "lib_path", "header_functions", "slimspec_head_forward",
-    "specvocab_head_forward", "ss_topk_rows", "spec_verify", "spec_verify_lowrank",
+    "specvocab_head_forward", "ss_topk_rows", "spec_verify", "spec_verify_lazy", "spec_verify_lowrank",
     "ss_get_device_error", "slimspec_head_workspace_size", "specvocab_head_workspace_size",
     "spec_verify_workspace_size", "spec_verify_lowrank_workspace_size", "ss_topk_workspace_size",
     "trimmed_head_forward", "trimmed_head_workspace_size", "ss_philox_uniforms",
@@ -66,6 +66,8 @@ _SIGS = {
     "ss_topk_rows": (_i, [_vp, _i, _i, _i, _vp, _vp, _sz, _vp]),
     "spec_verify_workspace_size": (_sz, [_i, _i, _i, _f]),
     "spec_verify": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _u64, _u64, _vp, _vp, _vp, _vp, _sz,
+                         _vp]),
+    "spec_verify_lazy": (_i, [_vp, _vp, _vp, _i, _i, _i, _f, _u64, _u64, _vp, _vp, _vp, _vp, _sz,
                          _vp]),
     "spec_verify_lowrank_workspace_size": (_sz, [_i, _i, _i, _i]),
     "trimmed_head_workspace_size": (_sz, [_i, _i, _i]),
@@ -280,10 +282,12 @@ def ss_topk_rows(scores, k, *, out=None, stream=None):
 
 
 def spec_verify(target_logits, draft_logits, draft_tokens, temperature=0.0, uniforms=None, *,
-                seed=0, offset=0, workspace=None, out=None, stream=None) -> dict:
+                seed=0, offset=0, lazy=False, workspace=None, out=None, stream=None) -> dict:
     """Verification of B sequences: target (B, g+1, V), draft (B, g, V) fp32,
     draft_tokens (B, g) int32.  Sampling draws u[b, j] from Philox4x32-10 at
-    (seed, offset, row b, slot j), or takes uniforms (B, g+1) fp32 when given."""
+    (seed, offset, row b, slot j), or takes uniforms (B, g+1) fp32 when given.
+    lazy=True reads the rows position by position, only for the sequences
+    still kept (spec_verify_lazy); the results are the same."""
     B, g1, V = target_logits.shape
     gamma = g1 - 1
     dev = target_logits.device
@@ -294,11 +298,12 @@ def spec_verify(target_logits, draft_logits, draft_tokens, temperature=0.0, unif
         o["num_accepted"] = torch.empty(B, dtype=torch.int32, device=dev)
     nbytes = spec_verify_workspace_size(B, gamma, V, temperature)
     ws = _workspace(nbytes, dev, workspace)
-    st = lib().spec_verify(
+    fn = lib().spec_verify_lazy if lazy else lib().spec_verify
+    st = fn(
         _ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens), B, gamma, V,
         float(temperature), int(seed), int(offset), _ptr(uniforms), _ptr(o["tokens"]),
         _ptr(o["num_accepted"]), _ptr(ws), ws.numel(), _stream(stream))
-    _check(st, "spec_verify")
+    _check(st, "spec_verify_lazy" if lazy else "spec_verify")
     return o
 
 

@@ -349,10 +349,12 @@ int spec_verify_lowrank(const float* target_logits, const void* z, const void* w
                                            out_num_accepted, workspace, stream));
 }
 
-int spec_verify(const float* target_logits, const float* draft_logits, const int32_t* draft_tokens,
-                int B, int gamma, int V, float temperature, uint64_t seed, uint64_t offset,
-                const float* uniforms, int32_t* out_tokens, int32_t* out_num_accepted,
-                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+// Both schedules: the split one (spec_verify) and, lazy, position by position.
+static int verify_entry(const float* target_logits, const float* draft_logits,
+                        const int32_t* draft_tokens, int B, int gamma, int V, float temperature,
+                        uint64_t seed, uint64_t offset, const float* uniforms, int32_t* out_tokens,
+                        int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                        cudaStream_t stream, bool lazy) {
   if (B < 0 || gamma < 1 || gamma > 32 || V <= 0 || !temp_ok(temperature))
     return SS_ERR_INVALID_ARG;
   if ((long long)B * (gamma + 1) * V >= (1LL << 40)) return SS_ERR_UNSUPPORTED;
@@ -372,7 +374,26 @@ int spec_verify(const float* target_logits, const float* draft_logits, const int
   if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return SS_ERR_WORKSPACE;
   return cuda_status(launch_verify(target_logits, draft_logits, draft_tokens, B, gamma, V,
                                    temperature, Draws{uniforms, seed, offset}, out_tokens,
-                                   out_num_accepted, workspace, stream));
+                                   out_num_accepted, workspace, stream, lazy));
+}
+
+int spec_verify(const float* target_logits, const float* draft_logits, const int32_t* draft_tokens,
+                int B, int gamma, int V, float temperature, uint64_t seed, uint64_t offset,
+                const float* uniforms, int32_t* out_tokens, int32_t* out_num_accepted,
+                void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+  return verify_entry(target_logits, draft_logits, draft_tokens, B, gamma, V, temperature, seed,
+                      offset, uniforms, out_tokens, out_num_accepted, workspace, workspace_bytes,
+                      stream, false);
+}
+
+int spec_verify_lazy(const float* target_logits, const float* draft_logits,
+                     const int32_t* draft_tokens, int B, int gamma, int V, float temperature,
+                     uint64_t seed, uint64_t offset, const float* uniforms, int32_t* out_tokens,
+                     int32_t* out_num_accepted, void* workspace, size_t workspace_bytes,
+                     cudaStream_t stream) {
+  return verify_entry(target_logits, draft_logits, draft_tokens, B, gamma, V, temperature, seed,
+                      offset, uniforms, out_tokens, out_num_accepted, workspace, workspace_bytes,
+                      stream, true);
 }
 
 // ------------------------------------------------------- Philox uniforms --

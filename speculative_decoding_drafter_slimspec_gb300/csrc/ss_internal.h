@@ -178,7 +178,8 @@ cudaError_t launch_verify_lowrank(const float* target, const void* z, const void
                                   cudaStream_t st);
 cudaError_t launch_verify(const float* target, const float* draft, const int32_t* tokens, int B,
                           int gamma, int V, float temperature, const Draws& draws,
-                          int32_t* out_tokens, int32_t* out_nacc, void* ws, cudaStream_t st);
+                          int32_t* out_tokens, int32_t* out_nacc, void* ws, cudaStream_t st,
+                          bool lazy = false);
 
 // ------------------------------------------------------------- specvocab --
 size_t topk_ws_bytes(int M, int V, int k);

@@ -244,28 +244,30 @@ __device__ __forceinline__ bool position_accepts(const PosInputs& in, int V, flo
 }
 
 // ---------------------------------------------------------------- K8b ----
-// Position 0 of every sequence, decided between the two row passes: one CTA
-// per sequence, warp 0 merging the partials of the target row, warp 1 those
-// of the draft row (sampling) and warp 2 loading the token-side inputs;
-// seq_ok[b] = 1 iff the drafted token is kept (the later positions are read
-// only for those sequences).
+// Position j of every sequence, decided between row passes: one CTA per
+// sequence, warp 0 merging the partials of the target row, warp 1 those of
+// the draft row (sampling) and warp 2 loading the token-side inputs.  j = 0
+// sets seq_ok[b] = 1 iff the drafted token is kept; j > 0 (the lazy
+// schedule) clears it when position j rejects, for the sequences still kept
+// (the later positions are read only for those).
 template <bool kSample>
 __global__ void __launch_bounds__(96)
     k_verify_first(const float* __restrict__ target, DraftSide ds,
                    const int32_t* __restrict__ tokens, int B, int gamma, int V, float c,
                    int n_chunks, const float* __restrict__ vmax, const float* __restrict__ vsum,
-                   const int* __restrict__ varg, Draws dr, int* __restrict__ seq_ok) {
+                   const int* __restrict__ varg, Draws dr, int j, int* __restrict__ seq_ok) {
   __shared__ RowState s_st[2];
   __shared__ PosInputs s_in;
   pdl_launch_dependents();
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int b = blockIdx.x;
   if (warp == 2) {  // inputs that do not depend on the row pass
-    if (lane == 0) s_in = load_position<kSample>(target, ds, tokens, dr, b, 0, gamma, V);
+    if (lane == 0) s_in = load_position<kSample>(target, ds, tokens, dr, b, j, gamma, V);
   }
   pdl_wait_producer();
+  if (j > 0 && seq_ok[b] == 0) return;  // rejected earlier: position j was not read
   if (warp == 0 || (kSample && warp == 1 && ds.rows != nullptr)) {
-    const int row = warp == 0 ? b * (gamma + 1) : B * (gamma + 1) + b * gamma;
+    const int row = warp == 0 ? b * (gamma + 1) + j : B * (gamma + 1) + b * gamma + j;
     const RowState st = warp_row_state<kSample>(row, n_chunks, vmax, vsum, varg, c, lane);
     if (lane == 0) s_st[warp] = st;
   }
@@ -792,7 +794,7 @@ cudaError_t launch_pdl(Kern kern, int grid, int block, cudaStream_t st, Args... 
 cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
                         const int32_t* tokens, int B, int gamma, int V, float temperature,
                         const Draws& dr, int32_t* out_tokens, int32_t* out_nacc, void* ws,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool lazy = false) {
   if (B <= 0) return cudaSuccess;
   const bool sample = temperature > 0.f;
   const bool lowrank = sample && ds.rows == nullptr;
@@ -852,20 +854,28 @@ cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
     return cudaGetLastError();
   };
   cudaError_t e;
-  if (split) {
+  auto decide_at = [&](int j) -> cudaError_t {
+    ProfScope ps(kKVerifyFirst, st);
+    return sample ? launch_pdl(k_verify_first<true>, B, 96, st, target, ds, tokens, B, gamma, V,
+                               c, n_chunks, (const float*)vmax, (const float*)vsum,
+                               (const int*)varg, dr, j, seq_ok)
+                  : launch_pdl(k_verify_first<false>, B, 96, st, target, ds, tokens, B, gamma,
+                               V, c, n_chunks, (const float*)vmax, (const float*)vsum,
+                               (const int*)varg, dr, j, seq_ok);
+  };
+  if (lazy) {
+    // position by position: each position's rows only for the sequences that
+    // kept every earlier drafted token, then that position's tests; the
+    // bonus row only for the sequences that kept all gamma
+    for (int j = 0; j <= gamma; ++j) {
+      if ((e = rows_pass(j, j, j == 0 ? nullptr : seq_ok, j > 0)) != cudaSuccess) return e;
+      if (j < gamma && (e = decide_at(j)) != cudaSuccess) return e;
+    }
+  } else if (split) {
     // position 0 of every sequence, its decision, then the rest of the
     // sequences that kept their position-0 token
     if ((e = rows_pass(0, 0, nullptr, false)) != cudaSuccess) return e;
-    {
-      ProfScope ps(kKVerifyFirst, st);
-      e = sample ? launch_pdl(k_verify_first<true>, B, 96, st, target, ds, tokens, B, gamma,
-                              V, c, n_chunks, (const float*)vmax, (const float*)vsum,
-                              (const int*)varg, dr, seq_ok)
-                 : launch_pdl(k_verify_first<false>, B, 96, st, target, ds, tokens, B,
-                              gamma, V, c, n_chunks, (const float*)vmax, (const float*)vsum,
-                              (const int*)varg, dr, seq_ok);
-      if (e != cudaSuccess) return e;
-    }
+    if ((e = decide_at(0)) != cudaSuccess) return e;
     if ((e = rows_pass(1, gamma, seq_ok, true)) != cudaSuccess) return e;
   } else {
     // greedy: a dependent launch, streaming the rows while the preceding
@@ -875,7 +885,9 @@ cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
   {
     const int rows = (sample && !lowrank) ? 2 * gamma + 1 : gamma + 1;
     const int dthreads = 32 * (std::min(16, rows) + 1);  // merging warps + a loading warp
-    const int* ok = split ? seq_ok : nullptr;
+    // (lazy: every position up to a sequence's first rejection has its
+    // partials, and the decide recomputes them all)
+    const int* ok = split && !lazy ? seq_ok : nullptr;
     ProfScope ps(kKVerifyDecide, st);
     e = sample ? launch_pdl(k_verify_decide<true>, B, dthreads, st, target, ds, tokens, B,
                             gamma, V, c, n_chunks, (const float*)vmax, (const float*)vsum,
@@ -933,13 +945,14 @@ cudaError_t verify_impl(const float* target, DraftSide ds, const void* w_up,
 
 cudaError_t launch_verify(const float* target, const float* draft, const int32_t* tokens, int B,
                           int gamma, int V, float temperature, const Draws& draws,
-                          int32_t* out_tokens, int32_t* out_nacc, void* ws, cudaStream_t st) {
+                          int32_t* out_tokens, int32_t* out_nacc, void* ws, cudaStream_t st,
+                          bool lazy) {
   DraftSide ds{};
   ds.rows = draft;
   ds.ts = gamma;
   ds.tp = 1;
   return verify_impl(target, ds, nullptr, tokens, B, gamma, V, temperature, draws, out_tokens,
-                     out_nacc, ws, st);
+                     out_nacc, ws, st, lazy);
 }
 
 cudaError_t launch_verify_lowrank(const float* target, const void* z, const void* w_up,

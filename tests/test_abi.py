@@ -116,10 +116,13 @@ def test_head_argument_errors(lib):
     assert _head(lib, M=0) == ss.SS_OK               # empty batch: nothing to do
 
 
-def test_verify_argument_errors(lib):
+@pytest.mark.parametrize("entry", ["spec_verify", "spec_verify_lazy"])
+def test_verify_argument_errors(lib, entry):
+    fn = getattr(lib, entry)
+
     def call(B=2, g=3, V=100, T=0.0, tgt=FAKE, dr=NULL, tok=FAKE, u=NULL, ot=FAKE, on=FAKE,
              ws=FAKE, wsb=1 << 20):
-        return lib.spec_verify(tgt, dr, tok, B, g, V, T, 0, 0, u, ot, on, ws, wsb, NULL)
+        return fn(tgt, dr, tok, B, g, V, T, 0, 0, u, ot, on, ws, wsb, NULL)
     E = ss.SS_ERR_INVALID_ARG
     assert call(B=-1) == E
     assert call(g=0) == E

@@ -370,3 +370,65 @@ def test_verify_lowrank_after_head_calls():
         assert np.all(got_t[b, :n] == xn[b, :n])
         verdict = check_verify_sampling(got_t[b], n, target[b], draft[b], xn[b], u[b], T)
         assert verdict is not None
+
+
+def _run_both(v, x, T, seed=5):
+    """The split and the lazy schedule on the same inputs (Philox draws at the
+    same seed and offset)."""
+    tgt = to_dev(v["target"], "f32")
+    dr = to_dev(v["draft"], "f32") if T > 0 else None
+    xd = to_dev(x, "i32")
+    a = ss.spec_verify(tgt, dr, xd, T, seed=seed, offset=3)
+    b = ss.spec_verify(tgt, dr, xd, T, seed=seed, offset=3, lazy=True)
+    torch.cuda.synchronize()
+    assert ss.ss_get_device_error() == ss.SS_OK
+    return ({k: t.cpu().numpy() for k, t in a.items()},
+            {k: t.cpu().numpy() for k, t in b.items()})
+
+
+@pytest.mark.parametrize("T", [0.0, 1.0])
+@pytest.mark.parametrize("B,g,V", [(7, 3, 1001), (64, 4, 4097), (16, 6, 40000), (4, 32, 2048)])
+def test_verify_lazy_equals_split(B, g, V, T):
+    """The lazy schedule (rows read position by position, only for the
+    sequences still kept) gives the split schedule's results bit for bit:
+    its decisions take the same partials of the same rows."""
+    v = synth.verify_logits(300 + V + g, B=B, gamma=g, V=V, kind="zipf", draft_sigma=0.5)
+    x = _drafts(v, T)
+    if T == 0.0:
+        a0 = np.argmax(v["target"][:, :g], axis=2)
+        x[::3] = a0[::3]                      # some sequences keep every position
+        x[1::3, 0] = (a0[1::3, 0] + 1) % V    # some reject position 0
+    a, b = _run_both(v, x, T)
+    np.testing.assert_array_equal(b["num_accepted"], a["num_accepted"])
+    np.testing.assert_array_equal(b["tokens"], a["tokens"])
+    if T == 0.0:
+        assert np.all(a["num_accepted"][::3] == g)
+        assert np.all(a["num_accepted"][1::3] == 0)
+
+
+@pytest.mark.parametrize("T", [0.0, 0.7])
+def test_verify_lazy_matches_oracle(T):
+    """The lazy schedule against the oracle above the split size, with
+    sequences rejected at every position."""
+    B, g, V = 24, 5, 65536
+    v = synth.verify_logits(91, B=B, gamma=g, V=V, kind="zipf", draft_sigma=0.4)
+    x = _drafts(v, T)
+    if T == 0.0:
+        a = np.argmax(v["target"][:, :g], axis=2)
+        for b in range(B):                    # sequence b keeps exactly min(b % (g+1), g) tokens
+            keep = b % (g + 1)
+            x[b, :keep] = a[b, :keep]
+            if keep < g:
+                x[b, keep] = (a[b, keep] + 1) % V
+    tgt = to_dev(v["target"], "f32")
+    dr = to_dev(v["draft"], "f32") if T > 0 else None
+    u = to_dev(v["u_verify"], "f32") if T > 0 else None
+    o = ss.spec_verify(tgt, dr, to_dev(x, "i32"), T, u, lazy=True)
+    torch.cuda.synchronize()
+    assert ss.ss_get_device_error() == ss.SS_OK
+    toks, n = o["tokens"].cpu().numpy(), o["num_accepted"].cpu().numpy()
+    c = check(v, x, T, toks, n)
+    if T == 0.0:
+        np.testing.assert_array_equal(n, [b % (g + 1) for b in range(B)])
+    else:
+        assert c["exact"] >= 0.8 * B
