@@ -51,7 +51,9 @@ static size_t head_ws_bytes(int M, int r, int V, bool bf16) {
     const MmaPlan p = mma_plan(r, M, V);
     size_t s = align256((size_t)M * r * 2);
     s += 3 * align256((size_t)M * p.n_sub * sizeof(float));
-    s += align256(2 * kMmaCtrs * sizeof(unsigned));  // tile counters of the two launches
+    // tile counters of the two launches, then the rows' best keys (greedy);
+    // the down-projection zeroes them all
+    s += align256((2 * kMmaCtrs + 2 * (size_t)M) * sizeof(unsigned));
     return s;
   }
   const HeadPlan plan = head_plan(bf16, r, M, V);
@@ -132,7 +134,7 @@ static size_t trimmed_ws_bytes(int M, int d, int Vk) {
   const MmaPlan p = mma_plan(d, M, Vk);
   if (!p.ok) return 0;
   size_t s = 3 * align256((size_t)M * p.n_sub * sizeof(float));  // sub-tile partials
-  s += align256(kMmaCtrs * sizeof(unsigned));                     // tile counters
+  s += align256((kMmaCtrs + 2 * (size_t)M) * sizeof(unsigned));  // tile counters, best keys
   return s;
 }
 
@@ -165,9 +167,11 @@ int trimmed_head_forward(const void* hidden, const void* w_kept, const int32_t* 
   wk.pmax = cv.take<float>((size_t)M * mp.n_sub);
   wk.psum = cv.take<float>((size_t)M * mp.n_sub);
   wk.parg = cv.take<int>((size_t)M * mp.n_sub);
-  unsigned* ctr = cv.take<unsigned>(kMmaCtrs);
-  // the rows of h are the tensor-core kernel's z; its tile counters start at 0
-  cudaError_t e = cudaMemsetAsync(ctr, 0, kMmaCtrs * sizeof(unsigned), stream);
+  const size_t n_ctr = kMmaCtrs + 2 * (size_t)M;  // counters, then M 64-bit best keys
+  unsigned* ctr = cv.take<unsigned>(n_ctr);
+  wk.best = reinterpret_cast<unsigned long long*>(ctr + kMmaCtrs);
+  // the rows of h are the tensor-core kernel's z; its tile counters and keys start at 0
+  cudaError_t e = cudaMemsetAsync(ctr, 0, n_ctr * sizeof(unsigned), stream);
   if (e != cudaSuccess) return cuda_status(e);
   const HeadOutputs outs{Draws{uniforms, seed, offset}, out_tokens, out_logprob, out_row_max,
                          out_row_lse, kept_ids};
@@ -210,7 +214,9 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
     wk.pmax = cv.take<float>((size_t)M * mp.n_sub);
     wk.psum = cv.take<float>((size_t)M * mp.n_sub);
     wk.parg = cv.take<int>((size_t)M * mp.n_sub);
-    unsigned* ctr = cv.take<unsigned>(2 * kMmaCtrs);
+    const int n_ctr = 2 * kMmaCtrs + 2 * M;  // counters, then M 64-bit best keys
+    unsigned* ctr = cv.take<unsigned>((size_t)n_ctr);
+    wk.best = reinterpret_cast<unsigned long long*>(ctr + 2 * kMmaCtrs);
     const HeadOutputs outs{Draws{uniforms, seed, offset}, out_tokens, out_logprob, out_row_max,
                            out_row_lse};
     // many rows of h: the down-projection as a split-K tensor-core GEMM, its
@@ -218,10 +224,10 @@ int slimspec_head_forward(const void* hidden, const void* w_down, const void* w_
     const size_t part_cap = 3 * align256((size_t)M * mp.n_sub * sizeof(float));
     const DownMmaPlan dp = M >= kDownMmaMinM ? down_mma_plan(M, d, r, part_cap) : DownMmaPlan{};
     cudaError_t e =
-        dp.ok ? launch_down_mma(dp, hidden, w_down, M, d, r, wk.pmax, z_ws, out_z, ctr,
-                                2 * kMmaCtrs, stream)
-              : launch_down_proj(bf16, hidden, w_down, M, d, r, true, z_ws, out_z, ctr,
-                                 2 * kMmaCtrs, stream);
+        dp.ok ? launch_down_mma(dp, hidden, w_down, M, d, r, wk.pmax, z_ws, out_z, ctr, n_ctr,
+                                stream)
+              : launch_down_proj(bf16, hidden, w_down, M, d, r, true, z_ws, out_z, ctr, n_ctr,
+                                 stream);
     if (e == cudaSuccess && out_logits != nullptr)
       e = launch_head_mma(mp, z_ws, w_up, M, r, V, 0.f, wk, outs, out_logits, ctr, stream);
     if (e == cudaSuccess)

@@ -187,7 +187,19 @@ struct MmaPart {
   float* pmax;  // [M][n_sub]  per 64-row vocabulary sub-tile
   float* psum;
   int* parg;
+  // greedy, when given: per row of z, atomicMax of (float_key(max) << 32 |
+  // ~index) over every thread's tiles -- the row's maximum with the lowest
+  // index among ties -- instead of the per-sub-tile partials
+  unsigned long long* best = nullptr;
 };
+
+__device__ __forceinline__ unsigned long long best_key(float v, int idx) {
+  return ((unsigned long long)float_key(v) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)idx);
+}
+// the float a float_key came from (the key maps -0 to +0)
+__device__ __forceinline__ float key_float(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
 
 // One chunk of 32 logits of a thread's row pushed into its running state.
 // Out-of-range columns (only in the last vocabulary tile) are masked to -inf.
@@ -491,6 +503,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_sub = 2 * n_tiles;
     ResidRow rr{nullptr, 0.f, 0.f, 0.f, 1};
     if (kMode == 2 && live) rr = rrows[row];
+    // greedy with best keys: each row's running key over this thread's tiles
+    const bool keys = kMode == 0 && !kSample && part.best != nullptr;
+    unsigned long long run_key[kMT];
+#pragma unroll
+    for (int mt = 0; mt < kMT; ++mt) run_key[mt] = 0ull;
     for (int i = 0;; ++i) {
       const int slot = i % kTileRing;
       bool ok = mbar_wait_bounded(&tile_full[slot], (i / kTileRing) & 1, err);
@@ -578,7 +595,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (kMode == 0 && live) {
+        if (kMode == 0 && live && keys) {
+          if (st.mx != kNegInf) {
+            const unsigned long long kk = best_key(st.mx, st.arg);
+            run_key[mt] = kk > run_key[mt] ? kk : run_key[mt];
+          }
+        } else if (kMode == 0 && live) {
           const size_t o = (size_t)row * n_sub + 2 * t + h;
           part.pmax[o] = st.mx;
           part.parg[o] = st.arg;
@@ -593,6 +615,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+    if (keys) {  // this thread's rows, once: the finish reads one key per row
+#pragma unroll
+      for (int mt = 0; mt < kMT; ++mt) {
+        const int rw = m0 + mt * kTileM + quad * 32 + lane;
+        const int mrows = mt == 0 ? Ml : Ml1;
+        if (quad * 32 + lane < mrows && run_key[mt] != 0ull) atomicMax(part.best + rw, run_key[mt]);
+      }
     }
   }
   __syncwarp();
@@ -840,6 +870,22 @@ __global__ void __launch_bounds__(kFinThreads)
                                      : 0.f;
   pdl_wait_producer();
   if (m >= M) return;
+  if (!kSample && part.best != nullptr) {
+    // the row's maximum and its lowest index, reduced by the up-projection
+    if (threadIdx.x == 0) {
+      const unsigned long long kk = __ldcg(part.best + m);
+      const float gmax = kk != 0ull ? key_float((uint32_t)(kk >> 32)) : kNegInf;
+      const int idx = (int)(0xFFFFFFFFu - (uint32_t)kk);
+      // (no key, or an index outside the vocabulary, only after an aborted
+      // up-projection: no token then, and no id-map read)
+      const bool in = kk != 0ull && idx >= 0 && idx < V;
+      out.tokens[m] = !in ? -1 : out.id_map != nullptr ? out.id_map[idx] : idx;
+      if (out.logprob) out.logprob[m] = 0.f;
+      if (out.row_max) out.row_max[m] = gmax;
+      if (out.row_lse) out.row_lse[m] = gmax;
+    }
+    return;
+  }
   const int per = (n_sub + kFinThreads - 1) / kFinThreads;
   const int j0 = min(n_sub, (int)threadIdx.x * per), nj = min(n_sub, j0 + per) - j0;
   const float* pm = part.pmax + (size_t)m * n_sub + j0;
@@ -1245,7 +1291,8 @@ cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up
   const bool sample = temperature > 0.f && scores == nullptr;
   const double inv = sample ? 1.0 / (double)temperature : 0.0;
   const float c = (float)(1.4426950408889634 * inv), inv_t = (float)inv;
-  const MmaPart part{w.pmax, w.psum, w.parg};
+  // greedy reductions use the best keys when the caller provides them
+  const MmaPart part{w.pmax, w.psum, w.parg, scores == nullptr ? w.best : nullptr};
   cudaError_t e;
   if (scores != nullptr) {
     e = launch_mma_one<false, 1>(p, z_ws, tw, tw2, M, r, V, c, part, scores, ctr, st, kind);

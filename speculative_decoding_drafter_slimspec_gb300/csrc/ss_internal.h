@@ -155,6 +155,9 @@ struct MmaWork {
   float* pmax;  // [M][n_sub]
   float* psum;
   int* parg;
+  // greedy: per row, the largest (value key, inverted index) over every CTA,
+  // zeroed with the tile counters (see k_head_mma); null: partials only
+  unsigned long long* best = nullptr;
 };
 // z_ws: M x r bf16.  With `scores` non-null the fp32 products z W_up^T are
 // written there (M x V) instead of being reduced.  ctr: the launch's kMmaCtrs
