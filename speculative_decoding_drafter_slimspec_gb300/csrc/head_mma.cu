@@ -184,13 +184,11 @@ __host__ __device__ __forceinline__ int z_bytes(int Ml, int KB) { return KB * z_
 }  // namespace
 
 struct MmaPart {
-  float* pmax;  // [M][n_sub]  per 64-row vocabulary sub-tile
+  float* pmax;  // [M][n_sub]  per 64-row vocabulary sub-tile (sampling, residual)
   float* psum;
-  int* parg;
-  // greedy, when given: per row of z, atomicMax of (float_key(max) << 32 |
-  // ~index) over every thread's tiles -- the row's maximum with the lowest
-  // index among ties -- instead of the per-sub-tile partials
-  unsigned long long* best = nullptr;
+  // greedy: per row of z, atomicMax of (float_key(max) << 32 | ~index) over
+  // every thread's tiles -- the row's maximum with the lowest index among ties
+  unsigned long long* best;
 };
 
 __device__ __forceinline__ unsigned long long best_key(float v, int idx) {
@@ -199,6 +197,21 @@ __device__ __forceinline__ unsigned long long best_key(float v, int idx) {
 // the float a float_key came from (the key maps -0 to +0)
 __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+// The greedy outputs of row m from its best key: the token (through the id
+// map of a trimmed head), log-probability 0, and the maximum as both the row's
+// maximum and its log-sum-exp (the temperature-0 limit).  No key, or an index
+// outside the vocabulary, only follows an aborted up-projection: no token then,
+// and no id-map read.
+__device__ __forceinline__ void write_greedy(const HeadOutputs& out, int V, int m,
+                                             unsigned long long kk) {
+  const float gmax = kk != 0ull ? key_float((uint32_t)(kk >> 32)) : kNegInf;
+  const int idx = (int)(0xFFFFFFFFu - (uint32_t)kk);
+  const bool in = kk != 0ull && idx >= 0 && idx < V;
+  out.tokens[m] = !in ? -1 : out.id_map != nullptr ? out.id_map[idx] : idx;
+  if (out.logprob) out.logprob[m] = 0.f;
+  if (out.row_max) out.row_max[m] = gmax;
+  if (out.row_lse) out.row_lse[m] = gmax;
 }
 
 // One chunk of 32 logits of a thread's row pushed into its running state.
@@ -503,8 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_sub = 2 * n_tiles;
     ResidRow rr{nullptr, 0.f, 0.f, 0.f, 1};
     if (kMode == 2 && live) rr = rrows[row];
-    // greedy with best keys: each row's running key over this thread's tiles
-    const bool keys = kMode == 0 && !kSample && part.best != nullptr;
+    // greedy: each row's running best key over this thread's tiles
+    constexpr bool keys = kMode == 0 && !kSample;
     unsigned long long run_key[kMT];
 #pragma unroll
     for (int mt = 0; mt < kMT; ++mt) run_key[mt] = 0ull;
@@ -595,7 +608,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
-        if (kMode == 0 && live && keys) {
+        if (keys && live) {
           if (st.mx != kNegInf) {
             const unsigned long long kk = best_key(st.mx, st.arg);
             run_key[mt] = kk > run_key[mt] ? kk : run_key[mt];
@@ -603,8 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (kMode == 0 && live) {
           const size_t o = (size_t)row * n_sub + 2 * t + h;
           part.pmax[o] = st.mx;
-          part.parg[o] = st.arg;
-          if (kSample) part.psum[o] = st.sum;
+          part.psum[o] = st.sum;
         }
         if (kMode == 2 && live) {
           const size_t o = (size_t)row * n_sub + 2 * t + h;
@@ -841,16 +853,17 @@ __device__ __forceinline__ void recompute_group(const uint8_t* __restrict__ w_up
   }
 }
 
-// One CTA of 8 warps per row of z.  Thread j owns the contiguous run of
-// sub-tile partials [j*per, (j+1)*per) in vocabulary order, per <= kFinPer,
-// loaded once into registers (all loads of the CTA in flight together).
-//   greedy: the maximum over all sub-tiles, ties to the lowest vocabulary id.
-//   sampling: the maximum g, then each thread's mass sum_s psum_s 2^((pmax_s - g)c)
-//   in order, an ordered block scan of those masses, and the thread whose
-//   run holds the crossing of u * W finds the sub-tile; the 8 warps then
-//   recompute that sub-tile's logits (8 rows each, every load issued up front,
-//   CUDA-core fp32 accumulation of the same bf16 products) and warp 0 walks
-//   them in row order.
+// Greedy: one thread per row of z reads the row's best key (the maximum and
+// its lowest vocabulary id, reduced by the up-projection) and writes the
+// outputs.  Sampling: one CTA of 8 warps per row.  Thread j owns the
+// contiguous run of sub-tile partials [j*per, (j+1)*per) in vocabulary order,
+// per <= kFinPer, loaded once into registers (all loads of the CTA in flight
+// together): the maximum g, then each thread's mass sum_s psum_s
+// 2^((pmax_s - g)c) in order, an ordered block scan of those masses, and the
+// thread whose run holds the crossing of u * W finds the sub-tile; the 8
+// warps then recompute that sub-tile's logits (8 rows each, every load issued
+// up front, CUDA-core fp32 accumulation of the same bf16 products) and warp 0
+// walks them in row order.
 template <bool kSample>
 __global__ void __launch_bounds__(kFinThreads)
     k_head_mma_finish(const uint8_t* __restrict__ w_up, const uint8_t* __restrict__ z, int M,
@@ -862,7 +875,7 @@ __global__ void __launch_bounds__(kFinThreads)
   __shared__ float s_f[3];  // W, residual mass inside the chosen sub-tile
   __shared__ int s_i[2];    // chosen thread, chosen sub-tile
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m = blockIdx.x;
+  const int m = kSample ? (int)blockIdx.x : (int)(blockIdx.x * blockDim.x + threadIdx.x);
   pdl_launch_dependents();  // the next call's down-projection may start reading
   // an input (or the counter-based stream): read before the wait
   const float u = (kSample && m < M) ? draw_uniform(out.draws.uniforms, out.draws.seed,
@@ -870,56 +883,24 @@ __global__ void __launch_bounds__(kFinThreads)
                                      : 0.f;
   pdl_wait_producer();
   if (m >= M) return;
-  if (!kSample && part.best != nullptr) {
-    // the row's maximum and its lowest index, reduced by the up-projection
-    if (threadIdx.x == 0) {
-      const unsigned long long kk = __ldcg(part.best + m);
-      const float gmax = kk != 0ull ? key_float((uint32_t)(kk >> 32)) : kNegInf;
-      const int idx = (int)(0xFFFFFFFFu - (uint32_t)kk);
-      // (no key, or an index outside the vocabulary, only after an aborted
-      // up-projection: no token then, and no id-map read)
-      const bool in = kk != 0ull && idx >= 0 && idx < V;
-      out.tokens[m] = !in ? -1 : out.id_map != nullptr ? out.id_map[idx] : idx;
-      if (out.logprob) out.logprob[m] = 0.f;
-      if (out.row_max) out.row_max[m] = gmax;
-      if (out.row_lse) out.row_lse[m] = gmax;
-    }
+  if (!kSample) {
+    write_greedy(out, V, m, __ldcg(part.best + m));
     return;
   }
   const int per = (n_sub + kFinThreads - 1) / kFinThreads;
   const int j0 = min(n_sub, (int)threadIdx.x * per), nj = min(n_sub, j0 + per) - j0;
   const float* pm = part.pmax + (size_t)m * n_sub + j0;
   const float* ps = part.psum + (size_t)m * n_sub + j0;
-  const int* pa = part.parg + (size_t)m * n_sub + j0;
   float vmx[kFinPer], vsm[kFinPer];
-  int varg[kFinPer];
 #pragma unroll
   for (int k = 0; k < kFinPer; ++k) {
     vmx[k] = k < nj ? __ldcg(pm + k) : kNegInf;
-    if (kSample) vsm[k] = k < nj ? __ldcg(ps + k) : 0.f;
-    else varg[k] = k < nj ? __ldcg(pa + k) : 0x7FFFFFFF;
+    vsm[k] = k < nj ? __ldcg(ps + k) : 0.f;
   }
   BlockArg loc{kNegInf, 0x7FFFFFFF};
 #pragma unroll
-  for (int k = 0; k < kFinPer; ++k)
-    if (vmx[k] > loc.v) {
-      loc.v = vmx[k];
-      if (!kSample) loc.i = varg[k];
-    }
-  const BlockArg best = block_argmax(loc, s_red);
-  const float gmax = best.v;
-  if (!kSample) {
-    if (threadIdx.x == 0) {
-      // (an index outside the vocabulary only comes from partials an aborted
-      // up-projection never wrote: no token then, and no id-map read)
-      const bool in = best.i >= 0 && best.i < V;
-      out.tokens[m] = !in ? -1 : out.id_map != nullptr ? out.id_map[best.i] : best.i;
-      if (out.logprob) out.logprob[m] = 0.f;
-      if (out.row_max) out.row_max[m] = gmax;
-      if (out.row_lse) out.row_lse[m] = gmax;
-    }
-    return;
-  }
+  for (int k = 0; k < kFinPer; ++k) loc.v = fmaxf(loc.v, vmx[k]);
+  const float gmax = block_argmax(loc, s_red).v;
   // this thread's masses, in order
   float mass = 0.f;
 #pragma unroll
@@ -1291,8 +1272,9 @@ cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up
   const bool sample = temperature > 0.f && scores == nullptr;
   const double inv = sample ? 1.0 / (double)temperature : 0.0;
   const float c = (float)(1.4426950408889634 * inv), inv_t = (float)inv;
-  // greedy reductions use the best keys when the caller provides them
-  const MmaPart part{w.pmax, w.psum, w.parg, scores == nullptr ? w.best : nullptr};
+  // a greedy head reduces into the rows' best keys
+  if (!sample && scores == nullptr && w.best == nullptr) return cudaErrorInvalidValue;
+  const MmaPart part{w.pmax, w.psum, w.best};
   cudaError_t e;
   if (scores != nullptr) {
     e = launch_mma_one<false, 1>(p, z_ws, tw, tw2, M, r, V, c, part, scores, ctr, st, kind);
@@ -1319,10 +1301,11 @@ cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up
     e = launch_mma_one<false, 0>(p, z_ws, tw, tw2, M, r, V, c, part, nullptr, ctr, st, kind);
   }
   if (e != cudaSuccess) return e;
-  // the per-row finish, launched to overlap the tail of the MMA grid
+  // the per-row finish, launched to overlap the tail of the MMA grid: a CTA
+  // per row when sampling, a thread per row when greedy
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(M);
-  cfg.blockDim = dim3(kFinThreads);
+  cfg.gridDim = dim3(sample ? M : (M + 31) / 32);
+  cfg.blockDim = dim3(sample ? kFinThreads : 32);
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;

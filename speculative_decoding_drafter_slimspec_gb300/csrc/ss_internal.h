@@ -152,11 +152,12 @@ cudaError_t launch_head_mma_resid(const MmaPlan& plan, const void* z, const void
                                   int r, int V, float temperature, const ResidRow* rows,
                                   float* rmass, float* pmass, unsigned* ctr, cudaStream_t st);
 struct MmaWork {
-  float* pmax;  // [M][n_sub]
+  float* pmax;  // [M][n_sub] sub-tile partials (sampling)
   float* psum;
-  int* parg;
-  // greedy: per row, the largest (value key, inverted index) over every CTA,
-  // zeroed with the tile counters (see k_head_mma); null: partials only
+  int* parg;    // [M][n_sub], unused by the head: with pmax and psum, contiguous
+                // room for the down-projection's split-K slices
+  // greedy (required then): per row, the largest (value key, inverted index)
+  // over every CTA, zeroed with the tile counters (see k_head_mma)
   unsigned long long* best = nullptr;
 };
 // z_ws: M x r bf16.  With `scores` non-null the fp32 products z W_up^T are
