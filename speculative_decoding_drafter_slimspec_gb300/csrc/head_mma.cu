@@ -76,14 +76,37 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
       : "memory");
 }
-// One box of a 4-D map (x, y, z, w) -- the wide stages' {64, 8, 4, 16} boxes.
+// The same load with an L2 cache policy (createpolicy) for the lines read.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar, uint64_t pol) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(pol)
+      : "memory");
+}
+// One box of a 4-D map (x, y, z, w) -- the wide stages' {64, 8, 4, 16} boxes --
+// with an L2 cache policy.
 __device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int x, int y, int z,
-                                            int w, uint64_t* bar) {
+                                            int w, uint64_t* bar, uint64_t pol) {
   asm volatile(
       "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)),
+      "l"(pol)
       : "memory");
+}
+// L2 policies: lines read once are evicted first, so that a stream larger
+// than L2 does not push out what was written beside it and is read next
+__device__ __forceinline__ uint64_t l2_evict_first() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_normal() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -360,6 +383,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // group goes out: a short ring (a large z) issues in pairs, a ring of wide
     // stages one at a time (one 64 KB box keeps ~80 B/clk under way).
     const int G = kWide ? 1 : (NST >= 2 * kProdGroup ? kProdGroup : 2);
+    // W_up is read once when one M tile (or every CTA both) covers z: its
+    // lines go first, and the partials, keys and z stay in L2 for the finish.
+    // With the M tiles split over CTAs the second read is meant to hit L2.
+    const uint64_t pol = m_tiles == 1 ? l2_evict_first() : l2_evict_normal();
     int it = 0;
     bool ok = true;
     // Tiles cb + k * gm (k < kStaticTiles) are this CTA's own (the first is
@@ -403,13 +430,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[s], (uint32_t)kStageBytes);
           uint8_t* dst = sB + (size_t)s * kStageBytes;
           if (!kWide) {
-            tma_load_2d(dst, &tm_w, (st0 + lane) * 64, t * kTileN, &full[s]);
+            tma_load_2d(dst, &tm_w, (st0 + lane) * 64, t * kTileN, &full[s], pol);
           } else {
             const int kb0 = (st0 + lane) * KPS;
-            if (WB > 0) tma_load_4d(dst, &tm_w, 0, 0, kb0, t * (kTileN / 8), &full[s]);
+            if (WB > 0) tma_load_4d(dst, &tm_w, 0, 0, kb0, t * (kTileN / 8), &full[s], pol);
             if (WB < KPS)  // the ragged last K block (columns past r read as zero)
               tma_load_2d(dst + (size_t)WB * kBlockBytes, &tm_w2, (kb0 + WB) * 64, t * kTileN,
-                          &full[s]);
+                          &full[s], pol);
           }
           atomicAdd(&s_fills[s], 1);
         }
