@@ -816,27 +816,16 @@ __global__ void __launch_bounds__(256)
 
 // ------------------------------------------------------------------ finish --
 // Fixed-order block reductions over the 256 threads of the finish.
-struct BlockArg {
-  float v;
-  int i;
-};
-__device__ __forceinline__ BlockArg better(BlockArg a, BlockArg b) {
-  return (b.v > a.v || (b.v == a.v && b.i < a.i)) ? b : a;  // larger value, then lower index
-}
-// Maximum (lowest index among equals) over the block; every thread gets it.
-__device__ __forceinline__ BlockArg block_argmax(BlockArg x, BlockArg* sh) {
+// Maximum over the block; every thread gets it (sh: one float per warp).
+__device__ __forceinline__ float block_max(float x, float* sh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    BlockArg y{__shfl_xor_sync(0xFFFFFFFFu, x.v, o), __shfl_xor_sync(0xFFFFFFFFu, x.i, o)};
-    x = better(x, y);
-  }
+  for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
   if (lane == 0) sh[warp] = x;
   __syncthreads();
-  BlockArg r = sh[0];
+  float r = sh[0];
 #pragma unroll
-  for (int w = 1; w < kFinThreads / 32; ++w) r = better(r, sh[w]);
-  __syncthreads();
+  for (int w = 1; w < kFinThreads / 32; ++w) r = fmaxf(r, sh[w]);
   return r;
 }
 
@@ -882,25 +871,25 @@ __device__ __forceinline__ void recompute_group(const uint8_t* __restrict__ w_up
 
 // Greedy: one thread per row of z reads the row's best key (the maximum and
 // its lowest vocabulary id, reduced by the up-projection) and writes the
-// outputs.  Sampling: one CTA of 8 warps per row.  Thread j owns the
-// contiguous run of sub-tile partials [j*per, (j+1)*per) in vocabulary order,
-// per <= kFinPer, loaded once into registers (all loads of the CTA in flight
-// together): the maximum g, then each thread's mass sum_s psum_s
-// 2^((pmax_s - g)c) in order, an ordered block scan of those masses, and the
-// thread whose run holds the crossing of u * W finds the sub-tile; the 8
-// warps then recompute that sub-tile's logits (8 rows each, every load issued
-// up front, CUDA-core fp32 accumulation of the same bf16 products) and warp 0
-// walks them in row order.
+// outputs.  Sampling: one CTA of 8 warps per row.  Warp w owns a contiguous
+// run of 32 * per sub-tile partials (per <= kFinPer), lane-interleaved and
+// loaded once into registers (all loads of the CTA in flight together): the
+// maximum g, the masses psum_s 2^((pmax_s - g)c), each warp's total over its
+// chunks of 32 in vocabulary order, the warp totals in order, and the warp
+// whose run holds the crossing of u * W walks its chunks to the sub-tile; the
+// 8 warps then recompute that sub-tile's logits (8 rows each, every load
+// issued up front, CUDA-core fp32 accumulation of the same bf16 products) and
+// warp 0 walks them in row order.
 template <bool kSample>
 __global__ void __launch_bounds__(kFinThreads)
     k_head_mma_finish(const uint8_t* __restrict__ w_up, const uint8_t* __restrict__ z, int M,
                       int r, int V, float c, float inv_t, int n_sub, MmaPart part,
                       HeadOutputs out) {
   __shared__ float s_logit[kSubW];
-  __shared__ BlockArg s_red[kFinThreads / 32];
+  __shared__ float s_max[kFinThreads / 32];
   __shared__ float s_wsum[kFinThreads / 32];
-  __shared__ float s_f[3];  // W, residual mass inside the chosen sub-tile
-  __shared__ int s_i[2];    // chosen thread, chosen sub-tile
+  __shared__ float s_f[2];  // W, residual mass inside the chosen sub-tile
+  __shared__ int s_sid;     // chosen sub-tile
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = kSample ? (int)blockIdx.x : (int)(blockIdx.x * blockDim.x + threadIdx.x);
   pdl_launch_dependents();  // the next call's down-projection may start reading
@@ -914,84 +903,110 @@ __global__ void __launch_bounds__(kFinThreads)
     write_greedy(out, V, m, __ldcg(part.best + m));
     return;
   }
+  // Warp w owns the run of sub-tiles [w*32*per, (w+1)*32*per), lane l its
+  // elements l + 32k (k < per): each load of a warp is 128 contiguous bytes,
+  // and the run is scanned chunk by chunk of 32 in vocabulary order.
   const int per = (n_sub + kFinThreads - 1) / kFinThreads;
-  const int j0 = min(n_sub, (int)threadIdx.x * per), nj = min(n_sub, j0 + per) - j0;
-  const float* pm = part.pmax + (size_t)m * n_sub + j0;
-  const float* ps = part.psum + (size_t)m * n_sub + j0;
+  const int wbase = warp * 32 * per;
+  const float* pm = part.pmax + (size_t)m * n_sub;
+  const float* ps = part.psum + (size_t)m * n_sub;
   float vmx[kFinPer], vsm[kFinPer];
 #pragma unroll
   for (int k = 0; k < kFinPer; ++k) {
-    vmx[k] = k < nj ? __ldcg(pm + k) : kNegInf;
-    vsm[k] = k < nj ? __ldcg(ps + k) : 0.f;
+    const int e = wbase + 32 * k + lane;
+    const bool in = k < per && e < n_sub;
+    vmx[k] = in ? __ldcg(pm + e) : kNegInf;
+    vsm[k] = in ? __ldcg(ps + e) : 0.f;
   }
-  BlockArg loc{kNegInf, 0x7FFFFFFF};
+  float lmax = kNegInf;
 #pragma unroll
-  for (int k = 0; k < kFinPer; ++k) loc.v = fmaxf(loc.v, vmx[k]);
-  const float gmax = block_argmax(loc, s_red).v;
-  // this thread's masses, in order
-  float mass = 0.f;
+  for (int k = 0; k < kFinPer; ++k) lmax = fmaxf(lmax, vmx[k]);
+  const float gmax = block_max(lmax, s_max);
+  // the masses, and each chunk's total as a butterfly sum (every lane gets
+  // the same value; the chunks' sums are independent and overlap)
+  float tk[kFinPer];
 #pragma unroll
   for (int k = 0; k < kFinPer; ++k) {
     vsm[k] = vsm[k] * fast_exp2((vmx[k] - gmax) * c);  // 0 past the run (0 * 2^-inf)
-    mass = __fadd_rn(mass, vsm[k]);
+    tk[k] = vsm[k];
   }
-  // ordered block scan: inclusive within the warp, then the warp totals
-  const float wincl = warp_incl_scan(mass, lane);
-  if (lane == 31) s_wsum[warp] = wincl;
-  __syncthreads();
-  float woff = 0.f, W = 0.f;
 #pragma unroll
-  for (int w = 0; w < kFinThreads / 32; ++w) {
-    if (w < warp) woff = __fadd_rn(woff, s_wsum[w]);
-    W = __fadd_rn(W, s_wsum[w]);
-  }
-  const float incl = __fadd_rn(woff, wincl);
-  const float prev = __shfl_up_sync(0xFFFFFFFFu, wincl, 1);
-  const float excl = lane > 0 ? __fadd_rn(woff, prev) : woff;
+  for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+    for (int k = 0; k < kFinPer; ++k) tk[k] = __fadd_rn(tk[k], __shfl_xor_sync(0xFFFFFFFFu, tk[k], o));
+  float wtot = 0.f;  // the chunk totals in order (those past the run are 0)
+#pragma unroll
+  for (int k = 0; k < kFinPer; ++k) wtot = __fadd_rn(wtot, tk[k]);
+  if (lane == 0) s_wsum[warp] = wtot;
+  __syncthreads();
+  // every thread: W, this warp's offset, and the crossing warp -- the first
+  // whose inclusive total passes u * W, else (the target at the very top
+  // after rounding) the last one with mass
+  float W = 0.f, woff = 0.f;
+#pragma unroll
+  for (int w = 0; w < kFinThreads / 32; ++w) W = __fadd_rn(W, s_wsum[w]);
   const float target = u * W;
-  // the first thread whose inclusive mass passes the target; else the last
-  // thread with any mass (the target sits at the very top after rounding).
-  // Both in one reduction: the key ranks hits above misses, then by thread.
-  const int hit = mass > 0.f && incl > target;
-  const BlockArg sel_r = block_argmax(
-      BlockArg{mass > 0.f ? (hit ? 2.f * kFinThreads - (float)threadIdx.x : (float)threadIdx.x)
-                          : -1.f,
-               0},
-      s_red);
-  const int sel = sel_r.v >= (float)kFinThreads ? (int)(2.f * kFinThreads - sel_r.v)
-                                                : max(0, (int)sel_r.v);
-  if (threadIdx.x == sel) {
-    // walk the run: the first sub-tile with mass whose cumulative passes the
-    // target, else (rounding) the last one with mass
-    float cum = excl, before_sid = excl, before_last = excl;
-    int sid = -1, lastpos = -1;
+  int cw = -1, lastw = 0;
+  {
+    float run = 0.f;
+#pragma unroll
+    for (int w = 0; w < kFinThreads / 32; ++w) {
+      const float t = s_wsum[w], nxt = __fadd_rn(run, t);
+      if (w == warp) woff = run;
+      if (t > 0.f && cw < 0) {
+        if (nxt > target) cw = w;
+        else lastw = w;
+      }
+      run = nxt;
+    }
+  }
+  if (cw < 0) cw = lastw;
+  if (warp == cw) {
+    // the chunk whose running total passes the target, else (rounding) the
+    // last chunk with mass; then, in it, the first element whose running
+    // total passes, else the last element with mass
+    float cum = woff, before_c = woff, last_c = woff;
+    int kc = -1, klast = 0;
 #pragma unroll
     for (int k = 0; k < kFinPer; ++k) {
-      if (k < nj && sid < 0) {
-        const float nxt = __fadd_rn(cum, vsm[k]);
-        if (vsm[k] > 0.f) {
-          if (nxt > target) {
-            sid = j0 + k;
-            before_sid = cum;
-          } else {
-            lastpos = j0 + k;
-            before_last = cum;
-          }
+      const float nxt = __fadd_rn(cum, tk[k]);
+      if (tk[k] > 0.f && kc < 0) {
+        if (nxt > target) {
+          kc = k;
+          before_c = cum;
+        } else {
+          klast = k;
+          last_c = cum;
         }
-        cum = nxt;
       }
+      cum = nxt;
     }
-    if (sid < 0) {
-      sid = lastpos >= 0 ? lastpos : j0;
-      before_sid = before_last;
+    const bool top = kc < 0;
+    if (top) {
+      kc = klast;
+      before_c = last_c;
     }
-    s_f[0] = W;
-    s_f[1] = target - before_sid;
-    s_i[1] = sid;
+    float mk = 0.f;
+#pragma unroll
+    for (int k = 0; k < kFinPer; ++k)
+      if (k == kc) mk = vsm[k];
+    const float incl = warp_incl_scan(mk, lane);
+    const float up = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
+    const float ce = lane > 0 ? __fadd_rn(before_c, up) : before_c;
+    const unsigned pos = __ballot_sync(0xFFFFFFFFu, mk > 0.f);
+    const unsigned hit =
+        __ballot_sync(0xFFFFFFFFu, mk > 0.f && __fadd_rn(before_c, incl) > target) & (top ? 0u : ~0u);
+    const int l = hit ? __ffs(hit) - 1 : pos ? 31 - __clz(pos) : 0;
+    const float before = __shfl_sync(0xFFFFFFFFu, ce, l);
+    if (lane == 0) {
+      s_f[0] = W;
+      s_f[1] = target - before;
+      s_sid = min(wbase + 32 * kc + l, n_sub - 1);
+    }
   }
   __syncthreads();
   const float resid = s_f[1];
-  const int v0 = s_i[1] * kSubW;
+  const int v0 = s_sid * kSubW;
   const int n = max(0, min(kSubW, V - v0));
   // recompute: warp w takes rows 8w .. 8w+7 of the sub-tile, lanes over K in
   // groups of 64 16-byte chunks (every load of a group issued up front); one
