@@ -108,6 +108,19 @@ __device__ __forceinline__ uint64_t l2_evict_normal() {
   asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
+// A box of a tensor map brought into L2 only (no shared memory, no barrier).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int x, int y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_4d(const CUtensorMap* map, int x, int y, int z, int w) {
+  asm volatile("cp.async.bulk.prefetch.tensor.4d.L2.global.tile [%0, {%1, %2, %3, %4}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
@@ -378,6 +391,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_w);
       if (kWide && WB < KPS) tma_prefetch_desc(&tm_w2);
+      // the static tiles' stages beyond the ring, into L2 while z is still
+      // being computed: they are read as soon as the MMAs free the ring
+      for (int q = NST; q < kStaticTiles * SPT; ++q) {
+        const int t = cb + (q / SPT) * gm;
+        if (t >= n_tiles) break;
+        const int kb0 = (q % SPT) * (kWide ? KPS : 1);
+        if (!kWide) {
+          tma_prefetch_2d(&tm_w, kb0 * 64, t * kTileN);
+        } else {
+          if (WB > 0) tma_prefetch_4d(&tm_w, 0, 0, kb0, t * (kTileN / 8));
+          if (WB < KPS) tma_prefetch_2d(&tm_w2, (kb0 + WB) * 64, t * kTileN);
+        }
+      }
     }
     // Waiting for the last of G stages leaves NST - G + 1 in flight when a
     // group goes out: a short ring (a large z) issues in pairs, a ring of wide
