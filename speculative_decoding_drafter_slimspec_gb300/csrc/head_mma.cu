@@ -906,8 +906,10 @@ __device__ __forceinline__ void recompute_group(const uint8_t* __restrict__ w_up
 // 8 warps then recompute that sub-tile's logits (8 rows each, every load
 // issued up front, CUDA-core fp32 accumulation of the same bf16 products) and
 // warp 0 walks them in row order.
+// (88 registers: the default allocation for 256 threads spilled a value;
+// 88 x 256 still leaves room beside an up-projection CTA on the same SM)
 template <bool kSample>
-__global__ void __launch_bounds__(kFinThreads)
+__global__ void __maxnreg__(88)
     k_head_mma_finish(const uint8_t* __restrict__ w_up, const uint8_t* __restrict__ z, int M,
                       int r, int V, float c, float inv_t, int n_sub, MmaPart part,
                       HeadOutputs out) {
