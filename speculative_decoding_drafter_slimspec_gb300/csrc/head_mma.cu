@@ -392,8 +392,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_w);
       if (kWide && WB < KPS) tma_prefetch_desc(&tm_w2);
       // the static tiles' stages beyond the ring, into L2 while z is still
-      // being computed: they are read as soon as the MMAs free the ring
-      for (int q = NST; q < kStaticTiles * SPT; ++q) {
+      // being computed: they are read as soon as the MMAs free the ring (at
+      // most one more ring's worth: a tile of many K blocks would otherwise
+      // bring megabytes per CTA into L2 long before they are used)
+      for (int q = NST; q < kStaticTiles * SPT && q < 2 * NST; ++q) {
         const int t = cb + (q / SPT) * gm;
         if (t >= n_tiles) break;
         const int kb0 = (q % SPT) * (kWide ? KPS : 1);
