@@ -900,7 +900,8 @@ __device__ __forceinline__ void recompute_group(const uint8_t* __restrict__ w_up
 // Greedy: one thread per row of z reads the row's best key (the maximum and
 // its lowest vocabulary id, reduced by the up-projection) and writes the
 // outputs.  Sampling: one CTA of 8 warps per row.  Warp w owns a contiguous
-// run of 32 * per sub-tile partials (per <= kFinPer), lane-interleaved and
+// run of 32 * per sub-tile partials (per <= kPer, the register arrays' size:
+// 8, 16 or kFinPer, the smallest that holds per), lane-interleaved and
 // loaded once into registers (all loads of the CTA in flight together): the
 // maximum g, the masses psum_s 2^((pmax_s - g)c), each warp's total over its
 // chunks of 32 in vocabulary order, the warp totals in order, and the warp
@@ -910,7 +911,7 @@ __device__ __forceinline__ void recompute_group(const uint8_t* __restrict__ w_up
 // warp 0 walks them in row order.
 // (88 registers: the default allocation for 256 threads spilled a value;
 // 88 x 256 still leaves room beside an up-projection CTA on the same SM)
-template <bool kSample>
+template <bool kSample, int kPer>
 __global__ void __maxnreg__(88)
     k_head_mma_finish(const uint8_t* __restrict__ w_up, const uint8_t* __restrict__ z, int M,
                       int r, int V, float c, float inv_t, int n_sub, MmaPart part,
@@ -940,9 +941,9 @@ __global__ void __maxnreg__(88)
   const int wbase = warp * 32 * per;
   const float* pm = part.pmax + (size_t)m * n_sub;
   const float* ps = part.psum + (size_t)m * n_sub;
-  float vmx[kFinPer], vsm[kFinPer];
+  float vmx[kPer], vsm[kPer];
 #pragma unroll
-  for (int k = 0; k < kFinPer; ++k) {
+  for (int k = 0; k < kPer; ++k) {
     const int e = wbase + 32 * k + lane;
     const bool in = k < per && e < n_sub;
     vmx[k] = in ? __ldcg(pm + e) : kNegInf;
@@ -950,23 +951,23 @@ __global__ void __maxnreg__(88)
   }
   float lmax = kNegInf;
 #pragma unroll
-  for (int k = 0; k < kFinPer; ++k) lmax = fmaxf(lmax, vmx[k]);
+  for (int k = 0; k < kPer; ++k) lmax = fmaxf(lmax, vmx[k]);
   const float gmax = block_max(lmax, s_max);
   // the masses, and each chunk's total as a butterfly sum (every lane gets
   // the same value; the chunks' sums are independent and overlap)
-  float tk[kFinPer];
+  float tk[kPer];
 #pragma unroll
-  for (int k = 0; k < kFinPer; ++k) {
+  for (int k = 0; k < kPer; ++k) {
     vsm[k] = vsm[k] * fast_exp2((vmx[k] - gmax) * c);  // 0 past the run (0 * 2^-inf)
     tk[k] = vsm[k];
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-    for (int k = 0; k < kFinPer; ++k) tk[k] = __fadd_rn(tk[k], __shfl_xor_sync(0xFFFFFFFFu, tk[k], o));
+    for (int k = 0; k < kPer; ++k) tk[k] = __fadd_rn(tk[k], __shfl_xor_sync(0xFFFFFFFFu, tk[k], o));
   float wtot = 0.f;  // the chunk totals in order (those past the run are 0)
 #pragma unroll
-  for (int k = 0; k < kFinPer; ++k) wtot = __fadd_rn(wtot, tk[k]);
+  for (int k = 0; k < kPer; ++k) wtot = __fadd_rn(wtot, tk[k]);
   if (lane == 0) s_wsum[warp] = wtot;
   __syncthreads();
   // every thread: W, this warp's offset, and the crossing warp -- the first
@@ -998,7 +999,7 @@ __global__ void __maxnreg__(88)
     float cum = woff, before_c = woff, last_c = woff;
     int kc = -1, klast = 0;
 #pragma unroll
-    for (int k = 0; k < kFinPer; ++k) {
+    for (int k = 0; k < kPer; ++k) {
       const float nxt = __fadd_rn(cum, tk[k]);
       if (tk[k] > 0.f && kc < 0) {
         if (nxt > target) {
@@ -1018,7 +1019,7 @@ __global__ void __maxnreg__(88)
     }
     float mk = 0.f;
 #pragma unroll
-    for (int k = 0; k < kFinPer; ++k)
+    for (int k = 0; k < kPer; ++k)
       if (k == kc) mk = vsm[k];
     const float incl = warp_incl_scan(mk, lane);
     const float up = __shfl_up_sync(0xFFFFFFFFu, incl, 1);
@@ -1385,11 +1386,18 @@ cudaError_t launch_head_mma(const MmaPlan& p, const void* z_ws, const void* w_up
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   ProfScope ps(kKHeadFinish, st);
-  if (sample)
-    e = cudaLaunchKernelEx(&cfg, k_head_mma_finish<true>, (const uint8_t*)w_up,
+  const int per = (p.n_sub + kFinThreads - 1) / kFinThreads;  // <= kFinPer (the plan checks)
+  if (!sample)
+    e = cudaLaunchKernelEx(&cfg, k_head_mma_finish<false, 8>, (const uint8_t*)w_up,
+                           (const uint8_t*)z_ws, M, r, V, c, inv_t, p.n_sub, part, out);
+  else if (per <= 8)
+    e = cudaLaunchKernelEx(&cfg, k_head_mma_finish<true, 8>, (const uint8_t*)w_up,
+                           (const uint8_t*)z_ws, M, r, V, c, inv_t, p.n_sub, part, out);
+  else if (per <= 16)
+    e = cudaLaunchKernelEx(&cfg, k_head_mma_finish<true, 16>, (const uint8_t*)w_up,
                            (const uint8_t*)z_ws, M, r, V, c, inv_t, p.n_sub, part, out);
   else
-    e = cudaLaunchKernelEx(&cfg, k_head_mma_finish<false>, (const uint8_t*)w_up,
+    e = cudaLaunchKernelEx(&cfg, k_head_mma_finish<true, kFinPer>, (const uint8_t*)w_up,
                            (const uint8_t*)z_ws, M, r, V, c, inv_t, p.n_sub, part, out);
   return e != cudaSuccess ? e : cudaGetLastError();
 }

@@ -215,6 +215,16 @@ def test_head_many_rows_split_k_down_projection(seed, M, d, r, V, T):
     assert counts["exact"] >= M - 2
 
 
+# -------------------------------------------- sampling finish, run sizes ---
+# The sampling finish keeps each warp's run of sub-tile partials in registers,
+# in arrays of 8, 16 or 24 per lane chosen by ceil(n_sub / 256), n_sub =
+# 2 * ceil(V / 128): these vocabularies give runs of 1, 10 and 19.
+@pytest.mark.parametrize("V", [2000, 150000, 300000])
+@pytest.mark.parametrize("T", [0.7, 1.0])
+def test_head_sampling_finish_run_sizes(V, T):
+    run_case(40 + V % 97, 3, 128, 64, V, "bf16", T, logits=False)
+
+
 # ------------------------------------------------- position-adaptive rank ---
 @pytest.mark.parametrize("r", [384, 640, 768, 896, 1024, 2048])
 @pytest.mark.parametrize("T", [0.0, 1.0])
