@@ -15,7 +15,8 @@
 //               hands their ids to the other warps through a small ring in
 //               shared memory,
 //               and loads W_up (B, one 64-wide K block of a tile per 16 KB
-//               stage, 128B-swizzled) with TMA.  One issuing thread keeps only
+//               stage, or several as one 4-D box, 128B-swizzled) with TMA,
+//               L2 evict-first.  One issuing thread keeps only
 //               about one box per 800 cycles under way, short of this SM's
 //               share of HBM bandwidth, so lane 0 waits for a group of up to
 //               four free stages and that many lanes issue together.
@@ -27,9 +28,11 @@
 //               loads, in the 128B-swizzled layout, so that it does not queue
 //               behind the W_up boxes already in flight.  Then, per tile,
 //               tcgen05.ld of 32 columns at a time; every thread owns one row
-//               of z and reduces each 64-row sub-tile to one partial
-//               (max, sum of exp, argmax), written to workspace (or, in the
-//               scores mode, writes the fp32 values out)
+//               of z.  Sampling: each 64-row sub-tile reduced to one partial
+//               (max, sum of exp) in workspace.  Greedy: one running key of
+//               the row's maximum and its lowest index, added with a 64-bit
+//               atomicMax at the end.  (The scores mode writes the fp32
+//               values out.)
 //
 // z is stored compactly: a 128-row tile of z with only M' live rows keeps
 // ceil(M'/8) swizzle atoms (8 rows x 128 bytes) per K block.  The MMA still
@@ -37,9 +40,10 @@
 // memory and only reach rows of D that nothing reads.  For a few rows of z
 // this frees almost all of shared memory for W_up stages.
 //
-// k_head_mma_finish then reduces the partials, one CTA per row of z, in
-// vocabulary order: greedy argmax, or the inverse-CDF draw with the one
-// sub-tile it lands in recomputed on CUDA cores.
+// k_head_mma_finish then writes the outputs: greedy, one thread per row of z
+// from its key; sampling, one CTA per row reduces the partials in vocabulary
+// order to the inverse-CDF draw, the one sub-tile it lands in recomputed on
+// CUDA cores.
 #include <cuda.h>  // CUtensorMap and its enums; the encoder is fetched at run time
 
 #include <algorithm>
@@ -308,7 +312,8 @@ __device__ __forceinline__ void epi_chunk(const uint32_t (&v)[32], int vid0, int
 // gridDim.x / m_tiles CTAs of it (their own tile counter).  With two M tiles
 // each W_up tile is then read by two CTAs (the second read mostly from L2);
 // the dual plan below instead keeps both tiles of z in every CTA, when three
-// W_up stages still fit beside them, so that each SM takes W_up in once.  kMode 0: softmax partials; kMode 1: the fp32 scores
+// W_up stages still fit beside them, so that each SM takes W_up in once.  kMode 0: softmax
+// partials (sampling) or best keys (greedy); kMode 1: the fp32 scores
 // D[m, v] are written to out_scores (M x V); kMode 2: the residual masses of
 // a verified sequence's final draw (ResidRow), the target values of each
 // tile loaded ahead of its accumulator, into part.pmax (residual) and
